@@ -1,0 +1,428 @@
+#!/usr/bin/env python3
+"""Benchmark of the hybrid-attention decode hot path on GB300 (one JSON line on rank 0).
+
+Workload (default, `decode_single_layer`): 32 requests, H=32, D=128, bf16 KV, fp32 linear
+state, seq_lens ~ U{128..4096} with blocks shuffled across a pool; one step = one decode
+token for every request through one Full layer (slot mapping, KV append, split-K paged
+decode) and one Linear layer (in-place state step). Metric: req-tokens/s per layer
+= B * layers / step time. Inputs live in HBM before timing; the per-step working set
+(~1.2 GB of KV and 128 MiB of state) is far larger than L2, so no flush is needed.
+
+`value` is device time (CUDA events on the launching stream). `e2e` is the same step
+through the public dispatcher (hyb_layer_dispatch) with the step's q/k/v and metadata
+copied from pinned host memory and the outputs copied back, inside the timed region.
+`--impl reference` times the CPU oracle instead (bounded sample per step, host cores).
+With torchrun (N > 1) every rank runs its own replica (the path shards by request with
+no exchange) and rank 0 reports the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as W  # noqa: E402
+
+METRIC = "hybrid attn decode req-tokens/s per layer; HBM GB/s and % of GB300 roofline"
+UNIT = "req-tokens/s per layer"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2500)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ distributed
+class Dist:
+    def __init__(self, n):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")       # timing barrier / max only; no data exchange
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples during the timed region (SM clock, throttle reasons)."""
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.idx)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, which):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        rows = [l for (t, l) in self.lines if self.t0 and self.t1 and self.t0 - 0.15 <= t <= self.t1 + 0.15]
+        if not rows:
+            rows = [l for (_, l) in self.lines]
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            f = [x.strip() for x in r.split(",")]
+            if len(f) < 10:
+                continue
+            try:
+                sm.append(float(f[2]))
+                mx = float(f[3])
+            except ValueError:
+                continue
+            for name, val in zip(names, f[6:10]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ peaks
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    return 6800.0, 1900.0, "fallback"
+
+
+def traffic_record(kernel: str, src: str):
+    """ncu dram bytes per launch recorded under profiles/, valid only while the kernel
+    source is unchanged since the capture (sha256 of the .cu file)."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        rec = json.load(f).get(kernel)
+    if not rec:
+        return None
+    with open(os.path.join(ROOT, "paged_kv_linear_gb300", "csrc", src), "rb") as f:
+        if hashlib.sha256(f.read()).hexdigest() != rec.get("source_sha256"):
+            return None
+    return rec
+
+
+# ------------------------------------------------------------------ workload
+def build_workload(seed, device):
+    import torch
+    db = W.decode_single_layer(seed)
+    B, H, D, NB, MB = db.B, db.H, db.D, db.pool.num_blocks, db.pool.max_blocks
+    g = W.rng(seed + 1)
+    wl = dict(db=db, B=B, H=H, D=D, NB=NB, MB=MB)
+    wl["kc"] = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), seed * 10 + 1, D)
+    wl["vc"] = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), seed * 10 + 2, D)
+    wl["state"] = W.device_state_(torch.empty((B, H, D, D), device=device), seed * 10 + 3, db.seq_lens, D)
+    wl["host"] = {n: W.rows(g, (B, H, D), D, W.BF16) for n in ("qf", "kf", "vf", "ql", "kl", "vl")}
+    wl["slots_h"] = g.permutation(B).astype(np.int32)
+    return wl
+
+
+def bench_ours(args, dist):
+    import torch
+    from paged_kv_linear_gb300 import _build
+    if dist.rank == 0 or dist.world == 1:
+        _build.build()
+    dist.barrier()
+    _build.build()
+    import paged_kv_linear_gb300 as hyb
+
+    torch.cuda.set_device(dist.local)
+    device = torch.device("cuda", dist.local)
+    wl = build_workload(args.seed + dist.rank, device)
+    B, H, D, NB, MB, db = wl["B"], wl["H"], wl["D"], wl["NB"], wl["MB"], wl["db"]
+    d = hyb.dims(H, D, NB, MB, W.BF16)
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else a).to(device)
+    bf = lambda a: dev(a).view(torch.bfloat16) if a.dtype == np.uint16 else dev(a)
+    x = {n: bf(a) for n, a in wl["host"].items()}
+    bt = dev(db.pool.block_tables)
+    lens = dev(db.seq_lens)
+    ctx = dev(db.seq_lens - 1)
+    cu = dev(np.arange(B + 1, dtype=np.int32))
+    slots = dev(wl["slots_h"])
+    slot = torch.empty(B, dtype=torch.int64, device=device)
+    msl = int(db.seq_lens.max())
+    ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, msl, d)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=device)
+    out_f = torch.empty((B, H, D), dtype=torch.bfloat16, device=device)
+    out_l = torch.empty_like(out_f)
+    stream = torch.cuda.Stream(device=device)
+    sh = stream.cuda_stream
+    L = 2
+    n_ops = 4
+    names = ["slot_mapping", "kv_append", "paged_decode", "linear_step"]
+
+    def step(ev=None):
+        if ev: ev[0].record(stream)
+        hyb.check(hyb.hyb_slot_mapping(slot, bt, cu, ctx, B, B, d, sh))
+        if ev: ev[1].record(stream)
+        hyb.check(hyb.hyb_paged_kv_append(x["kf"], x["vf"], slot, B, wl["kc"], wl["vc"], d, sh))
+        if ev: ev[2].record(stream)
+        hyb.check(hyb.hyb_paged_attn_decode(out_f, x["qf"], wl["kc"], wl["vc"], bt, lens, B, msl, d, ws, ws_n, sh))
+        if ev: ev[3].record(stream)
+        hyb.check(hyb.hyb_linear_attn_step(out_l, x["ql"], x["kl"], x["vl"], wl["state"], B, slots, B, H, D, W.BF16, sh))
+        if ev: ev[4].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(n_ops + 1)] for _ in range(args.steps)]
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    time.sleep(0.3)
+    dist.barrier()
+    torch.cuda.synchronize()
+    hyb.hyb_launch_count(reset=True)
+    clocks.mark("t0")
+    with torch.cuda.stream(stream):
+        for s in range(args.steps):
+            step(evs[s])
+    torch.cuda.synchronize()
+    clocks.mark("t1")
+    launches = hyb.hyb_launch_count(reset=True)
+    dist.barrier()
+    clocks.stop()
+    per_op = np.zeros(n_ops)
+    total_ms = 0.0
+    for e in evs:
+        total_ms += e[0].elapsed_time(e[n_ops])
+        for i in range(n_ops):
+            per_op[i] += e[i].elapsed_time(e[i + 1])
+    per_op /= args.steps
+    ms_step = dist.max(total_ms / args.steps)
+    units = dist.sum(B * L)                       # request-tokens per layer-step over all ranks
+    value = units / (ms_step * 1e-3)
+    st, flags = hyb.hyb_device_status(clear=True)
+    if st != 0:
+        raise RuntimeError(f"device-side check flags {flags:#x}")
+
+    # ---- roofline of the dominant kernel (paged decode: split-K kernel + combine)
+    hbm_peak, tf_peak, peak_kind = measured_peaks()
+    tokens = int(db.seq_lens.sum())
+    alg_bytes = tokens * H * D * 2 * 2 + 2 * B * H * D * 2          # K+V read, q read, out write
+    achieved = alg_bytes / (per_op[2] * 1e-3) / 1e9
+    trec = traffic_record("paged_decode", "decode.cu")
+    roofline = {"kernel": "paged_decode (split-K + combine)", "bound": "hbm", "achieved": round(achieved, 1),
+                "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+                "traffic": (int(trec["bytes_per_launch"]) if trec else None),
+                "algorithmic_bytes": alg_bytes, "peak_source": f"{peak_kind} hbm_gbs"}
+    lin_bytes = B * H * D * D * 4 * 2
+    ops = {n: {"ms": round(float(t), 5)} for n, t in zip(names, per_op)}
+    ops["paged_decode"]["GB/s"] = round(achieved, 1)
+    ops["linear_step"]["GB/s"] = round(lin_bytes / (per_op[3] * 1e-3) / 1e9, 1)
+    ops["linear_step"]["frac"] = round(ops["linear_step"]["GB/s"] / hbm_peak, 4)
+
+    # ---- end to end through the public dispatcher, host buffers, copies timed
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else np.ascontiguousarray(a)).pin_memory()
+    h_in = {n: pin(a) for n, a in wl["host"].items()}
+    h_meta = {"lens": pin(db.seq_lens), "bt": pin(db.pool.block_tables), "ctx": pin(db.seq_lens - 1),
+              "slots": pin(wl["slots_h"]), "cu": pin(np.arange(B + 1, dtype=np.int32))}
+    d_in = {n: torch.empty(t.shape, dtype=t.dtype, device=device) for n, t in h_in.items()}
+    d_meta = {n: torch.empty(t.shape, dtype=t.dtype, device=device) for n, t in h_meta.items()}
+    h_out = [torch.empty((B, H, D), dtype=torch.int16).pin_memory() for _ in range(2)]
+    h2d = sum(t.numel() * t.element_size() for t in list(h_in.values()) + list(h_meta.values()))
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+    meta = hyb.batch_meta(B, B, seq_lens=d_meta["lens"], block_tables=d_meta["bt"], slot_mapping=slot,
+                          state_slots=d_meta["slots"], max_seq_len=msl)
+    bfv = lambda t: t.view(torch.bfloat16)
+    ios = [hyb.layer_io(out_f, bfv(d_in["qf"]), bfv(d_in["kf"]), bfv(d_in["vf"]), wl["kc"], wl["vc"]),
+           hyb.layer_io(out_l, bfv(d_in["ql"]), bfv(d_in["kl"]), bfv(d_in["vl"]), state_pool=wl["state"], num_state_slots=B)]
+
+    def e2e_step():
+        for n in h_in:
+            d_in[n].copy_(h_in[n], non_blocking=True)
+        for n in h_meta:
+            d_meta[n].copy_(h_meta[n], non_blocking=True)
+        hyb.check(hyb.hyb_slot_mapping(slot, d_meta["bt"], d_meta["cu"], d_meta["ctx"], B, B, d, sh))
+        hyb.check(hyb.hyb_layer_dispatch([0, 1], 2, 0, ios, meta, d, 64, ws, ws_n, sh))
+        h_out[0].copy_(out_f.view(torch.int16), non_blocking=True)
+        h_out[1].copy_(out_l.view(torch.int16), non_blocking=True)
+
+    e2e_steps = max(10, min(args.steps, 500))
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            e2e_step()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        dist.barrier()
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        stream.synchronize()
+    e2e_ms = dist.max(e0.elapsed_time(e1) / e2e_steps)
+    e2e_val = units / (e2e_ms * 1e-3)
+
+    # ---- CPU oracle beside it (rank 0, N = 1 only)
+    cpu = None
+    if dist.world == 1:
+        cpu = cpu_baseline_decode(wl, budget_s=15.0)
+
+    return {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dist.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1)/sqrt(D) q/k/v, shuffled block pool, N(0,seq/D^2) states)",
+        "config": {"workload": "decode_single_layer: 32 requests, H=32, D=128, block 16, seq_lens U{128..4096}, "
+                               "1 Full paged-decode + 1 Linear step", "B": B, "H": H, "D": D,
+                   "layers": ["full", "linear"], "kv_tokens": tokens, "pool_blocks": NB,
+                   "l2": "no flush: per-step working set %.2f GB > 129 MB L2" % ((alg_bytes + lin_bytes) / 1e9),
+                   "parallelism": f"replicas x{dist.world}"},
+        "roofline": roofline, "ops": ops,
+        "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "path": "hyb_slot_mapping + hyb_layer_dispatch, pinned host I/O"},
+        "gpu_launches": int(launches),
+        "clocks": clocks.summary(),
+        "cpu_baseline": cpu,
+    }
+
+
+def cpu_baseline_decode(wl, budget_s=15.0, requests=None):
+    """Times the CPU oracle (as it stands) on a bounded sample of the same workload: whole
+    requests through the Full-layer decode and the Linear step, all heads."""
+    import oracle
+    db = wl["db"]
+    H, D = wl["H"], wl["D"]
+    cores = oracle.set_threads(0)
+    kc = wl["kc"].cpu().view(__import__("torch").int16).numpy().view(np.uint16)
+    vc = wl["vc"].cpu().view(__import__("torch").int16).numpy().view(np.uint16)
+    st = wl["state"].cpu().numpy()
+    hq = wl["host"]
+    done, t_used = 0, 0.0
+    order = list(range(wl["B"])) if requests is None else list(requests)
+    for b in order:
+        t0 = time.perf_counter()
+        oracle.full_decode(hq["qf"][b:b + 1], kc, vc, db.pool.block_tables[b:b + 1], db.seq_lens[b:b + 1], D ** -0.5)
+        oracle.linear_step(hq["ql"][b:b + 1], hq["kl"][b:b + 1], hq["vl"][b:b + 1], st, wl["slots_h"][b:b + 1])
+        t_used += time.perf_counter() - t0
+        done += 1
+        if t_used > budget_s:
+            break
+    return {"value": round(done * 2 / t_used, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} of {wl['B']} requests (all {H} heads; Full decode + Linear step), fp64 C oracle, "
+                      f"{t_used:.1f} s"}
+
+
+def bench_reference(args, dist):
+    """The CPU oracle as the reference arm: each step is one request (rotating through the
+    batch) through both layers, on the host cores."""
+    if dist.rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    db = W.decode_single_layer(args.seed)
+    g = W.rng(args.seed + 1)
+    B, H, D = db.B, db.H, db.D
+    cores = oracle.set_threads(0)
+    # pool contents for the sampled requests only (host-drawn, same shapes)
+    kc = np.empty((db.pool.num_blocks, H, 16, D), np.uint16)
+    vc = np.empty_like(kc)
+    gk = W.rng(args.seed + 7)
+    kc[:] = W.rows(gk, kc.shape, D, W.BF16)
+    vc[:] = W.rows(gk, vc.shape, D, W.BF16)
+    st = W.synthetic_state(g, B, H, D, db.seq_lens)
+    q, k, v = (W.rows(g, (B, H, D), D, W.BF16) for _ in range(3))
+    slots = np.arange(B, dtype=np.int32)
+
+    def one(b):
+        oracle.full_decode(q[b:b + 1], kc, vc, db.pool.block_tables[b:b + 1], db.seq_lens[b:b + 1], D ** -0.5)
+        oracle.linear_step(q[b:b + 1], k[b:b + 1], v[b:b + 1], st, slots[b:b + 1])
+
+    for i in range(args.warmup):
+        one(i % B)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        one(i % B)
+    dt = time.perf_counter() - t0
+    ms = dt * 1e3 / args.steps
+    val = 2 / (ms * 1e-3)
+    return {"impl": "reference", "metric": METRIC, "value": round(val, 2), "unit": UNIT, "n_gpus": dist.world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": "decode_single_layer: 32 requests, H=32, D=128, block 16, seq_lens U{128..4096}, "
+                                   "1 Full paged-decode + 1 Linear step", "sample_per_step": "1 request, all heads"},
+            "cpu_baseline": {"value": round(val, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+                             "sample": "1 request per step (rotating over the 32), all 32 heads, Full decode + Linear step"},
+            "e2e": {"value": round(val, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main():
+    args = parse()
+    dist = Dist(args.gpus)
+    if args.impl == "reference":
+        res = bench_reference(args, dist)
+    else:
+        res = bench_ours(args, dist)
+    if dist.rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if dist.pg:
+        dist.pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,371 @@
+// Paged decode attention: split-K online softmax over 16-token KV blocks.
+//
+// Page: "推理框架适配Hybrid Model：KV Cache管理与算子调度实战", §2.3 (decode uses a
+// PagedAttention-type kernel reading K/V through the block table) and §2.1 (a decode
+// step of a Full layer costs O(S x D) and the KV cache is the bandwidth hog).
+//
+// Design (GB300): the work is pure HBM streaming -- every (block, head) K and V tile is
+// a contiguous 16 x D run of the [NB][H][16][D] pool (4 KiB each at D=128, bf16), read
+// once. A CTA owns one (row, head, split) and 4 warps; each warp walks every 4th block of
+// the split through its own 3-stage ring in shared memory, filled by the TMA engine
+// (cp.async.bulk, one 4 KiB copy per tile, completion on an mbarrier). Scores and the
+// online softmax run in fp32 on the CUDA cores with warp shuffles; partial states
+// (m, l, acc[D]) of the 4 warps merge in shared memory, and splits merge in a second
+// small kernel (log-sum-exp combine). The split size is a constant number of blocks, so
+// a request's result does not depend on the rest of the batch.
+//
+// The same kernel serves as the CUDA-core causal prefill for shapes without a
+// tensor-core kernel (PREFILL = true: one row per packed query token, n = position + 1).
+#include <cuda_bf16.h>
+
+#include "hyb_internal.cuh"
+
+namespace hyb {
+
+namespace {
+
+constexpr int kNW = 4;           // warps per CTA
+constexpr int kNST = 3;          // ring stages per warp
+constexpr int kBPS = 32;         // KV blocks per split (constant: batch-invariant results)
+
+template <typename T>
+struct Elt;
+template <>
+struct Elt<__nv_bfloat16> {
+  static constexpr int VEC = 8;
+  __device__ static void unpack(const uint4& u, float* f) {
+    f[0] = bf16_lo(u.x); f[1] = bf16_hi(u.x); f[2] = bf16_lo(u.y); f[3] = bf16_hi(u.y);
+    f[4] = bf16_lo(u.z); f[5] = bf16_hi(u.z); f[6] = bf16_lo(u.w); f[7] = bf16_hi(u.w);
+  }
+  __device__ static void store(__nv_bfloat16* p, float x) { *p = __float2bfloat16_rn(x); }
+};
+template <>
+struct Elt<float> {
+  static constexpr int VEC = 4;
+  __device__ static void unpack(const uint4& u, float* f) {
+    f[0] = __uint_as_float(u.x); f[1] = __uint_as_float(u.y);
+    f[2] = __uint_as_float(u.z); f[3] = __uint_as_float(u.w);
+  }
+  __device__ static void store(float* p, float x) { *p = x; }
+};
+
+// Length handled for a row after host/device bound checks (identical in both kernels).
+__device__ __forceinline__ int clamp_len(int n, int max_len, int MB) {
+  n = n < 0 ? 0 : n;
+  n = n > max_len ? max_len : n;
+  const int cap = MB * kBlockSize;
+  return n > cap ? cap : n;
+}
+
+template <typename T, int D>
+struct DecodeShape {
+  static constexpr int VEC = Elt<T>::VEC;
+  static constexpr int LPR = D / VEC;          // lanes covering one token row
+  static constexpr int TPI = 32 / LPR;         // token rows per warp load
+  static constexpr int ITER = kBlockSize / TPI;
+  static constexpr int TILE = kBlockSize * D * (int)sizeof(T);
+  static constexpr int SMEM = kNW * kNST * 2 * TILE + kNW * kNST * 8 + kNW * (D + 2) * 4;
+  static_assert(LPR >= 2 && LPR <= 32 && ITER >= 1, "unsupported head_dim");
+};
+
+template <typename T, int D, bool PREFILL>
+__global__ void __launch_bounds__(kNW * 32)
+paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __restrict__ kc,
+                    const T* __restrict__ vc, const int32_t* __restrict__ bt,
+                    const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu,
+                    const int32_t* __restrict__ ctx, int max_q, int H, int NB, int MB,
+                    int max_len, float scale_log2, int max_splits, float* __restrict__ ws_acc,
+                    float2* __restrict__ ws_ml, unsigned* status) {
+  using E = Elt<T>;
+  using S = DecodeShape<T, D>;
+  constexpr int VEC = S::VEC, LPR = S::LPR, TPI = S::TPI, ITER = S::ITER, TILE = S::TILE;
+
+  const int h = blockIdx.y, split = blockIdx.z;
+  int b, r, n_raw;                         // request, packed row of q/out, keys to attend
+  if (PREFILL) {                           // grid.x = B * max_q: (request, query index)
+    b = blockIdx.x / max_q;
+    const int j = blockIdx.x - b * max_q;
+    if (j >= cu[b + 1] - cu[b]) return;
+    r = cu[b] + j;
+    n_raw = (ctx ? ctx[b] : 0) + j + 1;
+  } else {
+    b = r = blockIdx.x;
+    n_raw = seq_lens[r];
+  }
+  const int n = clamp_len(n_raw, max_len, MB);
+  if (n != (n_raw < 0 ? 0 : n_raw) && split == 0 && threadIdx.x == 0)
+    flag(status, n_raw > max_len ? HYB_DEVERR_BAD_LENGTH : HYB_DEVERR_BAD_BLOCK);
+  const int nblk = (n + kBlockSize - 1) / kBlockSize;
+  const int nsplit = max(1, (nblk + kBPS - 1) / kBPS);
+  if (split >= nsplit) return;
+  const int blk_begin = split * kBPS, blk_end = min(nblk, blk_begin + kBPS);
+
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = smem + (size_t)warp * kNST * 2 * TILE;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kNW * kNST * 2 * TILE) + warp * kNST;
+  float* red_acc = reinterpret_cast<float*>(smem + (size_t)kNW * kNST * 2 * TILE + kNW * kNST * 8);
+  float* red_ml = red_acc + kNW * D;
+
+  const int c = lane % LPR, rr = lane / LPR;
+  float qf[VEC];
+  {
+    const uint4 u = *reinterpret_cast<const uint4*>(q + ((int64_t)r * H + h) * D + c * VEC);
+    E::unpack(u, qf);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) qf[e] *= scale_log2;
+  }
+
+  const int first = blk_begin + warp;   // this warp's logical blocks: first + i*kNW
+  const int ntiles = first < blk_end ? (blk_end - first + kNW - 1) / kNW : 0;
+  const int32_t* btrow = bt + (int64_t)b * MB;
+  const int64_t head_off = (int64_t)h * kBlockSize * D;
+  const int64_t blk_stride = (int64_t)H * kBlockSize * D;
+
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < kNST; ++s) mbar_init(&bars[s], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+
+  auto issue = [&](int i) {              // lane 0 only
+    const int pb = btrow[first + i * kNW];
+    if (pb < 0 || pb >= NB) return;      // the consumer flags and skips it
+    const int st = i % kNST;
+    uint8_t* dst = ring + st * 2 * TILE;
+    mbar_expect_tx(&bars[st], 2 * TILE);
+    bulk_g2s(dst, kc + pb * blk_stride + head_off, TILE, &bars[st]);
+    bulk_g2s(dst + TILE, vc + pb * blk_stride + head_off, TILE, &bars[st]);
+  };
+  if (lane == 0)
+    for (int i = 0; i < min(kNST, ntiles); ++i) issue(i);
+
+  float m = -INFINITY, l = 0.f, acc[VEC];
+#pragma unroll
+  for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+  uint32_t phase = 0;
+  int failed_at = -1;
+
+  for (int i = 0; i < ntiles; ++i) {
+    const int st = i % kNST;
+    const int pb = btrow[first + i * kNW];
+    if (pb < 0 || pb >= NB) {
+      if (lane == 0) flag(status, HYB_DEVERR_BAD_BLOCK);
+    } else {
+      if (!mbar_wait(&bars[st], (phase >> st) & 1u)) {
+        failed_at = i;
+        break;
+      }
+      phase ^= 1u << st;
+      const T* Ks = reinterpret_cast<const T*>(ring + st * 2 * TILE);
+      const T* Vs = reinterpret_cast<const T*>(ring + st * 2 * TILE + TILE);
+      const int tok0 = (first + i * kNW) * kBlockSize;
+      float s[ITER];
+      float mt = -INFINITY;
+#pragma unroll
+      for (int it = 0; it < ITER; ++it) {
+        const int tk = rr + it * TPI;
+        float kf[VEC];
+        E::unpack(*reinterpret_cast<const uint4*>(Ks + tk * D + c * VEC), kf);
+        float d = 0.f;
+#pragma unroll
+        for (int e = 0; e < VEC; ++e) d = fmaf(qf[e], kf[e], d);
+#pragma unroll
+        for (int o = LPR / 2; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+        s[it] = (tok0 + tk < n) ? d : -INFINITY;
+        mt = fmaxf(mt, s[it]);
+      }
+#pragma unroll
+      for (int o = LPR; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
+      const float m_new = fmaxf(m, mt);  // finite: a tile's first token is always < n
+      const float alpha = fast_exp2(m - m_new);
+      float ls = 0.f;
+#pragma unroll
+      for (int e = 0; e < VEC; ++e) acc[e] *= alpha;
+#pragma unroll
+      for (int it = 0; it < ITER; ++it) {
+        const int tk = rr + it * TPI;
+        const float p = fast_exp2(s[it] - m_new);
+        ls += p;
+        if (tok0 + tk < n) {             // rows past the sequence may hold anything (NaN)
+          float vf[VEC];
+          E::unpack(*reinterpret_cast<const uint4*>(Vs + tk * D + c * VEC), vf);
+#pragma unroll
+          for (int e = 0; e < VEC; ++e) acc[e] = fmaf(p, vf[e], acc[e]);
+        }
+      }
+#pragma unroll
+      for (int o = LPR; o < 32; o <<= 1) ls += __shfl_xor_sync(0xffffffffu, ls, o);
+      l = l * alpha + ls;
+      m = m_new;
+    }
+    __syncwarp();
+    if (lane == 0 && i + kNST < ntiles) issue(i + kNST);
+  }
+
+  if (failed_at >= 0) {
+    // A wait expired: report, then let the copies still in flight land before exiting.
+    if (lane == 0) {
+      flag(status, HYB_DEVERR_TIMEOUT);
+      for (int j = failed_at; j < min(failed_at + kNST, ntiles); ++j) {
+        const int pb = btrow[first + j * kNW];
+        if (pb >= 0 && pb < NB) {
+          const int st = j % kNST;
+          mbar_wait(&bars[st], (phase >> st) & 1u, 100000000ull);
+          phase ^= 1u << st;
+        }
+      }
+    }
+    __syncwarp();
+    m = -INFINITY; l = 0.f;
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
+  }
+
+  // merge the token sub-rows of the warp (lanes with the same c)
+#pragma unroll
+  for (int o = LPR; o < 32; o <<= 1)
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], o);
+  if (lane < LPR)
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) red_acc[warp * D + c * VEC + e] = acc[e];
+  if (lane == 0) {
+    red_ml[2 * warp] = m;
+    red_ml[2 * warp + 1] = l;
+  }
+  __syncthreads();
+
+  for (int t = threadIdx.x; t < D; t += kNW * 32) {
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < kNW; ++w) M = fmaxf(M, red_ml[2 * w]);
+    float L = 0.f, A = 0.f;
+    if (M != -INFINITY) {
+#pragma unroll
+      for (int w = 0; w < kNW; ++w) {
+        const float sc = fast_exp2(red_ml[2 * w] - M);
+        L = fmaf(red_ml[2 * w + 1], sc, L);
+        A = fmaf(red_acc[w * D + t], sc, A);
+      }
+    }
+    const int64_t rh = (int64_t)r * H + h;
+    if (nsplit == 1) {
+      E::store(out + rh * D + t, L > 0.f ? A / L : 0.f);
+    } else {
+      ws_acc[(rh * max_splits + split) * D + t] = A;
+      if (t == 0) ws_ml[rh * max_splits + split] = make_float2(M, L);
+    }
+  }
+}
+
+// Merges the splits of one (request, head): out = sum_s 2^(m_s-M) acc_s / sum_s 2^(m_s-M) l_s.
+template <typename T, int D>
+__global__ void __launch_bounds__(128)
+decode_combine_kernel(T* __restrict__ out, const int32_t* __restrict__ seq_lens, int H, int MB,
+                      int max_len, int max_splits, const float* __restrict__ ws_acc,
+                      const float2* __restrict__ ws_ml) {
+  const int r = blockIdx.x, h = blockIdx.y;
+  const int n = clamp_len(seq_lens[r], max_len, MB);
+  const int nblk = (n + kBlockSize - 1) / kBlockSize;
+  const int nsplit = max(1, (nblk + kBPS - 1) / kBPS);
+  if (nsplit <= 1) return;
+  const int64_t rh = (int64_t)r * H + h;
+  const float2* ml = ws_ml + rh * max_splits;
+  float M = -INFINITY;
+  for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[s].x);
+  for (int t = threadIdx.x; t < D; t += blockDim.x) {
+    float L = 0.f, A = 0.f;
+    if (M != -INFINITY) {
+      for (int s = 0; s < nsplit; ++s) {
+        const float2 v = ml[s];
+        const float sc = fast_exp2(v.x - M);
+        L = fmaf(v.y, sc, L);
+        A = fmaf(ws_acc[(rh * max_splits + s) * D + t], sc, A);
+      }
+    }
+    Elt<T>::store(out + rh * D + t, L > 0.f ? A / L : 0.f);
+  }
+}
+
+template <typename T, int D>
+cudaError_t launch_typed(void* out, const void* q, const void* kc, const void* vc,
+                         const int32_t* bt, const int32_t* seq_lens, const int32_t* cu,
+                         const int32_t* ctx, int R, int max_q, int H, int NB, int MB,
+                         int max_len, float scale, const DecodePlan& plan, void* ws,
+                         unsigned* status, cudaStream_t s) {
+  using Sh = DecodeShape<T, D>;
+  const bool prefill = cu != nullptr;
+  const void* fn = prefill ? (const void*)paged_decode_kernel<T, D, true>
+                           : (const void*)paged_decode_kernel<T, D, false>;
+  cudaError_t e = set_smem(fn, Sh::SMEM);
+  if (e != cudaSuccess) return e;
+  const int max_splits = prefill ? 1 : plan.max_splits;
+  float* ws_acc = static_cast<float*>(ws);
+  float2* ws_ml = reinterpret_cast<float2*>(
+      static_cast<char*>(ws) + (size_t)R * H * max_splits * D * sizeof(float));
+  dim3 grid(prefill ? R * max_q : R, H, max_splits);
+  const float scale_log2 = scale * 1.4426950408889634f;
+  if (prefill)
+    paged_decode_kernel<T, D, true><<<grid, kNW * 32, Sh::SMEM, s>>>(
+        (T*)out, (const T*)q, (const T*)kc, (const T*)vc, bt, seq_lens, cu, ctx, max_q, H, NB,
+        MB, max_len, scale_log2, max_splits, ws_acc, ws_ml, status);
+  else
+    paged_decode_kernel<T, D, false><<<grid, kNW * 32, Sh::SMEM, s>>>(
+        (T*)out, (const T*)q, (const T*)kc, (const T*)vc, bt, seq_lens, cu, ctx, max_q, H, NB,
+        MB, max_len, scale_log2, max_splits, ws_acc, ws_ml, status);
+  count_launch();
+  e = cudaGetLastError();
+  if (e != cudaSuccess || max_splits == 1) return e;
+  decode_combine_kernel<T, D><<<dim3(R, H), 128, 0, s>>>((T*)out, seq_lens, H, MB, max_len,
+                                                          max_splits, ws_acc, ws_ml);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+DecodePlan plan_decode(int B, int H, int D, int max_seq_len) {
+  DecodePlan p;
+  p.blocks_per_split = kBPS;
+  const int nblk = (std::max(max_seq_len, 0) + kBlockSize - 1) / kBlockSize;
+  p.max_splits = std::max(1, (nblk + kBPS - 1) / kBPS);
+  p.ws_bytes = p.max_splits > 1 ? (size_t)B * H * p.max_splits * ((size_t)D * 4 + 8) : 0;
+  return p;
+}
+
+bool decode_supported(int dtype, int D) {
+  if (dtype == HYB_BF16) return D == 16 || D == 32 || D == 64 || D == 128 || D == 256;
+  if (dtype == HYB_F32) return D == 16 || D == 32 || D == 64 || D == 128;
+  return false;
+}
+
+cudaError_t launch_paged_decode(void* out, const void* q, const void* kc, const void* vc,
+                                const int32_t* bt, const int32_t* seq_lens, const int32_t* cu,
+                                const int32_t* ctx, int R, int max_q, int H, int D, int dtype,
+                                int NB, int MB, int max_len, float scale,
+                                const DecodePlan& plan, void* ws, unsigned* status,
+                                cudaStream_t s) {
+  if (R == 0 || (cu && max_q == 0)) return cudaSuccess;
+#define HYB_DEC(T, DD)                                                                       \
+  if (D == DD)                                                                               \
+    return launch_typed<T, DD>(out, q, kc, vc, bt, seq_lens, cu, ctx, R, max_q, H, NB, MB,    \
+                               max_len, scale, plan, ws, status, s);
+  if (dtype == HYB_BF16) {
+    HYB_DEC(__nv_bfloat16, 16)
+    HYB_DEC(__nv_bfloat16, 32)
+    HYB_DEC(__nv_bfloat16, 64)
+    HYB_DEC(__nv_bfloat16, 128)
+    HYB_DEC(__nv_bfloat16, 256)
+  } else {
+    HYB_DEC(float, 16)
+    HYB_DEC(float, 32)
+    HYB_DEC(float, 64)
+    HYB_DEC(float, 128)
+  }
+#undef HYB_DEC
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace hyb

@@ -1,0 +1,144 @@
+// Internal declarations shared by the libhyb.so translation units (not part of the ABI).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <algorithm>
+
+#include "../../include/hyb.h"
+
+namespace hyb {
+
+constexpr int kBlockSize = 16;   // tokens per KV block [KV §2.1]
+
+// ------------------------------------------------------------------ host side
+void count_launch();                       // per-thread launch counter (hyb_launch_count)
+int num_sms();                             // SMs of the current device (cached)
+cudaError_t set_smem(const void* fn, int bytes);   // opt-in dynamic shared memory, once
+
+// kernel launchers (each returns the launch's cudaError_t)
+cudaError_t launch_slot_mapping(int64_t* slot, const int32_t* bt, const int32_t* cu,
+                                const int32_t* ctx, int B, int T, int MB, int NB,
+                                unsigned* status, cudaStream_t s);
+cudaError_t launch_kv_append(const void* k, const void* v, const int64_t* slot, int T, int H,
+                             int D, int esize, int NB, void* kc, void* vc, unsigned* status,
+                             cudaStream_t s);
+
+struct DecodePlan {
+  int blocks_per_split;   // KV blocks handled by one CTA
+  int max_splits;         // grid.x
+  size_t ws_bytes;        // workspace needed (0 if max_splits == 1)
+};
+DecodePlan plan_decode(int B, int H, int D, int max_seq_len);
+bool decode_supported(int dtype, int D);
+// decode mode (cu == nullptr): row r < R is request r and attends to seq_lens[r] keys.
+// prefill mode (cu != nullptr): R = B requests; query j < max_q of request b is packed row
+// cu[b] + j and attends to ctx[b] + j + 1 keys (no split-K; no workspace).
+cudaError_t launch_paged_decode(void* out, const void* q, const void* kc, const void* vc,
+                                const int32_t* bt, const int32_t* seq_lens, const int32_t* cu,
+                                const int32_t* ctx, int R, int max_q, int H, int D, int dtype,
+                                int NB, int MB, int max_len, float scale,
+                                const DecodePlan& plan, void* ws, unsigned* status,
+                                cudaStream_t s);
+
+bool linear_supported(int dtype, int D);
+cudaError_t launch_linear_step(void* out, const void* q, const void* k, const void* v,
+                               float* pool, int NS, const int32_t* slots, int B, int H, int D,
+                               int dtype, unsigned* status, cudaStream_t s);
+cudaError_t launch_linear_prefill_simt(void* out, const void* q, const void* k, const void* v,
+                                       const int32_t* cu, const int32_t* ctx, float* pool,
+                                       int NS, const int32_t* slots, const uint8_t* reset, int B,
+                                       int H, int D, int C, int dtype, unsigned* status,
+                                       cudaStream_t s);
+bool linear_prefill_tc_supported(int dtype, int D, int C);
+cudaError_t launch_linear_prefill_tc(void* out, const void* q, const void* k, const void* v,
+                                     const int32_t* cu, const int32_t* ctx, float* pool, int NS,
+                                     const int32_t* slots, const uint8_t* reset, int B, int T,
+                                     int max_len, int H, int C, unsigned* status,
+                                     cudaStream_t s);
+bool prefill_tc_supported(int dtype, int D);
+cudaError_t launch_prefill_tc(void* out, const void* q, const void* kc, const void* vc,
+                              const int32_t* bt, const int32_t* cu, const int32_t* ctx, int B,
+                              int T, int max_q_len, int H, int NB, int MB, float scale,
+                              unsigned* status, cudaStream_t s);
+
+}  // namespace hyb
+
+// ------------------------------------------------------------------ device side
+#ifdef __CUDACC__
+namespace hyb {
+
+__device__ __forceinline__ void flag(unsigned* st, unsigned bit) {
+  if (st) atomicOr(st, bit);
+}
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
+
+// 2^x with the hardware approximation (PTX ex2.approx.ftz.f32); 2^-inf = +0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// ---- mbarrier (CTA scope)
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+               : "memory");
+}
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+               "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+// Waits for the phase with the given parity to complete; gives up after ~`limit_ns`
+// nanoseconds and returns false (callers set HYB_DEVERR_TIMEOUT and unwind).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          uint64_t limit_ns = 2000000000ull) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  while (true) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if (global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+// ---- bulk copies (TMA engine, non-tensor form): global -> shared, completes on `bar`
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+}  // namespace hyb
+#endif

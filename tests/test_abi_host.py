@@ -1,0 +1,96 @@
+"""Host-only checks of the C-ABI library: it loads, exports every entry point that
+include/hyb.h declares, and rejects bad arguments before touching the GPU."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def hyb():
+    from paged_kv_linear_gb300 import _build
+    _build.build()
+    import paged_kv_linear_gb300 as hyb
+    return hyb
+
+
+def declared_entry_points():
+    src = open(os.path.join(ROOT, "include", "hyb.h"), encoding="utf-8").read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(hyb_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(hyb):
+    names = declared_entry_points()
+    assert len(names) >= 12
+    L = C.CDLL(hyb.LIB)
+    for n in names:
+        assert hasattr(L, n), f"{n} declared in include/hyb.h but not exported"
+
+
+def test_cache_bytes_matches_oracle_and_worked_example(hyb):
+    args = (24, 8, 32, 128, 32768, 8, 2, 2)
+    assert hyb.hyb_cache_bytes(*args) == oracle.cache_bytes(*args)
+    tot, full, lin = hyb.hyb_cache_bytes(*args)
+    assert round(full / 1e9) == 103 and round(lin / 1e6) == 67
+
+
+def test_status_strings(hyb):
+    for s in range(5):
+        assert hyb.status_string(s)
+    assert "unknown" in hyb.status_string(99)
+
+
+def test_bad_arguments_rejected_before_launch(hyb):
+    d = hyb.dims(32, 128, 100, 8)
+    fake = 1 << 20      # aligned, never dereferenced: validation fails first
+    # null pointers
+    assert hyb.hyb_paged_kv_append(None, fake, fake, 4, fake, fake + 256, d, 0) == hyb.HYB_ERR_INVALID_ARG
+    # misaligned data pointer
+    assert hyb.hyb_paged_kv_append(fake + 2, fake, fake, 4, fake, fake + 256, d, 0) == hyb.HYB_ERR_INVALID_ARG
+    # the same pool passed as K and V
+    assert hyb.hyb_paged_kv_append(fake, fake, fake, 4, fake, fake, d, 0) == hyb.HYB_ERR_INVALID_ARG
+    # block size other than 16
+    d16 = hyb.dims(32, 128, 100, 8, block_size=32)
+    assert hyb.hyb_paged_kv_append(fake, fake, fake, 4, fake, fake + 256, d16, 0) == hyb.HYB_ERR_UNSUPPORTED
+    # head_dim without a kernel
+    d7 = hyb.dims(4, 24, 100, 8)
+    assert hyb.hyb_paged_attn_decode(fake, fake, fake, fake, fake, fake, 2, 32, d7, None, 0, 0) == hyb.HYB_ERR_UNSUPPORTED
+    # max_seq_len beyond the block table's capacity (8 blocks x 16)
+    assert hyb.hyb_paged_attn_decode(fake, fake, fake, fake, fake, fake, 2, 129, d, fake, 1 << 20, 0) == hyb.HYB_ERR_INVALID_ARG
+    # workspace too small for a split sequence
+    need = hyb.hyb_paged_attn_decode_workspace_size(2, 128, hyb.dims(32, 128, 100, 64))
+    d64 = hyb.dims(32, 128, 100, 64)
+    need = hyb.hyb_paged_attn_decode_workspace_size(2, 1024, d64)
+    assert need > 0
+    assert hyb.hyb_paged_attn_decode(fake, fake, fake, fake, fake, fake, 2, 1024, d64, fake, need - 16, 0) == hyb.HYB_ERR_INVALID_ARG
+    # linear step: no slots / bad dtype / unsupported D
+    assert hyb.hyb_linear_attn_step(fake, fake, fake, fake, fake, 0, fake, 2, 4, 128, 1, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_linear_attn_step(fake, fake, fake, fake, fake, 4, fake, 2, 4, 128, 7, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_linear_attn_step(fake, fake, fake, fake, fake, 4, fake, 2, 4, 48, 1, 0) == hyb.HYB_ERR_UNSUPPORTED
+    # chunk size 0
+    assert hyb.hyb_linear_attn_chunked_prefill(fake, fake, fake, fake, fake, None, fake, 4, fake, None, 2, 64, 4, 128, 0, 1, 0) == hyb.HYB_ERR_INVALID_ARG
+
+
+def test_dispatch_rejects_shared_caches_and_bad_types(hyb):
+    d = hyb.dims(4, 16, 10, 4, dtype=hyb.HYB_F32)
+    f = 1 << 20
+    meta = hyb.batch_meta(2, 2, seq_lens=f, block_tables=f, slot_mapping=f, state_slots=f, max_seq_len=32)
+    a = hyb.layer_io(out=f, q=f, k=f, v=f, k_cache=f + 4096, v_cache=f + 8192)
+    # two Full layers sharing one cache (the failure the vLLM page reports for shared caches)
+    assert hyb.hyb_layer_dispatch([0, 0], 2, 0, [a, a], meta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
+    # unknown layer type
+    assert hyb.hyb_layer_dispatch([2], 1, 0, [a], meta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
+    # decode with T != B
+    meta_bad = hyb.batch_meta(2, 3, seq_lens=f, block_tables=f, slot_mapping=f, max_seq_len=32)
+    assert hyb.hyb_layer_dispatch([0], 1, 0, [a], meta_bad, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
+    # Linear layer without a state pool
+    lin = hyb.layer_io(out=f, q=f, k=f, v=f, num_state_slots=2)
+    assert hyb.hyb_layer_dispatch([1], 1, 0, [lin], meta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
+    # empty plan is a no-op
+    assert hyb.hyb_layer_dispatch([], 0, 0, [], meta, d, 64, None, 0, 0) == hyb.HYB_OK
