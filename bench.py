@@ -321,7 +321,7 @@ def bench_ours(args, dist):
     # ---- CPU oracle beside it (rank 0, N = 1 only)
     cpu = None
     if dist.world == 1:
-        cpu = cpu_baseline_decode(wl, budget_s=15.0)
+        cpu = cpu_baseline_decode(wl, budget_s=10.0)
 
     return {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dist.world,
@@ -355,16 +355,22 @@ def cpu_baseline_decode(wl, budget_s=15.0, requests=None):
     hq = wl["host"]
     done, t_used = 0, 0.0
     order = list(range(wl["B"])) if requests is None else list(requests)
-    for b in order:
-        t0 = time.perf_counter()
-        oracle.full_decode(hq["qf"][b:b + 1], kc, vc, db.pool.block_tables[b:b + 1], db.seq_lens[b:b + 1], D ** -0.5)
-        oracle.linear_step(hq["ql"][b:b + 1], hq["kl"][b:b + 1], hq["vl"][b:b + 1], st, wl["slots_h"][b:b + 1])
-        t_used += time.perf_counter() - t0
-        done += 1
-        if t_used > budget_s:
-            break
+    passes = 0
+    while t_used < budget_s:             # repeat the whole batch until ~budget_s of CPU work
+        for b in order:
+            t0 = time.perf_counter()
+            oracle.full_decode(hq["qf"][b:b + 1], kc, vc, db.pool.block_tables[b:b + 1],
+                               db.seq_lens[b:b + 1], D ** -0.5)
+            oracle.linear_step(hq["ql"][b:b + 1], hq["kl"][b:b + 1], hq["vl"][b:b + 1], st,
+                               wl["slots_h"][b:b + 1])
+            t_used += time.perf_counter() - t0
+            done += 1
+            if t_used > budget_s:
+                break
+        passes += 1
     return {"value": round(done * 2 / t_used, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done} of {wl['B']} requests (all {H} heads; Full decode + Linear step), fp64 C oracle, "
+            "sample": f"{done} request-steps ({passes} pass(es) over the {wl['B']} requests, all {H} heads; "
+                      f"Full decode + Linear step), fp64 C oracle with OpenMP over (request, head), "
                       f"{t_used:.1f} s"}
 
 
