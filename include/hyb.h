@@ -130,6 +130,28 @@ hyb_status_t hyb_paged_attn_decode(void* out, const void* q, const void* k_cache
                                    void* stream);
 
 /* -------------------------------------------------------------------------
+ * Paged decode without a workspace. The pages have no counterpart to this entry point:
+ * it exists for callers that cannot allocate device memory -- a runtime whose device
+ * memory is all assigned by its own planner and that gives an op only its input and
+ * output buffers, or a latency-critical loop that must not call cudaMalloc because it
+ * synchronises the device. Same contract and result as hyb_paged_attn_decode, but the
+ * split-K partials live in a 16 MiB array of device memory owned by the library (held
+ * by every GPU that loads libhyb.so until the process exits); nothing is allocated.
+ * - Returns HYB_ERR_UNSUPPORTED, launching nothing, when the partials would need more
+ *   than 16 MiB (hyb_paged_attn_decode_workspace_size() > 16 MiB).
+ * - The first call on a device looks up the array's device address (with that device
+ *   current); make that first call before any stream capture on the device.
+ * - All calls on a device share the array and it keeps the previous call's contents
+ *   (nothing in it needs to start at zero). Calls whose kernels overlap on the GPU race
+ *   on it: issue them one after another on one stream.
+ * ------------------------------------------------------------------------- */
+hyb_status_t hyb_paged_attn_decode_noalloc(void* out, const void* q, const void* k_cache,
+                                           const void* v_cache, const int32_t* block_tables,
+                                           const int32_t* seq_lens, int32_t B,
+                                           int32_t max_seq_len, const hyb_attn_dims_t* d,
+                                           void* stream);
+
+/* -------------------------------------------------------------------------
  * A4. Causal prefill attention [KV §2.3: prefill uses a FlashAttention-type kernel].
  * Packed row t of request b sits at absolute position i = ctx_lens[b] + (t - cu_q_lens[b])
  * and attends to every cached position p <= i of its request:

@@ -63,6 +63,7 @@ def _load():
         "hyb_paged_kv_append": [p, p, p, i32, p, p, p, p],
         "hyb_paged_attn_decode_workspace_size": ([i32, i32, p], sz),
         "hyb_paged_attn_decode": [p, p, p, p, p, p, i32, i32, p, p, sz, p],
+        "hyb_paged_attn_decode_noalloc": [p, p, p, p, p, p, i32, i32, p, p],
         "hyb_paged_attn_prefill_causal": [p, p, p, p, p, p, p, i32, i32, p, p],
         "hyb_linear_attn_step": [p, p, p, p, p, i32, p, i32, i32, i32, i32, p],
         "hyb_linear_attn_chunked_prefill": [p, p, p, p, p, p, p, i32, p, p, i32, i32, i32, i32,
@@ -160,6 +161,15 @@ def hyb_paged_attn_decode(out, q, k_cache, v_cache, block_tables, seq_lens, B, m
     return _lib.hyb_paged_attn_decode(_p(out), _p(q), _p(k_cache), _p(v_cache), _p(block_tables),
                                       _p(seq_lens), B, max_seq_len, C.byref(d), _p(workspace),
                                       ws_bytes, _s(stream))
+
+
+def hyb_paged_attn_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, B,
+                                  max_seq_len, d, stream=None):
+    """Paged decode whose split-K partials live in the library's own 16 MiB device array
+    (for callers that cannot allocate device memory); see include/hyb.h."""
+    return _lib.hyb_paged_attn_decode_noalloc(_p(out), _p(q), _p(k_cache), _p(v_cache),
+                                              _p(block_tables), _p(seq_lens), B, max_seq_len,
+                                              C.byref(d), _s(stream))
 
 
 def hyb_paged_attn_prefill_causal(out, q, k_cache, v_cache, block_tables, cu_q_lens, ctx_lens,

@@ -54,7 +54,7 @@ cudaError_t set_smem(const void* fn, int bytes) {
 }
 
 // Address of this device's status word (looked up once per device, with it current).
-static unsigned* status_word() {
+unsigned* status_word() {
   const int d = cur_dev();
   if (d < 0) return nullptr;
   std::lock_guard<std::mutex> lk(g_mu);

@@ -13,6 +13,7 @@ constexpr int kBlockSize = 16;   // tokens per KV block [KV §2.1]
 
 // ------------------------------------------------------------------ host side
 void count_launch();                       // per-thread launch counter (hyb_launch_count)
+unsigned* status_word();                   // this device's status word (nullptr on error)
 int num_sms();                             // SMs of the current device (cached)
 cudaError_t set_smem(const void* fn, int bytes);   // opt-in dynamic shared memory, once
 
