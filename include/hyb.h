@@ -158,14 +158,15 @@ hyb_status_t hyb_paged_attn_decode_noalloc(void* out, const void* q, const void*
  *     out[t][h][:] = sum_{p<=i} softmax_p(scale * q[t][h].K_p) V_p
  * K/V are read from the paged cache, so the call's own rows must be appended first
  * (hyb_paged_kv_append) and a cached prefix (ctx_lens[b] > 0) is attended to as well.
- * ctx_lens may be NULL (all 0). max_q_len (host) >= every request's row count.
+ * ctx_lens may be NULL (all 0). T (host) = cu_q_lens[B], the rows of q and out;
+ * max_q_len (host) >= every request's row count.
  * bf16 with D = 128 runs the tensor-core kernel; other supported (dtype, D) pairs run
  * a CUDA-core kernel with the same contract.
  * ------------------------------------------------------------------------- */
 hyb_status_t hyb_paged_attn_prefill_causal(void* out, const void* q, const void* k_cache,
                                            const void* v_cache, const int32_t* block_tables,
                                            const int32_t* cu_q_lens, const int32_t* ctx_lens,
-                                           int32_t B, int32_t max_q_len,
+                                           int32_t B, int32_t T, int32_t max_q_len,
                                            const hyb_attn_dims_t* d, void* stream);
 
 /* -------------------------------------------------------------------------
@@ -194,7 +195,8 @@ hyb_status_t hyb_linear_attn_step(void* out, const void* q, const void* k, const
  * This equals hyb_linear_attn_step applied token by token. The final state is written
  * back to the slot. A call must start on a chunk boundary: when ctx_lens is given,
  * ctx_lens[b] % chunk_size != 0 sets HYB_DEVERR_MISALIGNED and request b is skipped.
- * max_len (host) >= every request's row count. chunk_size 64 with D = 128 and bf16
+ * T (host) = cu_seqlens[B], the rows of q/k/v/out; max_len (host) >= every request's
+ * row count. chunk_size 64 with D = 128 and bf16
  * runs the tensor-core kernel; other (D, dtype, chunk) combinations run the CUDA-core
  * kernel (same contract).
  * ------------------------------------------------------------------------- */
@@ -203,8 +205,9 @@ hyb_status_t hyb_linear_attn_chunked_prefill(void* out, const void* q, const voi
                                              const int32_t* ctx_lens, float* state_pool,
                                              int32_t num_state_slots,
                                              const int32_t* state_slots, const uint8_t* reset,
-                                             int32_t B, int32_t max_len, int32_t H, int32_t D,
-                                             int32_t chunk_size, int32_t dtype, void* stream);
+                                             int32_t B, int32_t T, int32_t max_len, int32_t H,
+                                             int32_t D, int32_t chunk_size, int32_t dtype,
+                                             void* stream);
 
 /* -------------------------------------------------------------------------
  * A7. Layer dispatch [KV §2.2: layer types registered from the model config,

@@ -64,10 +64,10 @@ def _load():
         "hyb_paged_attn_decode_workspace_size": ([i32, i32, p], sz),
         "hyb_paged_attn_decode": [p, p, p, p, p, p, i32, i32, p, p, sz, p],
         "hyb_paged_attn_decode_noalloc": [p, p, p, p, p, p, i32, i32, p, p],
-        "hyb_paged_attn_prefill_causal": [p, p, p, p, p, p, p, i32, i32, p, p],
+        "hyb_paged_attn_prefill_causal": [p, p, p, p, p, p, p, i32, i32, i32, p, p],
         "hyb_linear_attn_step": [p, p, p, p, p, i32, p, i32, i32, i32, i32, p],
         "hyb_linear_attn_chunked_prefill": [p, p, p, p, p, p, p, i32, p, p, i32, i32, i32, i32,
-                                            i32, i32, p],
+                                            i32, i32, i32, p],
         "hyb_layer_dispatch": [p, i32, i32, p, p, p, i32, p, sz, p],
         "hyb_cache_bytes": ([i32, i32, i32, i32, i64, i32, i32, i32, p, p], u64),
         "hyb_device_status": [p, i32],
@@ -173,10 +173,10 @@ def hyb_paged_attn_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_le
 
 
 def hyb_paged_attn_prefill_causal(out, q, k_cache, v_cache, block_tables, cu_q_lens, ctx_lens,
-                                  B, max_q_len, d, stream=None):
+                                  B, T, max_q_len, d, stream=None):
     return _lib.hyb_paged_attn_prefill_causal(_p(out), _p(q), _p(k_cache), _p(v_cache),
                                               _p(block_tables), _p(cu_q_lens), _p(ctx_lens), B,
-                                              max_q_len, C.byref(d), _s(stream))
+                                              T, max_q_len, C.byref(d), _s(stream))
 
 
 def hyb_linear_attn_step(out, q, k, v, state_pool, num_state_slots, state_slots, B, H, D, dtype,
@@ -187,11 +187,11 @@ def hyb_linear_attn_step(out, q, k, v, state_pool, num_state_slots, state_slots,
 
 
 def hyb_linear_attn_chunked_prefill(out, q, k, v, cu_seqlens, ctx_lens, state_pool,
-                                    num_state_slots, state_slots, reset, B, max_len, H, D,
+                                    num_state_slots, state_slots, reset, B, T, max_len, H, D,
                                     chunk_size, dtype, stream=None):
     return _lib.hyb_linear_attn_chunked_prefill(
         _p(out), _p(q), _p(k), _p(v), _p(cu_seqlens), _p(ctx_lens), _p(state_pool),
-        num_state_slots, _p(state_slots), _p(reset), B, max_len, H, D, chunk_size, dtype,
+        num_state_slots, _p(state_slots), _p(reset), B, T, max_len, H, D, chunk_size, dtype,
         _s(stream))
 
 

@@ -123,11 +123,12 @@ hyb_status_t check_decode(const void* out, const void* q, const void* kc, const 
 }
 
 hyb_status_t check_prefill(const void* out, const void* q, const void* kc, const void* vc,
-                           const int32_t* bt, const int32_t* cu, const int32_t* ctx, int B,
+                           const int32_t* bt, const int32_t* cu, const int32_t* ctx, int B, int T,
                            int max_q_len, const hyb_attn_dims_t* d) {
   hyb_status_t st = check_dims(d);
   if (st != HYB_OK) return st;
-  if (B < 0 || max_q_len < 0) return HYB_ERR_INVALID_ARG;
+  if (B < 0 || T < 0 || max_q_len < 0 || max_q_len > T) return HYB_ERR_INVALID_ARG;
+  if (d->num_heads > 65535 || B > 65535) return HYB_ERR_UNSUPPORTED;
   if ((int64_t)max_q_len > (int64_t)d->max_blocks_per_seq * kBlockSize) return HYB_ERR_INVALID_ARG;
   if (!prefill_tc_supported(d->dtype, d->head_dim) && !decode_supported(d->dtype, d->head_dim))
     return HYB_ERR_UNSUPPORTED;
@@ -157,11 +158,11 @@ hyb_status_t check_linear_common(const void* out, const void* q, const void* k, 
 
 hyb_status_t check_linear_prefill(const void* out, const void* q, const void* k, const void* v,
                                   const int32_t* cu, const int32_t* ctx, const float* pool,
-                                  int NS, const int32_t* slots, const uint8_t* reset, int B,
+                                  int NS, const int32_t* slots, const uint8_t* reset, int B, int T,
                                   int max_len, int H, int D, int C, int dtype) {
   hyb_status_t st = check_linear_common(out, q, k, v, pool, NS, slots, B, H, D, dtype);
   if (st != HYB_OK) return st;
-  if (C <= 0 || max_len < 0) return HYB_ERR_INVALID_ARG;
+  if (C <= 0 || T < 0 || max_len < 0 || max_len > T) return HYB_ERR_INVALID_ARG;
   if (!linear_prefill_tc_supported(dtype, D, C) && D > 128) return HYB_ERR_UNSUPPORTED;
   if (B == 0) return HYB_OK;
   if (!cu || !al(cu, 4) || (ctx && !al(ctx, 4))) return HYB_ERR_INVALID_ARG;
@@ -268,14 +269,14 @@ hyb_status_t hyb_paged_attn_decode(void* out, const void* q, const void* k_cache
 hyb_status_t hyb_paged_attn_prefill_causal(void* out, const void* q, const void* k_cache,
                                            const void* v_cache, const int32_t* block_tables,
                                            const int32_t* cu_q_lens, const int32_t* ctx_lens,
-                                           int32_t B, int32_t max_q_len,
+                                           int32_t B, int32_t T, int32_t max_q_len,
                                            const hyb_attn_dims_t* d, void* stream) {
   hyb_status_t st = check_prefill(out, q, k_cache, v_cache, block_tables, cu_q_lens, ctx_lens, B,
-                                  max_q_len, d);
+                                  T, max_q_len, d);
   if (st != HYB_OK || B == 0 || max_q_len == 0) return st;
   unsigned* sw = status_word();
   if (!sw) return HYB_ERR_CUDA;
-  return run_prefill(out, q, k_cache, v_cache, block_tables, cu_q_lens, ctx_lens, B, -1,
+  return run_prefill(out, q, k_cache, v_cache, block_tables, cu_q_lens, ctx_lens, B, T,
                      max_q_len, d, sw, (cudaStream_t)stream);
 }
 
@@ -297,16 +298,17 @@ hyb_status_t hyb_linear_attn_chunked_prefill(void* out, const void* q, const voi
                                              const int32_t* ctx_lens, float* state_pool,
                                              int32_t num_state_slots,
                                              const int32_t* state_slots, const uint8_t* reset,
-                                             int32_t B, int32_t max_len, int32_t H, int32_t D,
-                                             int32_t chunk_size, int32_t dtype, void* stream) {
+                                             int32_t B, int32_t T, int32_t max_len, int32_t H,
+                                             int32_t D, int32_t chunk_size, int32_t dtype,
+                                             void* stream) {
   hyb_status_t st = check_linear_prefill(out, q, k, v, cu_seqlens, ctx_lens, state_pool,
-                                         num_state_slots, state_slots, reset, B, max_len, H, D,
+                                         num_state_slots, state_slots, reset, B, T, max_len, H, D,
                                          chunk_size, dtype);
   if (st != HYB_OK || B == 0) return st;
   unsigned* sw = status_word();
   if (!sw) return HYB_ERR_CUDA;
   return run_linear_prefill(out, q, k, v, cu_seqlens, ctx_lens, state_pool, num_state_slots,
-                            state_slots, reset, B, -1, max_len, H, D, chunk_size, dtype, sw,
+                            state_slots, reset, B, T, max_len, H, D, chunk_size, dtype, sw,
                             (cudaStream_t)stream);
 }
 
@@ -335,7 +337,7 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
                ? check_decode(io.out, io.q, io.k_cache, io.v_cache, meta->block_tables,
                               meta->seq_lens, B, meta->max_seq_len, d, workspace, ws_bytes)
                : check_prefill(io.out, io.q, io.k_cache, io.v_cache, meta->block_tables,
-                               meta->cu_q_lens, meta->ctx_lens, B, meta->max_q_len, d);
+                               meta->cu_q_lens, meta->ctx_lens, B, T, meta->max_q_len, d);
     } else if (layer_types[l] == HYB_LINEAR) {
       if (!io.state_pool || !seen.insert(io.state_pool).second) return HYB_ERR_INVALID_ARG;
       st = mode == HYB_MODE_DECODE
@@ -343,7 +345,7 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
                                      meta->state_slots, B, H, D, dt)
                : check_linear_prefill(io.out, io.q, io.k, io.v, meta->cu_q_lens, meta->ctx_lens,
                                       io.state_pool, io.num_state_slots, meta->state_slots,
-                                      meta->reset, B, meta->max_q_len, H, D, chunk_size, dt);
+                                      meta->reset, B, T, meta->max_q_len, H, D, chunk_size, dt);
     } else {
       return HYB_ERR_INVALID_ARG;
     }

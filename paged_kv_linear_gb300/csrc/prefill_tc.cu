@@ -1,0 +1,359 @@
+// Causal prefill attention over the paged KV cache on the tensor cores (tcgen05 + TMEM +
+// TMA), bf16, D = 128.
+//
+// Page: "推理框架适配Hybrid Model：KV Cache管理与算子调度实战", §2.3 -- prefill runs a
+// FlashAttention-type kernel; the result it must equal is causal softmax attention, here
+// read through the per-request block table (§2.1) so a cached prefix is attended as well.
+//
+// GB300 design. One CTA per (128-query tile, head, request); heavy (late) query tiles are
+// scheduled first. K and V come straight from the paged pool: each 128-key tile is eight
+// 16-token blocks, each fetched with two TMA boxes (16 rows x 64 columns, SW128) at the
+// row the block table names, into a 3-deep K ring and a 2-deep V ring. Per key tile:
+//   S = Q K^T     128 x 128 x 128  A = Q (K-major), B = K (K-major)    -> TMEM, 2 buffers
+//   O += P V      128 x 128 x 128  A = P (K-major), B = V (MN-major)   -> TMEM
+// Four softmax warps own one query row each: TMEM -> registers, causal/length mask,
+// online max, exp2, bf16 P -> shared memory. O stays in TMEM; a row is rescaled only when
+// its running max grows by more than 2^8 (exponents stay <= 2^8, exact after the final
+// division by the row sum). S double-buffering lets Q K^T of the next tile run on the
+// tensor core while the softmax warps work on the current one. One warp issues TMA and MMA.
+#include <cuda_bf16.h>
+
+#include "tc.cuh"
+
+namespace hyb {
+namespace {
+
+constexpr int kBM = 128, kBN = 128, kD = 128;
+constexpr int kSubQ = 128 * 128;             // [128 rows][64 cols] bf16 sub-tile = 16 KiB
+constexpr int kTile = 2 * kSubQ;             // [128][128] bf16 = 32 KiB
+constexpr int kNK = 3, kNV = 2;              // K and V ring depths
+constexpr int kOffQ = 0;
+constexpr int kOffK = kOffQ + kTile;
+constexpr int kOffV = kOffK + kNK * kTile;
+constexpr int kOffP = kOffV + kNV * kTile;
+constexpr int kOffBar = kOffP + kTile;
+constexpr int kSmem = kOffBar + 256 + 1024;
+constexpr int kNSW = 4;                      // softmax warps
+constexpr int kThreads = (kNSW + 1) * 32;
+constexpr uint32_t kTmemCols = 512;          // S0 [0,128) | S1 [128,256) | O [256,384)
+constexpr uint32_t kColO = 256;
+constexpr float kRescaleLog2 = 8.f;
+
+constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0, 0);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 0, 1);
+
+struct Bars {
+  uint64_t qfull, kfull[kNK], kempty[kNK], vfull[kNV], vempty[kNV];
+  uint64_t sfull[2], pfull, odone, drain;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                  const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ out,
+                  const int32_t* __restrict__ bt, const int32_t* __restrict__ cu,
+                  const int32_t* __restrict__ ctx, int H, int NB, int MB, float scale_log2,
+                  unsigned* status) {
+  const int qt = gridDim.x - 1 - blockIdx.x;           // heavy tiles first
+  const int h = blockIdx.y, b = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = cu[b], n = cu[b + 1] - t0;
+  const int q0 = qt * kBM;
+  if (q0 >= n) return;
+  const int c0 = ctx ? ctx[b] : 0;
+  const int rows = min(kBM, n - q0);
+  const int kv_end = c0 + q0 + rows;                   // keys the tile's last query sees
+  const int nkv = (kv_end + kBN - 1) / kBN;
+  const int pos0 = c0 + q0;                            // position of the tile's first query
+  const int32_t* btrow = bt + (int64_t)b * MB;
+  if ((kv_end + 15) / 16 > MB) {
+    if (tid == 0) flag(status, HYB_DEVERR_BAD_BLOCK);
+    return;
+  }
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                           ~static_cast<uintptr_t>(1023));
+  Bars* bars = reinterpret_cast<Bars*>(sm + kOffBar);
+  __shared__ uint32_t tmem_base;
+
+  if (warp == kNSW) {
+    if (lane == 0) {
+      mbar_init(&bars->qfull, 1);
+      for (int i = 0; i < kNK; ++i) { mbar_init(&bars->kfull[i], 1); mbar_init(&bars->kempty[i], 1); }
+      for (int i = 0; i < kNV; ++i) { mbar_init(&bars->vfull[i], 1); mbar_init(&bars->vempty[i], 1); }
+      mbar_init(&bars->sfull[0], 1);
+      mbar_init(&bars->sfull[1], 1);
+      mbar_init(&bars->pfull, kNSW * 32);
+      mbar_init(&bars->odone, 1);
+      mbar_init(&bars->drain, 1);
+      fence_mbar_init();
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+    }
+    __syncwarp();
+    tmem_alloc(&tmem_base, kTmemCols);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_base;
+  uint8_t* const q_s = sm + kOffQ;
+  uint8_t* const p_s = sm + kOffP;
+
+  if (warp == kNSW) {
+    // ------------------------------------------------------------ TMA + MMA warp
+    bool ok = true;
+    int k_issued = 0, v_issued = 0, k_used = 0, v_used = 0;
+    // one 128-key tile: 8 blocks x 2 boxes; blocks past kv_end (or with a bad id) are
+    // skipped. Returns the bytes requested.
+    auto load_kv = [&](const CUtensorMap* map, uint8_t* dst, int j, uint64_t* bar) {
+      int blk_ok[8];
+      int nbox = 0;
+#pragma unroll
+      for (int bi = 0; bi < 8; ++bi) {
+        const int lb = j * 8 + bi;
+        int pb = -1;
+        if (lb * 16 < kv_end) {
+          pb = btrow[lb];
+          if (pb < 0 || pb >= NB) { flag(status, HYB_DEVERR_BAD_BLOCK); pb = -1; }
+        }
+        blk_ok[bi] = pb;
+        nbox += pb >= 0 ? 2 : 0;
+      }
+      mbar_expect_tx(bar, nbox * 2048);
+#pragma unroll
+      for (int bi = 0; bi < 8; ++bi)
+        if (blk_ok[bi] >= 0) {
+          const int y = (blk_ok[bi] * H + h) * 16;
+          tma_load_2d(dst + bi * 2048, map, 0, y, bar);
+          tma_load_2d(dst + kSubQ + bi * 2048, map, 64, y, bar);
+        }
+    };
+    if (lane == 0) {
+      mbar_expect_tx(&bars->qfull, kTile);
+      tma_load_3d(q_s, &tq, 0, h, t0 + q0, &bars->qfull);
+      tma_load_3d(q_s + kSubQ, &tq, 64, h, t0 + q0, &bars->qfull);
+      for (int j = 0; j < min(kNK, nkv); ++j) load_kv(&tk, sm + kOffK + j * kTile, j, &bars->kfull[j]);
+      for (int j = 0; j < min(kNV, nkv); ++j) load_kv(&tv, sm + kOffV + j * kTile, j, &bars->vfull[j]);
+    }
+    k_issued = min(kNK, nkv);
+    v_issued = min(kNV, nkv);
+    const uint32_t qa = smem_u32(q_s), pa = smem_u32(p_s);
+    auto issue_qk = [&](int j) -> bool {           // S[j%2] = Q K_j^T
+      const int ks = j % kNK;
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->kfull[ks], (j / kNK) & 1))) return false;
+      k_used = j + 1;
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t ka = smem_u32(sm + kOffK + ks * kTile);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (k >> 2) * kSubQ + (k & 3) * 32;
+          tc_mma(tmem + (j & 1) * 128, sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024),
+                 kIdescQK, k > 0);
+        }
+        tc_commit(&bars->sfull[j & 1]);
+        tc_commit(&bars->kempty[ks]);
+      }
+      __syncwarp();
+      return true;
+    };
+    ok = __all_sync(0xffffffffu, mbar_wait(&bars->qfull, 0));
+    if (ok) ok = issue_qk(0);
+    if (ok && nkv > 1) ok = issue_qk(1);
+    for (int j = 0; j < nkv && ok; ++j) {
+      // refill the K slot of tile j with tile j + kNK once Q K_j^T is done
+      if (j + kNK < nkv) {
+        ok = mbar_wait(&bars->kempty[j % kNK], (j / kNK) & 1);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        if (lane == 0) load_kv(&tk, sm + kOffK + (j % kNK) * kTile, j + kNK, &bars->kfull[j % kNK]);
+        k_issued = j + kNK + 1;
+      }
+      // P_j ready (softmax of tile j done, O corrected) and V_j landed
+      const int vs = j % kNV;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->pfull, j & 1));
+      ok = ok && __all_sync(0xffffffffu, mbar_wait(&bars->vfull[vs], (j / kNV) & 1));
+      if (!ok) break;
+      v_used = j + 1;
+      uint8_t* v_s = sm + kOffV + vs * kTile;
+      if ((j + 1) * kBN > kv_end) {                // last tile: V rows past kv_end := 0
+        const int first = kv_end - j * kBN;
+        for (int e = lane; e < (kBN - first) * 16; e += 32) {
+          const int r = first + e / 16, sb = (e >> 3) & 1, ch = e & 7;
+          *reinterpret_cast<uint4*>(v_s + sb * kSubQ + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+        }
+        fence_async_smem();
+      }
+      __syncwarp();
+      if (lane == 0) {
+        tc_fence_after();
+        const uint32_t va = smem_u32(v_s);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {              // O += P V_j
+          const uint32_t aoff = (k >> 2) * kSubQ + (k & 3) * 32;
+          tc_mma(tmem + kColO, sw128_desc(pa + aoff, 16, 1024), sw128_desc(va + k * 2048, kSubQ, 1024),
+                 kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
+        }
+        tc_commit(&bars->odone);
+        tc_commit(&bars->vempty[vs]);
+      }
+      __syncwarp();
+      // next Q K^T into the S buffer tile j used (its softmax is done)
+      if (j + 2 < nkv) {
+        ok = issue_qk(j + 2);
+        if (!ok) break;
+      }
+      // refill the V slot of tile j with tile j + kNV once P V_j is done
+      if (j + kNV < nkv) {
+        ok = mbar_wait(&bars->vempty[vs], (j / kNV) & 1);
+        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
+        if (lane == 0) load_kv(&tv, sm + kOffV + vs * kTile, j + kNV, &bars->vfull[vs]);
+        v_issued = j + kNV + 1;
+      }
+    }
+    if (!ok && lane == 0) {
+      flag(status, HYB_DEVERR_TIMEOUT);
+      tc_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, 100000000ull);
+      for (int j = k_used; j < k_issued; ++j) mbar_wait(&bars->kfull[j % kNK], (j / kNK) & 1, 100000000ull);
+      for (int j = v_used; j < v_issued; ++j) mbar_wait(&bars->vfull[j % kNV], (j / kNV) & 1, 100000000ull);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------ softmax warps
+    const int r = warp * 32 + lane;                    // query row of the tile = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    const int qp = pos0 + r;                           // absolute query position
+    float m_used = -INFINITY, l = 0.f;
+    bool ok = true;
+    float x[kBN];
+    for (int j = 0; j < nkv && ok; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->sfull[j & 1], (j >> 1) & 1));
+      if (!ok) break;
+      tc_fence_after();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(tl + (j & 1) * 128 + c * 32, x + c * 32);
+      tmem_ld_wait();
+      const int kbase = j * kBN;
+      const bool masked = kbase + kBN - 1 > pos0 || kbase + kBN > kv_end;
+      float mx = -INFINITY;
+      if (masked) {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          const int kp = kbase + c;
+          x[c] = (kp <= qp && kp < kv_end) ? x[c] * scale_log2 : -INFINITY;
+          mx = fmaxf(mx, x[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < kBN; ++c) {
+          x[c] *= scale_log2;
+          mx = fmaxf(mx, x[c]);
+        }
+      }
+      const float m_new = fmaxf(m_used, mx);
+      const bool grow = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new != -INFINITY);
+      if (j > 0) {                                     // P V_{j-1} done: P buffer and O free
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone, (j - 1) & 1));
+        if (!ok) break;
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, grow)) {           // warp-wide TMEM access, per-row factor
+          const float alpha = (grow && m_used != -INFINITY) ? fast_exp2(m_used - m_new) : 1.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float o[32];
+            tmem_ld32(tl + kColO + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] *= alpha;
+            tmem_st32(tl + kColO + c * 32, o);
+          }
+          tmem_st_wait();
+          if (grow) l *= alpha;
+        }
+      }
+      if (grow) m_used = m_new;
+      float ls = 0.f;
+#pragma unroll
+      for (int c16 = 0; c16 < 16; ++c16) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = fast_exp2(x[c16 * 8 + 2 * e] - m_used);
+          const float p1 = fast_exp2(x[c16 * 8 + 2 * e + 1] - m_used);
+          ls += p0 + p1;
+          w[e] = pack_bf16(p0, p1);
+        }
+        *reinterpret_cast<uint4*>(p_s + (c16 >> 3) * kSubQ + sw128_off(r, c16 & 7)) =
+            make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l += ls;
+      fence_async_smem();
+      tc_fence_before();
+      mbar_arrive(&bars->pfull);
+    }
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone, (nkv - 1) & 1));
+    if (ok) {
+      tc_fence_after();
+      const bool store = q0 + r < n;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = out + ((int64_t)(t0 + q0 + r) * H + h) * kD;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        float o[32];
+        tmem_ld32(tl + kColO + c * 32, o);
+        tmem_ld_wait();
+        if (store) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 w;
+            w.x = pack_bf16(o[e] * inv, o[e + 1] * inv);
+            w.y = pack_bf16(o[e + 2] * inv, o[e + 3] * inv);
+            w.z = pack_bf16(o[e + 4] * inv, o[e + 5] * inv);
+            w.w = pack_bf16(o[e + 6] * inv, o[e + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + e) = w;
+          }
+        }
+      }
+    } else if (lane == 0) {
+      flag(status, HYB_DEVERR_TIMEOUT);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == kNSW) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+bool prefill_tc_supported(int dtype, int D) { return dtype == HYB_BF16 && D == kD; }
+
+cudaError_t launch_prefill_tc(void* out, const void* q, const void* kc, const void* vc,
+                              const int32_t* bt, const int32_t* cu, const int32_t* ctx, int B,
+                              int T, int max_q_len, int H, int NB, int MB, float scale,
+                              unsigned* status, cudaStream_t s) {
+  if (B == 0 || max_q_len == 0 || T <= 0) return cudaSuccess;
+  CUtensorMap mq, mk, mv;
+  const uint64_t qdims[3] = {(uint64_t)kD, (uint64_t)H, (uint64_t)T};
+  const uint64_t qstr[2] = {(uint64_t)kD * 2, (uint64_t)H * kD * 2};
+  const uint32_t qbox[3] = {64, 1, (uint32_t)kBM};
+  const uint64_t cdims[2] = {(uint64_t)kD, (uint64_t)NB * H * 16};
+  const uint64_t cstr[1] = {(uint64_t)kD * 2};
+  const uint32_t cbox[2] = {64, 16};
+  if (!encode_tmap_bf16(&mq, q, 3, qdims, qstr, qbox) ||
+      !encode_tmap_bf16(&mk, kc, 2, cdims, cstr, cbox) ||
+      !encode_tmap_bf16(&mv, vc, 2, cdims, cstr, cbox))
+    return cudaErrorInvalidValue;
+  cudaError_t e = set_smem((const void*)prefill_tc_kernel, kSmem);
+  if (e != cudaSuccess) return e;
+  dim3 grid((max_q_len + kBM - 1) / kBM, H, B);
+  prefill_tc_kernel<<<grid, kThreads, kSmem, s>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(out), bt,
+                                                  cu, ctx, H, NB, MB, scale * 1.4426950408889634f,
+                                                  status);
+  count_launch();
+  return cudaGetLastError();
+}
+
+}  // namespace hyb

@@ -74,7 +74,7 @@ def test_bad_arguments_rejected_before_launch(hyb):
     assert hyb.hyb_linear_attn_step(fake, fake, fake, fake, fake, 4, fake, 2, 4, 128, 7, 0) == hyb.HYB_ERR_INVALID_ARG
     assert hyb.hyb_linear_attn_step(fake, fake, fake, fake, fake, 4, fake, 2, 4, 48, 1, 0) == hyb.HYB_ERR_UNSUPPORTED
     # chunk size 0
-    assert hyb.hyb_linear_attn_chunked_prefill(fake, fake, fake, fake, fake, None, fake, 4, fake, None, 2, 64, 4, 128, 0, 1, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_linear_attn_chunked_prefill(fake, fake, fake, fake, fake, None, fake, 4, fake, None, 2, 128, 64, 4, 128, 0, 1, 0) == hyb.HYB_ERR_INVALID_ARG
 
 
 def test_dispatch_rejects_shared_caches_and_bad_types(hyb):

@@ -57,9 +57,9 @@ def _tiny_flow(hyb, use_dispatch, chunk):
         hyb.check(hyb.hyb_layer_dispatch([0, 1], 2, 1, layers, meta, d, chunk, None, 0))
     else:
         hyb.check(hyb.hyb_paged_kv_append(k, v, slot, T, kc, vc, d))
-        hyb.check(hyb.hyb_paged_attn_prefill_causal(fo, q, kc, vc, bt, cu_d, None, B, int(prompts.max()), d))
+        hyb.check(hyb.hyb_paged_attn_prefill_causal(fo, q, kc, vc, bt, cu_d, None, B, T, int(prompts.max()), d))
         hyb.check(hyb.hyb_linear_attn_chunked_prefill(lo, ql, kl, vl, cu_d, None, st_pool, 3, slots_d,
-                                                      reset_d, B, int(prompts.max()), H, D, chunk, W.F32))
+                                                      reset_d, B, T, int(prompts.max()), H, D, chunk, W.F32))
     res["full_out"].append(to_host(fo))
     res["lin_out"].append(to_host(lo))
     ws = torch.empty(1 << 16, dtype=torch.uint8, device="cuda")
