@@ -45,6 +45,10 @@ def parse():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--workload", default="decode_single_layer",
+                    choices=["decode_single_layer", "hybrid_32layer", "prefill_chunked", "long_context_decode"],
+                    help="decode_single_layer is the headline; the others are timed alone (e.g. for profiling)")
+    ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements of the other workloads")
     return ap.parse_args()
 
 
@@ -183,6 +187,178 @@ def build_workload(seed, device):
     return wl
 
 
+# ------------------------------------------------------------------ other rows
+def _time(fn, stream, iters, warmup=3):
+    """Average device time (ms) of fn() over `iters` calls, CUDA events on `stream`."""
+    import torch
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            fn()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            fn()
+        e1.record(stream)
+        stream.synchronize()
+    return e0.elapsed_time(e1) / iters
+
+
+def _roof(bound, achieved, peak, unit, kernel, alg, traffic=None, **extra):
+    r = {"kernel": kernel, "bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
+         "frac": round(achieved / peak, 4), "traffic": traffic, "algorithmic": alg}
+    r.update(extra)
+    return r
+
+
+def row_long_context(hyb, device, stream, iters, seed=0):
+    """8 requests x 131072 tokens: split-K paged decode over 8192 random blocks each, and the
+    Linear step on 8 x 32 x 128 x 128 fp32 states."""
+    import torch
+    hbm, _, _ = measured_peaks()
+    db = W.decode_long_context(seed)
+    B, H, D, NB = db.B, db.H, db.D, db.pool.num_blocks
+    d = hyb.dims(H, D, NB, db.pool.max_blocks, W.BF16)
+    kc = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), 51, D)
+    vc = W.device_rows_(torch.empty_like(kc), 52, D)
+    st = W.device_state_(torch.empty((B, H, D, D), device=device), 53, db.seq_lens, D)
+    g = W.rng(seed + 5)
+    q = torch.from_numpy(W.rows(g, (B, H, D), D, W.BF16).view(np.int16)).to(device).view(torch.bfloat16)
+    out = torch.empty_like(q)
+    bt = torch.from_numpy(db.pool.block_tables).to(device)
+    lens = torch.from_numpy(db.seq_lens).to(device)
+    slots = torch.arange(B, dtype=torch.int32, device=device)
+    n = int(db.seq_lens.max())
+    ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, n, d)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=device)
+    sh = stream.cuda_stream
+    t_dec = _time(lambda: hyb.check(hyb.hyb_paged_attn_decode(out, q, kc, vc, bt, lens, B, n, d, ws, ws_n, sh)), stream, iters)
+    t_lin = _time(lambda: hyb.check(hyb.hyb_linear_attn_step(out, q, q, q, st, B, slots, B, H, D, W.BF16, sh)), stream, iters)
+    dec_bytes = int(db.seq_lens.sum()) * H * D * 4 + 2 * B * H * D * 2
+    lin_bytes = B * H * D * D * 8
+    res = {"workload": "long_context_decode: 8 requests x 131072 tokens, H=32, D=128, 8192 random blocks each",
+           "value": round(B * 2 / ((t_dec + t_lin) * 1e-3), 1), "unit": UNIT,
+           "ms": {"paged_decode": round(t_dec, 4), "linear_step": round(t_lin, 4)},
+           "roofline": _roof("hbm", dec_bytes / (t_dec * 1e-3) / 1e9, hbm, "GB/s", "paged_decode (split-K + combine)", dec_bytes),
+           "linear_step": _roof("hbm", lin_bytes / (t_lin * 1e-3) / 1e9, hbm, "GB/s", "linear_step", lin_bytes)}
+    del kc, vc, st
+    torch.cuda.empty_cache()
+    return res
+
+
+def row_hybrid_32layer(hyb, device, stream, iters, seed=0):
+    """32 layers [F,F,F,Lin] x 8, batch 64 (80% ~128, 20% ~2048 tokens): one decode token per
+    request through all layers via hyb_layer_dispatch."""
+    import torch
+    hbm, _, _ = measured_peaks()
+    db = W.decode_hybrid_32layer(seed)
+    lt = db.extra["layer_types"]
+    B, H, D, NB, MB = db.B, db.H, db.D, db.pool.num_blocks, db.pool.max_blocks
+    d = hyb.dims(H, D, NB, MB, W.BF16)
+    g = W.rng(seed + 9)
+    mk = lambda: torch.from_numpy(W.rows(g, (B, H, D), D, W.BF16).view(np.int16)).to(device).view(torch.bfloat16)
+    keep, ios = [], []
+    for l, t in enumerate(lt):
+        q, k, v, o = mk(), mk(), mk(), torch.empty((B, H, D), dtype=torch.bfloat16, device=device)
+        if t == 0:
+            kc = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), 100 + l, D)
+            vc = W.device_rows_(torch.empty_like(kc), 200 + l, D)
+            keep += [q, k, v, o, kc, vc]
+            ios.append(hyb.layer_io(o, q, k, v, kc, vc))
+        else:
+            sp = W.device_state_(torch.empty((B, H, D, D), device=device), 300 + l, db.seq_lens, D)
+            keep += [q, k, v, o, sp]
+            ios.append(hyb.layer_io(o, q, k, v, state_pool=sp, num_state_slots=B))
+    bt = torch.from_numpy(db.pool.block_tables).to(device)
+    lens = torch.from_numpy(db.seq_lens).to(device)
+    ctx = torch.from_numpy(db.seq_lens - 1).to(device)
+    cu = torch.arange(B + 1, dtype=torch.int32, device=device)
+    slots = torch.from_numpy(g.permutation(B).astype(np.int32)).to(device)
+    slot = torch.empty(B, dtype=torch.int64, device=device)
+    msl = int(db.seq_lens.max())
+    ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, msl, d)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device=device)
+    meta = hyb.batch_meta(B, B, seq_lens=lens, block_tables=bt, slot_mapping=slot, state_slots=slots, max_seq_len=msl)
+    sh = stream.cuda_stream
+
+    def step():
+        hyb.check(hyb.hyb_slot_mapping(slot, bt, cu, ctx, B, B, d, sh))
+        hyb.check(hyb.hyb_layer_dispatch(lt, 32, 0, ios, meta, d, 64, ws, ws_n, sh))
+    hyb.hyb_launch_count(reset=True)
+    step()
+    launches = hyb.hyb_launch_count(reset=True)
+    t = _time(step, stream, iters)
+    n_full, n_lin = int((lt == 0).sum()), int((lt == 1).sum())
+    alg = n_full * (int(db.seq_lens.sum()) * H * D * 4 + 2 * B * H * D * 2) + n_lin * B * H * D * D * 8
+    res = {"workload": "hybrid_32layer: [full,full,full,linear] x 8, batch 64, 80% ~lognormal(128) / 20% ~lognormal(2048)",
+           "value": round(B * 32 / (t * 1e-3), 1), "unit": UNIT, "ms_per_step": round(t, 4),
+           "launches_per_step": int(launches),
+           "roofline": _roof("hbm", alg / (t * 1e-3) / 1e9, hbm, "GB/s", "whole 32-layer step (dispatch)", alg)}
+    del keep, ios
+    torch.cuda.empty_cache()
+    return res
+
+
+def row_prefill(hyb, device, stream, iters, seed=0):
+    """8 requests x 8192-token prompts, H=32, D=128: Full layer = slot mapping + KV append +
+    tensor-core causal prefill over the paged cache; Linear layer = tensor-core chunked
+    prefill (chunk 64) from a zero state."""
+    import torch
+    hbm, tf, _ = measured_peaks()
+    pb = W.prefill_chunked(seed)
+    B, H, D, NB = len(pb.q_lens), pb.H, pb.D, pb.pool.num_blocks
+    cu_h = W.cu_from_lens(pb.q_lens)
+    T = int(cu_h[-1])
+    d = hyb.dims(H, D, NB, pb.pool.max_blocks, W.BF16)
+    mk = lambda s: W.device_rows_(torch.empty((T, H, D), dtype=torch.bfloat16, device=device), s, D)
+    q, k, v, ql, kl, vl = (mk(60 + i) for i in range(6))
+    out, lo = torch.empty_like(q), torch.empty_like(q)
+    kc = torch.zeros((NB, H, 16, D), dtype=torch.bfloat16, device=device)
+    vc = torch.zeros_like(kc)
+    st = torch.zeros((B, H, D, D), device=device)
+    bt = torch.from_numpy(pb.pool.block_tables).to(device)
+    cu = torch.from_numpy(cu_h).to(device)
+    slots = torch.arange(B, dtype=torch.int32, device=device)
+    reset = torch.ones(B, dtype=torch.uint8, device=device)
+    slot = torch.empty(T, dtype=torch.int64, device=device)
+    sh = stream.cuda_stream
+    L = int(pb.q_lens.max())
+    t_slot = _time(lambda: hyb.check(hyb.hyb_slot_mapping(slot, bt, cu, None, B, T, d, sh)), stream, iters)
+    t_app = _time(lambda: hyb.check(hyb.hyb_paged_kv_append(k, v, slot, T, kc, vc, d, sh)), stream, iters)
+    t_pf = _time(lambda: hyb.check(hyb.hyb_paged_attn_prefill_causal(out, q, kc, vc, bt, cu, None, B, T, L, d, sh)), stream, iters)
+    t_lin = _time(lambda: hyb.check(hyb.hyb_linear_attn_chunked_prefill(lo, ql, kl, vl, cu, None, st, B, slots, reset,
+                                                                        B, T, L, H, D, pb.chunk, W.BF16, sh)), stream, iters)
+    st_, fl = hyb.hyb_device_status(clear=True)
+    if st_ != 0:
+        raise RuntimeError(f"device-side check flags {fl:#x}")
+    n = pb.q_lens.astype(np.float64)
+    pf_flops = 4.0 * H * D * float((n * (n + 1) / 2).sum())              # QK^T + PV over the causal triangle
+    lin_flops = T * H * (4.0 * pb.chunk * D + 4.0 * D * D)                # per token-head: 4CD + 4D^2
+    lin_bytes = 4 * T * H * D * 2 + B * H * D * D * 4                     # q,k,v read, o written, state written
+    app_bytes = 2 * 2 * T * H * D * 2
+    ai = lin_flops / lin_bytes
+    lin_gbs = lin_bytes / (t_lin * 1e-3) / 1e9
+    lin_tf = lin_flops / (t_lin * 1e-3) / 1e12
+    res = {"workload": "prefill_chunked: 8 requests x 8192-token prompts, H=32, D=128, chunk 64",
+           "value": round(T * 2 / ((t_slot + t_app + t_pf + t_lin) * 1e-3), 1), "unit": "prompt tokens/s per layer",
+           "ms": {"slot_mapping": round(t_slot, 4), "kv_append": round(t_app, 4), "prefill_causal": round(t_pf, 4),
+                  "linear_chunked_prefill": round(t_lin, 4)},
+           "roofline": _roof("tensor", pf_flops / (t_pf * 1e-3) / 1e12, tf, "TFLOP/s", "prefill_tc_kernel (causal, paged)",
+                             pf_flops, peak_source="measured bf16_tflops (burst)"),
+           "linear_chunked_prefill": _roof("hbm", lin_gbs, hbm, "GB/s", "linear_prefill_tc_kernel", lin_bytes,
+                                           tflops=round(lin_tf, 1), tensor_frac=round(lin_tf / tf, 4),
+                                           arithmetic_intensity=round(ai, 1),
+                                           frac_of_min_peak_ai_bw=round(lin_tf / min(tf, ai * hbm / 1e3), 4)),
+           "kv_append": _roof("hbm", app_bytes / (t_app * 1e-3) / 1e9, hbm, "GB/s", "kv_append_kernel", app_bytes)}
+    del q, k, v, ql, kl, vl, out, lo, kc, vc, st
+    torch.cuda.empty_cache()
+    return res
+
+
+ROWS = {"long_context_decode": row_long_context, "hybrid_32layer": row_hybrid_32layer,
+        "prefill_chunked": row_prefill}
+
+
 def bench_ours(args, dist):
     import torch
     from paged_kv_linear_gb300 import _build
@@ -194,6 +370,12 @@ def bench_ours(args, dist):
 
     torch.cuda.set_device(dist.local)
     device = torch.device("cuda", dist.local)
+    if args.workload != "decode_single_layer":          # one other workload, timed alone
+        stream = torch.cuda.Stream(device=device)
+        r = ROWS[args.workload](hyb, device, stream, max(args.steps, 1), args.seed + dist.rank)
+        r.update({"metric": METRIC, "n_gpus": dist.world, "steps": args.steps, "warmup": 3,
+                  "higher_is_better": True, "dtype": "bf16", "data": "synthetic"})
+        return r
     wl = build_workload(args.seed + dist.rank, device)
     B, H, D, NB, MB, db = wl["B"], wl["H"], wl["D"], wl["NB"], wl["MB"], wl["db"]
     d = hyb.dims(H, D, NB, MB, W.BF16)
@@ -323,6 +505,13 @@ def bench_ours(args, dist):
     if dist.world == 1:
         cpu = cpu_baseline_decode(wl, budget_s=10.0)
 
+    # ---- the other rows of the hot path, each against its own roofline (N = 1 only)
+    rows = None
+    if dist.world == 1 and not args.no_rows:
+        del wl
+        torch.cuda.empty_cache()
+        rows = {name: fn(hyb, device, stream, 20, args.seed) for name, fn in ROWS.items()}
+
     return {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
@@ -339,6 +528,7 @@ def bench_ours(args, dist):
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
+        "rows": rows,
     }
 
 

@@ -274,6 +274,10 @@ hyb_status_t hyb_device_status(uint32_t* flags, int32_t clear);
 /* Static description of a status code (never NULL). */
 const char* hyb_status_string(hyb_status_t s);
 
+/* Text of the CUDA runtime error behind the last HYB_ERR_CUDA that an entry point returned
+ * on this thread ("no error" if none). Never NULL. */
+const char* hyb_last_cuda_error(void);
+
 /* Number of kernel launches this library has issued on this thread since the last
  * call with reset != 0 (host-side counter; benchmarks report it). */
 uint64_t hyb_launch_count(int32_t reset);

@@ -72,6 +72,7 @@ def _load():
         "hyb_cache_bytes": ([i32, i32, i32, i32, i64, i32, i32, i32, p, p], u64),
         "hyb_device_status": [p, i32],
         "hyb_status_string": ([i32], C.c_char_p),
+        "hyb_last_cuda_error": ([], C.c_char_p),
         "hyb_launch_count": ([i32], u64),
     }
     for name, s in sig.items():
@@ -134,7 +135,12 @@ def dims(num_heads, head_dim, num_blocks, max_blocks_per_seq, dtype=HYB_BF16, sc
 
 def check(status: int, what: str = "hyb call") -> None:
     if status != HYB_OK:
-        raise HybError(f"{what}: {status_string(status)} (status {status})")
+        extra = f" [{hyb_last_cuda_error()}]" if status == HYB_ERR_CUDA else ""
+        raise HybError(f"{what}: {status_string(status)} (status {status}){extra}")
+
+
+def hyb_last_cuda_error() -> str:
+    return _lib.hyb_last_cuda_error().decode()
 
 
 def status_string(status: int) -> str:

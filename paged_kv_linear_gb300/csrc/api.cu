@@ -88,7 +88,13 @@ hyb_status_t check_dims(const hyb_attn_dims_t* d) {
   return HYB_OK;
 }
 
-hyb_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? HYB_OK : HYB_ERR_CUDA; }
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+hyb_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return HYB_OK;
+  g_last_cuda = e;
+  return HYB_ERR_CUDA;
+}
 
 // ---- per-op checks (no launch) -----------------------------------------------------
 hyb_status_t check_append(const void* k, const void* v, const int64_t* slot, int T,
@@ -406,6 +412,8 @@ hyb_status_t hyb_device_status(uint32_t* flags, int32_t clear) {
   *flags = v;
   return v ? HYB_ERR_DEVICE_CHECK : HYB_OK;
 }
+
+const char* hyb_last_cuda_error(void) { return cudaGetErrorString(g_last_cuda); }
 
 const char* hyb_status_string(hyb_status_t s) {
   switch (s) {

@@ -8,20 +8,23 @@
 //     O_c = Q_c S + tril(Q_c K_c^T) V_c        S <- S + K_c^T V_c
 //
 // GB300 design. One CTA per (request, head) walks its chunks in order (the state chain is
-// sequential); 256 chains of the 8 x 8192-token prompt fill the 152 SMs in under two
-// waves. Q/K/V chunks stream through a 3-stage TMA ring (SW128 tiles, one mbarrier per
-// stage). The state lives in TMEM for the whole call and is accumulated in place by the
-// tensor core. Four MMA groups per chunk (M x N x K):
-//   (a) P    = Q_c K_c^T          64 x 64 x 128   A = Q (K-major), B = K (K-major)
-//   (b) O^T  = S^T Q_c^T          128 x 64 x 128  A = S^T (MN-major, bf16 hi and lo parts),
-//                                                 B = Q (K-major); hi + lo keeps ~16 bits
+// sequential). Warp roles: one TMA warp streams Q/K/V chunks through a 3-stage ring (SW128
+// tiles, one mbarrier per stage); one MMA warp issues the tensor-core work; eight
+// conversion warps move TMEM -> registers -> shared/global memory. The state lives in TMEM
+// for the whole call and is accumulated in place. Per chunk (M x N x K), in issue order:
 //   (d) S   += K_c^T V_c          128 x 128 x 64  A = K^T (MN-major), B = V (MN-major)
+//   (b) O^T  = S^T Q_c^T          128 x 64 x 128  A = S^T of the previous chunk end, as two
+//                                                 bf16 parts hi + lo (~16 bits), B = Q
+//   (a) P    = Q_c K_c^T          64 x 64 x 128   A = Q (K-major), B = K (K-major)
 //   (c) O^T += V_c^T tril(P)^T    128 x 64 x 64   A = V^T (MN-major), B = tril(P) (K-major)
-// Eight conversion warps move TMEM -> registers -> shared memory: the causal mask and bf16
-// rounding of P, the hi/lo split of S for the next chunk's (b), and O^T -> global (one
-// column of O per thread, so stores of a warp are 64 contiguous bytes). One warp issues
-// TMA and MMA (lane 0) and zeroes the K/V rows past the end of a request's last chunk.
-// Output is computed transposed (M = value dim) so every MMA but (a) uses M = 128.
+// The chain that limits a request is (d) -> read S from TMEM -> hi/lo split -> next (d);
+// (d) is issued first so the conversion warps read the new state while (b) still runs, and
+// write the split only once (b) has consumed the previous one; (c) of a chunk is issued
+// after (a) of the next, so no state update waits for P's conversion. O^T and P are
+// double-buffered (TMEM and shared memory) and every handshake barrier exists once per
+// buffer parity, so none can run two phases ahead of its waiter. Output is computed
+// transposed (M = value dim) so all MMAs but (a) use M = 128, and each conversion thread
+// stores one column of O: a warp's stores are 64 contiguous bytes.
 #include <cuda_bf16.h>
 
 #include "tc.cuh"
@@ -36,13 +39,14 @@ constexpr int kTile = 2 * kSub;              // [64][128] bf16 tile
 constexpr int kStage = 3 * kTile;            // Q, K, V
 constexpr int kOffS = kNST * kStage;         // S^T hi / lo (each [128 k-rows][128], MN-major)
 constexpr int kSTile = 128 * 128 * 2;
-constexpr int kOffP = kOffS + 2 * kSTile;    // tril(P) [64][64] K-major
-constexpr int kOffBar = kOffP + kSub;
+constexpr int kOffP = kOffS + 2 * kSTile;    // tril(P) [64][64] K-major, two buffers
+constexpr int kOffBar = kOffP + 2 * kSub;
 constexpr int kSmem = kOffBar + 256 + 1024;  // + slack for 1024-byte alignment
 constexpr int kNCW = 8;                      // conversion warps
-constexpr int kThreads = (kNCW + 1) * 32;
-constexpr uint32_t kTmemCols = 256;          // S [0,128) | O^T [128,192) | P [192,256)
-constexpr uint32_t kColS = 0, kColO = 128, kColP = 192;
+constexpr int kWarpTma = kNCW, kWarpMma = kNCW + 1;
+constexpr int kThreads = (kNCW + 2) * 32;
+constexpr uint32_t kTmemCols = 512;          // S [0,128) | O^T x2 [128,256) | P x2 [256,384)
+constexpr uint32_t kColS = 0, kColO = 128, kColP = 256;
 
 constexpr uint32_t kIdescA = idesc_bf16(64, 64, 0, 0);
 constexpr uint32_t kIdescB = idesc_bf16(128, 64, 1, 0);
@@ -51,7 +55,8 @@ constexpr uint32_t kIdescC = idesc_bf16(128, 64, 1, 0);
 
 struct Bars {
   uint64_t full[kNST], empty[kNST];
-  uint64_t p_ready, p_written, s_ready, s_written, o_ready, o_read, drain;
+  uint64_t s_ready, b_done, s_written, drain;
+  uint64_t p_ready[2], p_written[2], o_ready[2], o_free[2];   // one per buffer parity
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -89,23 +94,23 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
   Bars* bars = reinterpret_cast<Bars*>(sm + kOffBar);
   __shared__ uint32_t tmem_base;
 
-  if (warp == kNCW) {
+  if (warp == kWarpMma) {
     if (lane == 0) {
       for (int s = 0; s < kNST; ++s) {
         mbar_init(&bars->full[s], 1);
         mbar_init(&bars->empty[s], 1);
       }
-      mbar_init(&bars->p_ready, 1);
       mbar_init(&bars->s_ready, 1);
-      mbar_init(&bars->o_ready, 1);
-      mbar_init(&bars->p_written, kNCW * 32);
+      mbar_init(&bars->b_done, 1);
       mbar_init(&bars->s_written, kNCW * 32);
-      mbar_init(&bars->o_read, kNCW * 32);
+      for (int i = 0; i < 2; ++i) {
+        mbar_init(&bars->p_ready[i], 1);
+        mbar_init(&bars->p_written[i], kNCW * 32);
+        mbar_init(&bars->o_ready[i], 1);
+        mbar_init(&bars->o_free[i], kNCW * 32);
+      }
       mbar_init(&bars->drain, 1);
       fence_mbar_init();
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
     }
     __syncwarp();
     tmem_alloc(&tmem_base, kTmemCols);
@@ -118,33 +123,67 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
   uint8_t* const s_lo = s_hi + kSTile;
   uint8_t* const p_tile = sm + kOffP;
 
-  if (warp == kNCW) {
-    // ------------------------------------------------------------ TMA + MMA warp
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA warp
+    if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
+    }
+    int issued = 0;
     bool ok = true;
-    int issued = 0, consumed = 0;            // chunks whose loads were issued / waited for
-    auto load = [&](int c) {                 // lane 0
+    for (int c = 0; c < nch; ++c) {
       const int st = c % kNST;
-      uint8_t* q = sm + st * kStage;
-      uint64_t* bar = &bars->full[st];
-      mbar_expect_tx(bar, kStage);
-      const int z = t0 + c * kC;
-      for (int sb = 0; sb < 2; ++sb) {
-        tma_load_3d(q + sb * kSub, &tq, sb * 64, h, z, bar);
-        tma_load_3d(q + kTile + sb * kSub, &tk, sb * 64, h, z, bar);
-        tma_load_3d(q + 2 * kTile + sb * kSub, &tv, sb * 64, h, z, bar);
+      if (c >= kNST) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->empty[st], ((c - kNST) / kNST) & 1));
+        if (!ok) break;
       }
+      if (lane == 0) {
+        uint8_t* q = sm + st * kStage;
+        uint64_t* bar = &bars->full[st];
+        mbar_expect_tx(bar, kStage);
+        const int z = t0 + c * kC;
+        for (int sb = 0; sb < 2; ++sb) {
+          tma_load_3d(q + sb * kSub, &tq, sb * 64, h, z, bar);
+          tma_load_3d(q + kTile + sb * kSub, &tk, sb * 64, h, z, bar);
+          tma_load_3d(q + 2 * kTile + sb * kSub, &tv, sb * 64, h, z, bar);
+        }
+      }
+      issued = c + 1;
+    }
+    if (!ok && lane == 0) {                  // let the loads in flight land before exiting
+      flag(status, HYB_DEVERR_TIMEOUT);
+      for (int c = max(0, issued - kNST); c < issued; ++c)
+        mbar_wait(&bars->full[c % kNST], (c / kNST) & 1, 100000000ull);
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA warp
+    // Issue order per chunk c: (d)_c, (b)_c, (a)_c, then (c)_{c-1} -- the output update of
+    // the previous chunk goes last so the next state update never waits for P's conversion.
+    bool ok = true;
+    const uint32_t ha = smem_u32(s_hi), la = smem_u32(s_lo), pa = smem_u32(p_tile);
+    auto issue_c = [&](int c) {                  // (c) O^T += V^T tril(P)^T of chunk c
+      const int st = c % kNST, pb = c & 1;
+      const uint32_t va = smem_u32(sm + st * kStage + 2 * kTile);
+      if (lane == 0) {
+        tc_fence_after();
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          tc_mma(tmem + kColO + pb * 64, sw128_desc(va + k * 2048, kSub, 1024),
+                 sw128_desc(pa + pb * kSub + k * 32, 16, 1024), kIdescC, 1);
+        tc_commit(&bars->o_ready[pb]);
+        tc_commit(&bars->empty[st]);
+      }
+      __syncwarp();
     };
-    if (lane == 0)
-      for (int c = 0; c < min(kNST, nch); ++c) load(c);
-    issued = min(kNST, nch);
     for (int c = 0; c < nch && ok; ++c) {
-      const int st = c % kNST;
+      const int st = c % kNST, ob = c & 1;
       uint8_t* qs = sm + st * kStage;
       uint8_t* ks = qs + kTile;
       uint8_t* vs = ks + kTile;
+      const uint32_t qa = smem_u32(qs), ka = smem_u32(ks), va = smem_u32(vs);
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->full[st], (c / kNST) & 1));
       if (!ok) break;
-      consumed = c + 1;
       const int nvalid = min(kC, n - c * kC);
       if (nvalid < kC) {                     // rows past the request: K and V rows := 0
         for (int e = lane; e < (kC - nvalid) * 2 * 8; e += 32) {
@@ -156,181 +195,210 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
         fence_async_smem();
       }
       __syncwarp();
-      if (lane == 0) {
-        tc_fence_after();
-        const uint32_t qa = smem_u32(qs), ka = smem_u32(ks);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {        // (a) P = Q K^T
-          const uint32_t off = (k >> 2) * kSub + (k & 3) * 32;
-          tc_mma(tmem + kColP, sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024),
-                 kIdescA, k > 0);
-        }
-        tc_commit(&bars->p_ready);
-      }
-      // refill the stage the previous chunk used, once its MMAs are done
-      if (c >= 1 && c - 1 + kNST < nch) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->empty[(c - 1) % kNST], ((c - 1) / kNST) & 1));
-        if (!ok) break;
-        if (lane == 0) load(c - 1 + kNST);
-        issued = c - 1 + kNST + 1;
-      }
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_written, c & 1));
-      if (ok && c > 0) ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_read, (c - 1) & 1));
       if (!ok) break;
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t qa = smem_u32(qs), ka = smem_u32(ks), va = smem_u32(vs);
-        const uint32_t ha = smem_u32(s_hi), la = smem_u32(s_lo);
-#pragma unroll
-        for (int part = 0; part < 2; ++part) {   // (b) O^T = S^T Q^T, hi then lo
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t a = (part ? la : ha) + k * 2048;
-            const uint32_t boff = (k >> 2) * kSub + (k & 3) * 32;
-            tc_mma(tmem + kColO, sw128_desc(a, 16384, 1024), sw128_desc(qa + boff, 16, 1024),
-                   kIdescB, (part | k) != 0);
-          }
-        }
 #pragma unroll
         for (int k = 0; k < 4; ++k)              // (d) S += K^T V
           tc_mma(tmem + kColS, sw128_desc(ka + k * 2048, kSub, 1024),
                  sw128_desc(va + k * 2048, kSub, 1024), kIdescD, 1);
         tc_commit(&bars->s_ready);
       }
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_written, c & 1));
-      if (!ok) break;
+      if (c >= 2) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_free[ob], ((c - 2) >> 1) & 1));
+        if (!ok) break;
+      }
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t va = smem_u32(vs), pa = smem_u32(p_tile);
+        const uint32_t od = tmem + kColO + ob * 64;
 #pragma unroll
-        for (int k = 0; k < 4; ++k)              // (c) O^T += V^T tril(P)^T
-          tc_mma(tmem + kColO, sw128_desc(va + k * 2048, kSub, 1024),
-                 sw128_desc(pa + k * 32, 16, 1024), kIdescC, 1);
-        tc_commit(&bars->o_ready);
-        tc_commit(&bars->empty[st]);
-      }
-    }
-    if (!ok) {
-      // A wait expired: report it, then let every issued MMA and TMA load land (bounded)
-      // before the CTA releases its shared memory and TMEM.
-      if (lane == 0) {
-        flag(status, HYB_DEVERR_TIMEOUT);
-        tc_commit(&bars->drain);
-        mbar_wait(&bars->drain, 0, 100000000ull);
-        for (int cc = consumed; cc < issued; ++cc)
-          mbar_wait(&bars->full[cc % kNST], (cc / kNST) & 1, 100000000ull);
+        for (int part = 0; part < 2; ++part) {   // (b) O^T = S^T Q^T, hi then lo
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t a = (part ? la : ha) + k * 2048;
+            const uint32_t boff = (k >> 2) * kSub + (k & 3) * 32;
+            tc_mma(od, sw128_desc(a, 16384, 1024), sw128_desc(qa + boff, 16, 1024), kIdescB,
+                   (part | k) != 0);
+          }
+        }
+        tc_commit(&bars->b_done);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {            // (a) P = Q K^T
+          const uint32_t off = (k >> 2) * kSub + (k & 3) * 32;
+          tc_mma(tmem + kColP + ob * 64, sw128_desc(qa + off, 16, 1024),
+                 sw128_desc(ka + off, 16, 1024), kIdescA, k > 0);
+        }
+        tc_commit(&bars->p_ready[ob]);
       }
       __syncwarp();
+      if (c >= 1) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_written[(c - 1) & 1], ((c - 1) >> 1) & 1));
+        if (!ok) break;
+        issue_c(c - 1);
+      }
+    }
+    if (ok) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_written[(nch - 1) & 1], ((nch - 1) >> 1) & 1));
+      if (ok) issue_c(nch - 1);
+    }
+    if (!ok && lane == 0) {                  // let every issued MMA finish before exiting
+      flag(status, HYB_DEVERR_TIMEOUT);
+      tc_commit(&bars->drain);
+      mbar_wait(&bars->drain, 0, 100000000ull);
     }
   } else {
     // ------------------------------------------------------------ conversion warps
     const int quarter = warp & 3, hf = warp >> 2;
     const int row = quarter * 32 + lane;                 // TMEM lane of this thread
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t soff0 = (row >> 3) * 1024;            // k-row group of the S^T operand
     bool ok = true;
-    // initial state -> TMEM (fp32) and S^T hi/lo operands
-    auto put_state = [&](const float* v, int j0) {       // 32 values, columns j0..j0+31
-      const int mb = j0 >> 6;                            // MN block of the operand
+    // hi/lo bf16 parts of 8 consecutive state values
+    auto split8 = [](const float* v, uint4& hi, uint4& lo) {
+      uint32_t hw[4], lw[4];
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t hi4[4], lo4[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float x0 = v[ch * 8 + 2 * e], x1 = v[ch * 8 + 2 * e + 1];
-          const __nv_bfloat16 h0 = __float2bfloat16_rn(x0), h1 = __float2bfloat16_rn(x1);
-          hi4[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-          lo4[e] = pack_bf16(x0 - __bfloat162float(h0), x1 - __bfloat162float(h1));
-        }
-        const int c16 = ((j0 & 63) >> 3) + ch;
-        const uint32_t off = mb * 16384 + (row >> 3) * 1024 + sw128_off(row & 7, c16);
-        *reinterpret_cast<uint4*>(s_hi + off) = make_uint4(hi4[0], hi4[1], hi4[2], hi4[3]);
-        *reinterpret_cast<uint4*>(s_lo + off) = make_uint4(lo4[0], lo4[1], lo4[2], lo4[3]);
+      for (int e = 0; e < 4; ++e) {
+        const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
+        hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
+        lw[e] = pack_bf16(v[2 * e] - __bfloat162float(h0), v[2 * e + 1] - __bfloat162float(h1));
       }
+      hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+      lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
     };
-    {
+    // this thread's part of the S^T operands: k-row `row`, value columns hf*64 .. +63
+    auto put8 = [&](int ch, const uint4& hi, const uint4& lo) {   // ch = chunk 0..7 of MN block hf
+      const uint32_t off = hf * 16384 + soff0 + sw128_off(row & 7, ch);
+      *reinterpret_cast<uint4*>(s_hi + off) = hi;
+      *reinterpret_cast<uint4*>(s_lo + off) = lo;
+    };
+    // O^T of chunk cc -> global: this thread owns value dim j = row, tokens hf*32 .. +31
+    auto store_out = [&](int cc) -> bool {
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_ready[cc & 1], (cc >> 1) & 1))) return false;
+      tc_fence_after();
       float v[32];
+      tmem_ld32(tl + kColO + (cc & 1) * 64 + hf * 32, v);
+      tmem_ld_wait();
+      const int nv = min(kC, n - cc * kC) - hf * 32;     // valid tokens of this half
+      __nv_bfloat16* o = out + ((int64_t)(t0 + cc * kC + hf * 32) * H + h) * kD + row;
+      const int64_t step = (int64_t)H * kD;               // one token further
+#pragma unroll
+      for (int e = 0; e < 32; ++e) {
+        if (e < nv) *o = __float2bfloat16_rn(v[e]);
+        o += step;
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[cc & 1]);
+      return true;
+    };
+    {                                                    // initial state, 32 columns at a time
+#pragma unroll 1
       for (int part = 0; part < 2; ++part) {
         const int j0 = hf * 64 + part * 32;
+        float v[32];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          float4 x = zero_start ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                : *reinterpret_cast<const float4*>(Sg + (int64_t)row * kD + j0 + e);
+          const float4 x = zero_start ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                      : *reinterpret_cast<const float4*>(Sg + (int64_t)row * kD + j0 + e);
           v[e] = x.x; v[e + 1] = x.y; v[e + 2] = x.z; v[e + 3] = x.w;
         }
         tmem_st32(tl + kColS + j0, v);
-        put_state(v, j0);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint4 hi, lo;
+          split8(v + ch * 8, hi, lo);
+          put8(part * 4 + ch, hi, lo);
+        }
       }
       tmem_st_wait();
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->s_written);
     }
-    for (int c = 0; c < nch && ok; ++c) {
-      const int nvalid = min(kC, n - c * kC);
-      float v[32];
-      // ---- tril(P) -> shared (K-major [t][t'])
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_ready, c & 1));
-      if (!ok) break;
-      tc_fence_after();
-      tmem_ld32(tl + kColP + hf * 32, v);
-      tmem_ld_wait();
-      if (lane < 16) {
-        const int t = quarter * 16 + lane;               // M = 64 layout: lanes 0..15 of each quarter
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint32_t w[4];
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            const int tp = hf * 32 + ch * 8 + 2 * e;
-            w[e] = pack_bf16(tp <= t ? v[ch * 8 + 2 * e] : 0.f, tp + 1 <= t ? v[ch * 8 + 2 * e + 1] : 0.f);
-          }
-          *reinterpret_cast<uint4*>(p_tile + sw128_off(t, hf * 4 + ch)) = make_uint4(w[0], w[1], w[2], w[3]);
-        }
-      }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars->p_written);
-      // ---- state: next chunk's S^T hi/lo operands, or the final state to global
+    for (int c = 0; c < nch; ++c) {
+      const bool last = c == nch - 1;
+      // ---- new state: read it from TMEM; write the hi/lo operand once (b) has used the old one
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_ready, c & 1));
       if (!ok) break;
       tc_fence_after();
-      const bool last = c == nch - 1;
-      for (int part = 0; part < 2; ++part) {
-        const int j0 = hf * 64 + part * 32;
-        tmem_ld32(tl + kColS + j0, v);
-        tmem_ld_wait();
-        if (last) {
+      if (last) {
+#pragma unroll 1
+        for (int part = 0; part < 2; ++part) {
+          const int j0 = hf * 64 + part * 32;
+          float v[32];
+          tmem_ld32(tl + kColS + j0, v);
+          tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(Sg + (int64_t)row * kD + j0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
-        } else {
-          put_state(v, j0);
+        }
+      } else {
+        // first 32 columns split before (b) releases the old operand, the rest after:
+        // keeps the live registers within the 10-warp budget
+        uint4 hi[4], lo[4];
+        {
+          float v[32];
+          tmem_ld32(tl + kColS + hf * 64, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) split8(v + ch * 8, hi[ch], lo[ch]);
+        }
+        float v2[32];
+        tmem_ld32(tl + kColS + hf * 64 + 32, v2);
+        tmem_ld_wait();
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->b_done, c & 1));
+        if (!ok) break;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) put8(ch, hi[ch], lo[ch]);
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          uint4 h2, l2;
+          split8(v2 + ch * 8, h2, l2);
+          put8(4 + ch, h2, l2);
+        }
+        fence_async_smem();
+      }
+      tc_fence_before();
+      mbar_arrive(&bars->s_written);
+      // ---- tril(P) -> shared (K-major [t][t']), buffer c & 1
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_ready[c & 1], (c >> 1) & 1));
+      if (!ok) break;
+      tc_fence_after();
+      {
+        float v[32];
+        tmem_ld32(tl + kColP + (c & 1) * 64 + hf * 32, v);
+        tmem_ld_wait();
+        uint8_t* const pt = p_tile + (c & 1) * kSub;
+        if (lane < 16) {
+          const int t = quarter * 16 + lane;             // M = 64 layout: lanes 0..15 of each quarter
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const int tp = hf * 32 + ch * 8 + 2 * e;
+              w[e] = pack_bf16(tp <= t ? v[ch * 8 + 2 * e] : 0.f, tp + 1 <= t ? v[ch * 8 + 2 * e + 1] : 0.f);
+            }
+            *reinterpret_cast<uint4*>(pt + sw128_off(t, hf * 4 + ch)) = make_uint4(w[0], w[1], w[2], w[3]);
+          }
         }
       }
       fence_async_smem();
       tc_fence_before();
-      mbar_arrive(&bars->s_written);
-      // ---- O^T -> global: this thread owns value dim j = row, tokens hf*32 .. hf*32+31
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready, c & 1));
-      if (!ok) break;
-      tc_fence_after();
-      tmem_ld32(tl + kColO + hf * 32, v);
-      tmem_ld_wait();
-      __nv_bfloat16* o = out + ((int64_t)(t0 + c * kC) * H + h) * kD + row;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int t = hf * 32 + e;
-        if (t < nvalid) o[(int64_t)t * H * kD] = __float2bfloat16_rn(v[e]);
+      mbar_arrive(&bars->p_written[c & 1]);
+      // ---- output of the previous chunk (its (c) is issued after this chunk's (a))
+      if (c >= 1) {
+        ok = store_out(c - 1);
+        if (!ok) break;
       }
-      tc_fence_before();
-      mbar_arrive(&bars->o_read);
     }
+    if (ok) ok = store_out(nch - 1);
     if (!ok && lane == 0) flag(status, HYB_DEVERR_TIMEOUT);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kNCW) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
@@ -346,9 +414,7 @@ cudaError_t launch_linear_prefill_tc(void* out, const void* q, const void* k, co
                                      cudaStream_t s) {
   (void)max_len;
   (void)C;
-  if (B == 0 || T == 0) {
-    if (B == 0) return cudaSuccess;
-  }
+  if (B == 0) return cudaSuccess;
   CUtensorMap mq, mk, mv;
   const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)H, (uint64_t)(T > 0 ? T : 1)};
   const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)H * kD * 2};

@@ -6,16 +6,19 @@
 // read through the per-request block table (§2.1) so a cached prefix is attended as well.
 //
 // GB300 design. One CTA per (128-query tile, head, request); heavy (late) query tiles are
-// scheduled first. K and V come straight from the paged pool: each 128-key tile is eight
-// 16-token blocks, each fetched with two TMA boxes (16 rows x 64 columns, SW128) at the
-// row the block table names, into a 3-deep K ring and a 2-deep V ring. Per key tile:
+// scheduled first. Warp roles: a TMA warp, an MMA warp and four softmax warps (one query
+// row per thread). K and V come straight from the paged pool: each 128-key tile is eight
+// 16-token blocks, each fetched with two TMA boxes (16 rows x 64 columns, SW128) at the row
+// the block table names, into a 3-deep K ring and a 2-deep V ring; the TMA warp reads the
+// block ids 32 at a time (four tiles) and shares them with shuffles. Per key tile:
 //   S = Q K^T     128 x 128 x 128  A = Q (K-major), B = K (K-major)    -> TMEM, 2 buffers
 //   O += P V      128 x 128 x 128  A = P (K-major), B = V (MN-major)   -> TMEM
-// Four softmax warps own one query row each: TMEM -> registers, causal/length mask,
-// online max, exp2, bf16 P -> shared memory. O stays in TMEM; a row is rescaled only when
+// The softmax warps read S from TMEM, apply the causal/length mask, keep the running max
+// and sum, and write bf16 P to shared memory. O stays in TMEM; a row is rescaled only when
 // its running max grows by more than 2^8 (exponents stay <= 2^8, exact after the final
-// division by the row sum). S double-buffering lets Q K^T of the next tile run on the
-// tensor core while the softmax warps work on the current one. One warp issues TMA and MMA.
+// division by the row sum). S is double-buffered so Q K^T of tile j+2 and P V of tile j run
+// on the tensor core while the softmax warps exponentiate tile j+1; they wait for P V of
+// tile j only to overwrite P (and to rescale O when needed).
 #include <cuda_bf16.h>
 
 #include "tc.cuh"
@@ -34,7 +37,8 @@ constexpr int kOffP = kOffV + kNV * kTile;
 constexpr int kOffBar = kOffP + kTile;
 constexpr int kSmem = kOffBar + 256 + 1024;
 constexpr int kNSW = 4;                      // softmax warps
-constexpr int kThreads = (kNSW + 1) * 32;
+constexpr int kWarpTma = kNSW, kWarpMma = kNSW + 1;
+constexpr int kThreads = (kNSW + 2) * 32;
 constexpr uint32_t kTmemCols = 512;          // S0 [0,128) | S1 [128,256) | O [256,384)
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;
@@ -76,7 +80,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
   Bars* bars = reinterpret_cast<Bars*>(sm + kOffBar);
   __shared__ uint32_t tmem_base;
 
-  if (warp == kNSW) {
+  if (warp == kWarpMma) {
     if (lane == 0) {
       mbar_init(&bars->qfull, 1);
       for (int i = 0; i < kNK; ++i) { mbar_init(&bars->kfull[i], 1); mbar_init(&bars->kempty[i], 1); }
@@ -87,9 +91,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       mbar_init(&bars->odone, 1);
       mbar_init(&bars->drain, 1);
       fence_mbar_init();
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
     }
     __syncwarp();
     tmem_alloc(&tmem_base, kTmemCols);
@@ -101,49 +102,87 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
   uint8_t* const q_s = sm + kOffQ;
   uint8_t* const p_s = sm + kOffP;
 
-  if (warp == kNSW) {
-    // ------------------------------------------------------------ TMA + MMA warp
+  if (warp == kWarpTma) {
+    // ------------------------------------------------------------ TMA warp
     bool ok = true;
-    int k_issued = 0, v_issued = 0, k_used = 0, v_used = 0;
-    // one 128-key tile: 8 blocks x 2 boxes; blocks past kv_end (or with a bad id) are
-    // skipped. Returns the bytes requested.
-    auto load_kv = [&](const CUtensorMap* map, uint8_t* dst, int j, uint64_t* bar) {
-      int blk_ok[8];
-      int nbox = 0;
-#pragma unroll
-      for (int bi = 0; bi < 8; ++bi) {
-        const int lb = j * 8 + bi;
-        int pb = -1;
-        if (lb * 16 < kv_end) {
-          pb = btrow[lb];
-          if (pb < 0 || pb >= NB) { flag(status, HYB_DEVERR_BAD_BLOCK); pb = -1; }
-        }
-        blk_ok[bi] = pb;
-        nbox += pb >= 0 ? 2 : 0;
-      }
-      mbar_expect_tx(bar, nbox * 2048);
-#pragma unroll
-      for (int bi = 0; bi < 8; ++bi)
-        if (blk_ok[bi] >= 0) {
-          const int y = (blk_ok[bi] * H + h) * 16;
-          tma_load_2d(dst + bi * 2048, map, 0, y, bar);
-          tma_load_2d(dst + kSubQ + bi * 2048, map, 64, y, bar);
-        }
-    };
+    int k_issued = 0, v_issued = 0;
     if (lane == 0) {
+      tma_prefetch_desc(&tq);
+      tma_prefetch_desc(&tk);
+      tma_prefetch_desc(&tv);
       mbar_expect_tx(&bars->qfull, kTile);
       tma_load_3d(q_s, &tq, 0, h, t0 + q0, &bars->qfull);
       tma_load_3d(q_s + kSubQ, &tq, 64, h, t0 + q0, &bars->qfull);
-      for (int j = 0; j < min(kNK, nkv); ++j) load_kv(&tk, sm + kOffK + j * kTile, j, &bars->kfull[j]);
-      for (int j = 0; j < min(kNV, nkv); ++j) load_kv(&tv, sm + kOffV + j * kTile, j, &bars->vfull[j]);
     }
-    k_issued = min(kNK, nkv);
-    v_issued = min(kNV, nkv);
+    int ids = -1;                                      // block ids of 4 tiles, one per lane
+    for (int j = 0; j < nkv; ++j) {
+      if ((j & 3) == 0) {
+        const int lb = j * 8 + lane;
+        ids = -1;
+        if (lb * 16 < kv_end) {
+          ids = btrow[lb];
+          if (ids < 0 || ids >= NB) {
+            flag(status, HYB_DEVERR_BAD_BLOCK);
+            ids = -1;
+          }
+        }
+      }
+      int blk[8];
+      int nbox = 0;
+#pragma unroll
+      for (int bi = 0; bi < 8; ++bi) {
+        blk[bi] = __shfl_sync(0xffffffffu, ids, (j & 3) * 8 + bi);
+        nbox += blk[bi] >= 0 ? 2 : 0;
+      }
+      if (j >= kNK) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->kempty[j % kNK], ((j - kNK) / kNK) & 1));
+        if (!ok) break;
+      }
+      if (lane == 0) {
+        uint8_t* dst = sm + kOffK + (j % kNK) * kTile;
+        uint64_t* bar = &bars->kfull[j % kNK];
+        mbar_expect_tx(bar, nbox * 2048);
+#pragma unroll
+        for (int bi = 0; bi < 8; ++bi)
+          if (blk[bi] >= 0) {
+            const int y = (blk[bi] * H + h) * 16;
+            tma_load_2d(dst + bi * 2048, &tk, 0, y, bar);
+            tma_load_2d(dst + kSubQ + bi * 2048, &tk, 64, y, bar);
+          }
+      }
+      k_issued = j + 1;
+      if (j >= kNV) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->vempty[j % kNV], ((j - kNV) / kNV) & 1));
+        if (!ok) break;
+      }
+      if (lane == 0) {
+        uint8_t* dst = sm + kOffV + (j % kNV) * kTile;
+        uint64_t* bar = &bars->vfull[j % kNV];
+        mbar_expect_tx(bar, nbox * 2048);
+#pragma unroll
+        for (int bi = 0; bi < 8; ++bi)
+          if (blk[bi] >= 0) {
+            const int y = (blk[bi] * H + h) * 16;
+            tma_load_2d(dst + bi * 2048, &tv, 0, y, bar);
+            tma_load_2d(dst + kSubQ + bi * 2048, &tv, 64, y, bar);
+          }
+      }
+      v_issued = j + 1;
+    }
+    if (!ok && lane == 0) {                            // let the loads in flight land
+      flag(status, HYB_DEVERR_TIMEOUT);
+      for (int j = max(0, k_issued - kNK); j < k_issued; ++j)
+        mbar_wait(&bars->kfull[j % kNK], (j / kNK) & 1, 100000000ull);
+      for (int j = max(0, v_issued - kNV); j < v_issued; ++j)
+        mbar_wait(&bars->vfull[j % kNV], (j / kNV) & 1, 100000000ull);
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA warp
+    bool ok = true;
     const uint32_t qa = smem_u32(q_s), pa = smem_u32(p_s);
     auto issue_qk = [&](int j) -> bool {           // S[j%2] = Q K_j^T
       const int ks = j % kNK;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->kfull[ks], (j / kNK) & 1))) return false;
-      k_used = j + 1;
       if (lane == 0) {
         tc_fence_after();
         const uint32_t ka = smem_u32(sm + kOffK + ks * kTile);
@@ -163,19 +202,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     if (ok) ok = issue_qk(0);
     if (ok && nkv > 1) ok = issue_qk(1);
     for (int j = 0; j < nkv && ok; ++j) {
-      // refill the K slot of tile j with tile j + kNK once Q K_j^T is done
-      if (j + kNK < nkv) {
-        ok = mbar_wait(&bars->kempty[j % kNK], (j / kNK) & 1);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        if (lane == 0) load_kv(&tk, sm + kOffK + (j % kNK) * kTile, j + kNK, &bars->kfull[j % kNK]);
-        k_issued = j + kNK + 1;
-      }
-      // P_j ready (softmax of tile j done, O corrected) and V_j landed
       const int vs = j % kNV;
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->pfull, j & 1));
       ok = ok && __all_sync(0xffffffffu, mbar_wait(&bars->vfull[vs], (j / kNV) & 1));
       if (!ok) break;
-      v_used = j + 1;
       uint8_t* v_s = sm + kOffV + vs * kTile;
       if ((j + 1) * kBN > kv_end) {                // last tile: V rows past kv_end := 0
         const int first = kv_end - j * kBN;
@@ -199,27 +229,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         tc_commit(&bars->vempty[vs]);
       }
       __syncwarp();
-      // next Q K^T into the S buffer tile j used (its softmax is done)
-      if (j + 2 < nkv) {
-        ok = issue_qk(j + 2);
-        if (!ok) break;
-      }
-      // refill the V slot of tile j with tile j + kNV once P V_j is done
-      if (j + kNV < nkv) {
-        ok = mbar_wait(&bars->vempty[vs], (j / kNV) & 1);
-        if (!__all_sync(0xffffffffu, ok)) { ok = false; break; }
-        if (lane == 0) load_kv(&tv, sm + kOffV + vs * kTile, j + kNV, &bars->vfull[vs]);
-        v_issued = j + kNV + 1;
-      }
+      if (j + 2 < nkv) ok = issue_qk(j + 2);       // into the S buffer tile j used
     }
     if (!ok && lane == 0) {
       flag(status, HYB_DEVERR_TIMEOUT);
       tc_commit(&bars->drain);
       mbar_wait(&bars->drain, 0, 100000000ull);
-      for (int j = k_used; j < k_issued; ++j) mbar_wait(&bars->kfull[j % kNK], (j / kNK) & 1, 100000000ull);
-      for (int j = v_used; j < v_issued; ++j) mbar_wait(&bars->vfull[j % kNV], (j / kNV) & 1, 100000000ull);
     }
-    __syncwarp();
   } else {
     // ------------------------------------------------------------ softmax warps
     const int r = warp * 32 + lane;                    // query row of the tile = TMEM lane
@@ -227,33 +243,48 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const int qp = pos0 + r;                           // absolute query position
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    float x[kBN];
     for (int j = 0; j < nkv && ok; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->sfull[j & 1], (j >> 1) & 1));
       if (!ok) break;
       tc_fence_after();
+      float x[kBN];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(tl + (j & 1) * 128 + c * 32, x + c * 32);
       tmem_ld_wait();
       const int kbase = j * kBN;
       const bool masked = kbase + kBN - 1 > pos0 || kbase + kBN > kv_end;
-      float mx = -INFINITY;
       if (masked) {
 #pragma unroll
         for (int c = 0; c < kBN; ++c) {
           const int kp = kbase + c;
-          x[c] = (kp <= qp && kp < kv_end) ? x[c] * scale_log2 : -INFINITY;
-          mx = fmaxf(mx, x[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < kBN; ++c) {
-          x[c] *= scale_log2;
-          mx = fmaxf(mx, x[c]);
+          x[c] = (kp <= qp && kp < kv_end) ? x[c] : -INFINITY;
         }
       }
+      // row max of the raw scores (scale > 0 keeps the order): 8 independent chains
+      float mp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mp[i] = x[i];
+#pragma unroll
+      for (int c = 8; c < kBN; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * scale_log2;
       const float m_new = fmaxf(m_used, mx);
       const bool grow = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new != -INFINITY);
+      const float m_tgt = grow ? m_new : m_used;
+      // exponentials of this tile first: they do not depend on P V of the previous tile.
+      // p = 2^(x * scale_log2 - m) as one fma per element; sum in 8 independent chains.
+      uint32_t w[kBN / 2];
+      float sp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) sp[i] = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBN / 2; ++c) {
+        const float p0 = fast_exp2(fmaf(x[2 * c], scale_log2, -m_tgt));
+        const float p1 = fast_exp2(fmaf(x[2 * c + 1], scale_log2, -m_tgt));
+        sp[c & 7] += p0 + p1;
+        w[c] = pack_bf16(p0, p1);
+      }
+      const float ls = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
       if (j > 0) {                                     // P V_{j-1} done: P buffer and O free
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone, (j - 1) & 1));
         if (!ok) break;
@@ -273,22 +304,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
           if (grow) l *= alpha;
         }
       }
-      if (grow) m_used = m_new;
-      float ls = 0.f;
-#pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = fast_exp2(x[c16 * 8 + 2 * e] - m_used);
-          const float p1 = fast_exp2(x[c16 * 8 + 2 * e + 1] - m_used);
-          ls += p0 + p1;
-          w[e] = pack_bf16(p0, p1);
-        }
-        *reinterpret_cast<uint4*>(p_s + (c16 >> 3) * kSubQ + sw128_off(r, c16 & 7)) =
-            make_uint4(w[0], w[1], w[2], w[3]);
-      }
+      m_used = m_tgt;
       l += ls;
+#pragma unroll
+      for (int c16 = 0; c16 < 16; ++c16)
+        *reinterpret_cast<uint4*>(p_s + (c16 >> 3) * kSubQ + sw128_off(r, c16 & 7)) =
+            make_uint4(w[4 * c16], w[4 * c16 + 1], w[4 * c16 + 2], w[4 * c16 + 3]);
       fence_async_smem();
       tc_fence_before();
       mbar_arrive(&bars->pfull);
@@ -307,12 +328,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         if (store) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
-            uint4 w;
-            w.x = pack_bf16(o[e] * inv, o[e + 1] * inv);
-            w.y = pack_bf16(o[e + 2] * inv, o[e + 3] * inv);
-            w.z = pack_bf16(o[e + 4] * inv, o[e + 5] * inv);
-            w.w = pack_bf16(o[e + 6] * inv, o[e + 7] * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + e) = w;
+            uint4 wv;
+            wv.x = pack_bf16(o[e] * inv, o[e + 1] * inv);
+            wv.y = pack_bf16(o[e + 2] * inv, o[e + 3] * inv);
+            wv.z = pack_bf16(o[e + 4] * inv, o[e + 5] * inv);
+            wv.w = pack_bf16(o[e + 6] * inv, o[e + 7] * inv);
+            *reinterpret_cast<uint4*>(orow + c * 32 + e) = wv;
           }
         }
       }
@@ -323,7 +344,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kNSW) tmem_dealloc(tmem, kTmemCols);
+  if (warp == kWarpMma) tmem_dealloc(tmem, kTmemCols);
 }
 
 }  // namespace
