@@ -161,16 +161,20 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
     // Issue order per chunk c: (d)_c, (b)_c, (a)_c, then (c)_{c-1} -- the output update of
     // the previous chunk goes last so the next state update never waits for P's conversion.
     bool ok = true;
-    const uint32_t ha = smem_u32(s_hi), la = smem_u32(s_lo), pa = smem_u32(p_tile);
+    // descriptors built once; every MMA below adds an offset (see desc_add)
+    const uint32_t sm0 = smem_u32(sm);
+    const uint64_t mn0 = sw128_desc(sm0, kSub, 1024);          // MN-major, 64-row sub-tiles
+    const uint64_t km0 = sw128_desc(sm0, 16, 1024);            // K-major
+    const uint64_t st0 = sw128_desc(sm0 + kOffS, 16384, 1024); // S^T hi (lo at +kSTile)
     auto issue_c = [&](int c) {                  // (c) O^T += V^T tril(P)^T of chunk c
       const int st = c % kNST, pb = c & 1;
-      const uint32_t va = smem_u32(sm + st * kStage + 2 * kTile);
+      const uint32_t vo = st * kStage + 2 * kTile, po = kOffP + pb * kSub;
       if (lane == 0) {
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 4; ++k)
-          tc_mma(tmem + kColO + pb * 64, sw128_desc(va + k * 2048, kSub, 1024),
-                 sw128_desc(pa + pb * kSub + k * 32, 16, 1024), kIdescC, 1);
+          tc_mma(tmem + kColO + pb * 64, desc_add(mn0, vo + k * 2048), desc_add(km0, po + k * 32),
+                 kIdescC, 1);
         tc_commit(&bars->o_ready[pb]);
         tc_commit(&bars->empty[st]);
       }
@@ -181,7 +185,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
       uint8_t* qs = sm + st * kStage;
       uint8_t* ks = qs + kTile;
       uint8_t* vs = ks + kTile;
-      const uint32_t qa = smem_u32(qs), ka = smem_u32(ks), va = smem_u32(vs);
+      const uint32_t qo = st * kStage, ko = qo + kTile, vo = ko + kTile;   // byte offsets in sm
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->full[st], (c / kNST) & 1));
       if (!ok) break;
       const int nvalid = min(kC, n - c * kC);
@@ -201,8 +205,8 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
         tc_fence_after();
 #pragma unroll
         for (int k = 0; k < 4; ++k)              // (d) S += K^T V
-          tc_mma(tmem + kColS, sw128_desc(ka + k * 2048, kSub, 1024),
-                 sw128_desc(va + k * 2048, kSub, 1024), kIdescD, 1);
+          tc_mma(tmem + kColS, desc_add(mn0, ko + k * 2048), desc_add(mn0, vo + k * 2048),
+                 kIdescD, 1);
         tc_commit(&bars->s_ready);
       }
       if (c >= 2) {
@@ -216,9 +220,8 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
         for (int part = 0; part < 2; ++part) {   // (b) O^T = S^T Q^T, hi then lo
 #pragma unroll
           for (int k = 0; k < 8; ++k) {
-            const uint32_t a = (part ? la : ha) + k * 2048;
             const uint32_t boff = (k >> 2) * kSub + (k & 3) * 32;
-            tc_mma(od, sw128_desc(a, 16384, 1024), sw128_desc(qa + boff, 16, 1024), kIdescB,
+            tc_mma(od, desc_add(st0, part * kSTile + k * 2048), desc_add(km0, qo + boff), kIdescB,
                    (part | k) != 0);
           }
         }
@@ -226,8 +229,8 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
 #pragma unroll
         for (int k = 0; k < 8; ++k) {            // (a) P = Q K^T
           const uint32_t off = (k >> 2) * kSub + (k & 3) * 32;
-          tc_mma(tmem + kColP + ob * 64, sw128_desc(qa + off, 16, 1024),
-                 sw128_desc(ka + off, 16, 1024), kIdescA, k > 0);
+          tc_mma(tmem + kColP + ob * 64, desc_add(km0, qo + off), desc_add(km0, ko + off), kIdescA,
+                 k > 0);
         }
         tc_commit(&bars->p_ready[ob]);
       }

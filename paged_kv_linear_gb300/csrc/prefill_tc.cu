@@ -6,19 +6,22 @@
 // read through the per-request block table (§2.1) so a cached prefix is attended as well.
 //
 // GB300 design. One CTA per (128-query tile, head, request); heavy (late) query tiles are
-// scheduled first. Warp roles: a TMA warp, an MMA warp and four softmax warps (one query
-// row per thread). K and V come straight from the paged pool: each 128-key tile is eight
+// scheduled first. Warp roles: two TMA warps (K ring, V ring), an MMA warp and eight
+// softmax warps. K and V come straight from the paged pool: each 128-key tile is eight
 // 16-token blocks, each fetched with two TMA boxes (16 rows x 64 columns, SW128) at the row
-// the block table names, into a 3-deep K ring and a 2-deep V ring; the TMA warp reads the
+// the block table names, into a 3-deep K ring and a 2-deep V ring; each TMA warp reads the
 // block ids 32 at a time (four tiles) and shares them with shuffles. Per key tile:
 //   S = Q K^T     128 x 128 x 128  A = Q (K-major), B = K (K-major)    -> TMEM, 2 buffers
-//   O += P V      128 x 128 x 128  A = P (K-major), B = V (MN-major)   -> TMEM
-// The softmax warps read S from TMEM, apply the causal/length mask, keep the running max
-// and sum, and write bf16 P to shared memory. O stays in TMEM; a row is rescaled only when
-// its running max grows by more than 2^8 (exponents stay <= 2^8, exact after the final
-// division by the row sum). S is double-buffered so Q K^T of tile j+2 and P V of tile j run
-// on the tensor core while the softmax warps exponentiate tile j+1; they wait for P V of
-// tile j only to overwrite P (and to rescale O when needed).
+//   O += P V      128 x 128 x 128  A = P (TMEM),    B = V (MN-major)   -> TMEM
+// Each query row is split over two softmax threads (two warps, 64 columns each) that swap
+// their partial row max through shared memory once per tile. They apply the causal/length
+// mask, keep the running max and sum, and write bf16 P back into TMEM (two buffers), where
+// P V reads it as its A operand: P never touches shared memory, which leaves the tensor
+// core's shared-memory bandwidth to Q, K and V. O stays in TMEM; a row is rescaled only
+// when its running max grows by more than 2^8 (exponents stay <= 2^8, exact after the
+// final division by the row sum). S is double-buffered so Q K^T of tile j+2 and P V of
+// tile j run on the tensor core while the softmax threads exponentiate tile j+1; they wait
+// for P V only to reuse a P buffer (two tiles back) or to rescale O.
 #include <cuda_bf16.h>
 
 #include "tc.cuh"
@@ -33,22 +36,23 @@ constexpr int kNK = 3, kNV = 2;              // K and V ring depths
 constexpr int kOffQ = 0;
 constexpr int kOffK = kOffQ + kTile;
 constexpr int kOffV = kOffK + kNK * kTile;
-constexpr int kOffP = kOffV + kNV * kTile;
-constexpr int kOffBar = kOffP + kTile;
-constexpr int kSmem = kOffBar + 256 + 1024;
-constexpr int kNSW = 4;                      // softmax warps
-constexpr int kWarpTma = kNSW, kWarpMma = kNSW + 1;
-constexpr int kThreads = (kNSW + 2) * 32;
-constexpr uint32_t kTmemCols = 512;          // S0 [0,128) | S1 [128,256) | O [256,384)
-constexpr uint32_t kColO = 256;
+constexpr int kOffBar = kOffV + kNV * kTile;
+constexpr int kSmem = kOffBar + 4096 + 1024;
+constexpr int kNSW = 8;                      // softmax warps: 2 per TMEM lane quarter
+constexpr int kWarpTmaK = kNSW, kWarpTmaV = kNSW + 1, kWarpMma = kNSW + 2;
+constexpr int kThreads = (kNSW + 3) * 32;
+constexpr uint32_t kTmemCols = 512;          // S0 | S1 | O | P0 | P1 (P: bf16 pairs)
+constexpr uint32_t kColO = 256, kColP = 384;
 constexpr float kRescaleLog2 = 8.f;
 
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0, 0);
-constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 0, 1);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 0, 1);   // A = P from TMEM
 
 struct Bars {
   uint64_t qfull, kfull[kNK], kempty[kNK], vfull[kNV], vempty[kNV];
-  uint64_t sfull[2], pfull, odone, drain;
+  uint64_t sfull[2], pfull[2], odone[2], drain;   // handshakes per tile parity
+  uint64_t pair[4][2];                       // the two warps of a lane quarter, per parity
+  float red[2][2][kBM];                      // row-half partial max per parity; final sums
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -87,9 +91,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       for (int i = 0; i < kNV; ++i) { mbar_init(&bars->vfull[i], 1); mbar_init(&bars->vempty[i], 1); }
       mbar_init(&bars->sfull[0], 1);
       mbar_init(&bars->sfull[1], 1);
-      mbar_init(&bars->pfull, kNSW * 32);
-      mbar_init(&bars->odone, 1);
+      mbar_init(&bars->pfull[0], kNSW * 32);
+      mbar_init(&bars->pfull[1], kNSW * 32);
+      mbar_init(&bars->odone[0], 1);
+      mbar_init(&bars->odone[1], 1);
       mbar_init(&bars->drain, 1);
+      for (int qq = 0; qq < 4; ++qq) {
+        mbar_init(&bars->pair[qq][0], 64);
+        mbar_init(&bars->pair[qq][1], 64);
+      }
       fence_mbar_init();
     }
     __syncwarp();
@@ -100,19 +110,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   uint8_t* const q_s = sm + kOffQ;
-  uint8_t* const p_s = sm + kOffP;
 
-  if (warp == kWarpTma) {
-    // ------------------------------------------------------------ TMA warp
+  if (warp == kWarpTmaK || warp == kWarpTmaV) {
+    // ------------------------------------------------------------ TMA warps (K ring, V ring)
+    // Two independent producers so K can run ahead of V (K is needed one tile earlier).
+    const bool isk = warp == kWarpTmaK;
+    const CUtensorMap* map = isk ? &tk : &tv;
+    const int depth = isk ? kNK : kNV;
+    uint8_t* const ring = sm + (isk ? kOffK : kOffV);
+    uint64_t* const fullb = isk ? bars->kfull : bars->vfull;
+    uint64_t* const emptyb = isk ? bars->kempty : bars->vempty;
     bool ok = true;
-    int k_issued = 0, v_issued = 0;
+    int issued = 0;
     if (lane == 0) {
-      tma_prefetch_desc(&tq);
-      tma_prefetch_desc(&tk);
-      tma_prefetch_desc(&tv);
-      mbar_expect_tx(&bars->qfull, kTile);
-      tma_load_3d(q_s, &tq, 0, h, t0 + q0, &bars->qfull);
-      tma_load_3d(q_s + kSubQ, &tq, 64, h, t0 + q0, &bars->qfull);
+      tma_prefetch_desc(map);
+      if (isk) {
+        tma_prefetch_desc(&tq);
+        mbar_expect_tx(&bars->qfull, kTile);
+        tma_load_3d(q_s, &tq, 0, h, t0 + q0, &bars->qfull);
+        tma_load_3d(q_s + kSubQ, &tq, 64, h, t0 + q0, &bars->qfull);
+      }
     }
     int ids = -1;                                      // block ids of 4 tiles, one per lane
     for (int j = 0; j < nkv; ++j) {
@@ -134,63 +151,47 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         blk[bi] = __shfl_sync(0xffffffffu, ids, (j & 3) * 8 + bi);
         nbox += blk[bi] >= 0 ? 2 : 0;
       }
-      if (j >= kNK) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->kempty[j % kNK], ((j - kNK) / kNK) & 1));
+      const int slot = j % depth;
+      if (j >= depth) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&emptyb[slot], ((j - depth) / depth) & 1));
         if (!ok) break;
       }
       if (lane == 0) {
-        uint8_t* dst = sm + kOffK + (j % kNK) * kTile;
-        uint64_t* bar = &bars->kfull[j % kNK];
-        mbar_expect_tx(bar, nbox * 2048);
+        uint8_t* dst = ring + slot * kTile;
+        mbar_expect_tx(&fullb[slot], nbox * 2048);
 #pragma unroll
         for (int bi = 0; bi < 8; ++bi)
           if (blk[bi] >= 0) {
             const int y = (blk[bi] * H + h) * 16;
-            tma_load_2d(dst + bi * 2048, &tk, 0, y, bar);
-            tma_load_2d(dst + kSubQ + bi * 2048, &tk, 64, y, bar);
+            tma_load_2d(dst + bi * 2048, map, 0, y, &fullb[slot]);
+            tma_load_2d(dst + kSubQ + bi * 2048, map, 64, y, &fullb[slot]);
           }
       }
-      k_issued = j + 1;
-      if (j >= kNV) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->vempty[j % kNV], ((j - kNV) / kNV) & 1));
-        if (!ok) break;
-      }
-      if (lane == 0) {
-        uint8_t* dst = sm + kOffV + (j % kNV) * kTile;
-        uint64_t* bar = &bars->vfull[j % kNV];
-        mbar_expect_tx(bar, nbox * 2048);
-#pragma unroll
-        for (int bi = 0; bi < 8; ++bi)
-          if (blk[bi] >= 0) {
-            const int y = (blk[bi] * H + h) * 16;
-            tma_load_2d(dst + bi * 2048, &tv, 0, y, bar);
-            tma_load_2d(dst + kSubQ + bi * 2048, &tv, 64, y, bar);
-          }
-      }
-      v_issued = j + 1;
+      issued = j + 1;
     }
     if (!ok && lane == 0) {                            // let the loads in flight land
       flag(status, HYB_DEVERR_TIMEOUT);
-      for (int j = max(0, k_issued - kNK); j < k_issued; ++j)
-        mbar_wait(&bars->kfull[j % kNK], (j / kNK) & 1, 100000000ull);
-      for (int j = max(0, v_issued - kNV); j < v_issued; ++j)
-        mbar_wait(&bars->vfull[j % kNV], (j / kNV) & 1, 100000000ull);
+      for (int j = max(0, issued - depth); j < issued; ++j)
+        mbar_wait(&fullb[j % depth], (j / depth) & 1, 100000000ull);
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA warp
     bool ok = true;
-    const uint32_t qa = smem_u32(q_s), pa = smem_u32(p_s);
+    // descriptors built once; every MMA below adds a compile-time offset
+    const uint64_t qdesc = sw128_desc(smem_u32(q_s), 16, 1024);
+    const uint64_t kdesc = sw128_desc(smem_u32(sm + kOffK), 16, 1024);
+    const uint64_t vdesc = sw128_desc(smem_u32(sm + kOffV), kSubQ, 1024);
     auto issue_qk = [&](int j) -> bool {           // S[j%2] = Q K_j^T
       const int ks = j % kNK;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->kfull[ks], (j / kNK) & 1))) return false;
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t ka = smem_u32(sm + kOffK + ks * kTile);
+        const uint64_t kd = desc_add(kdesc, ks * kTile);
+        const uint32_t sd = tmem + (j & 1) * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k >> 2) * kSubQ + (k & 3) * 32;
-          tc_mma(tmem + (j & 1) * 128, sw128_desc(qa + off, 16, 1024), sw128_desc(ka + off, 16, 1024),
-                 kIdescQK, k > 0);
+          tc_mma(sd, desc_add(qdesc, off), desc_add(kd, off), kIdescQK, k > 0);
         }
         tc_commit(&bars->sfull[j & 1]);
         tc_commit(&bars->kempty[ks]);
@@ -203,8 +204,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     if (ok && nkv > 1) ok = issue_qk(1);
     for (int j = 0; j < nkv && ok; ++j) {
       const int vs = j % kNV;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->pfull, j & 1));
-      ok = ok && __all_sync(0xffffffffu, mbar_wait(&bars->vfull[vs], (j / kNV) & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->pfull[j & 1], (j >> 1) & 1));
+      if (!ok) break;
+      // softmax of tile j is done with S buffer j&1: queue Q K_{j+2} first so the softmax
+      // threads have their next-but-one scores early (an MMA issue blocks while the tensor
+      // core is busy, so issue order is execution order)
+      if (j + 2 < nkv) {
+        ok = issue_qk(j + 2);
+        if (!ok) break;
+      }
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->vfull[vs], (j / kNV) & 1));
       if (!ok) break;
       uint8_t* v_s = sm + kOffV + vs * kTile;
       if ((j + 1) * kBN > kv_end) {                // last tile: V rows past kv_end := 0
@@ -218,18 +227,16 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       __syncwarp();
       if (lane == 0) {
         tc_fence_after();
-        const uint32_t va = smem_u32(v_s);
+        const uint64_t vd = desc_add(vdesc, vs * kTile);
+        const uint32_t pt = tmem + kColP + (j & 1) * 64;
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {              // O += P V_j
-          const uint32_t aoff = (k >> 2) * kSubQ + (k & 3) * 32;
-          tc_mma(tmem + kColO, sw128_desc(pa + aoff, 16, 1024), sw128_desc(va + k * 2048, kSubQ, 1024),
-                 kIdescPV, (j > 0 || k > 0) ? 1u : 0u);
-        }
-        tc_commit(&bars->odone);
+        for (int k = 0; k < 8; ++k)                // O += P V_j, P read from TMEM buffer j&1
+          tc_mma_ta(tmem + kColO, pt + k * 8, desc_add(vd, k * 2048), kIdescPV,
+                    (j > 0 || k > 0) ? 1u : 0u);
+        tc_commit(&bars->odone[j & 1]);
         tc_commit(&bars->vempty[vs]);
       }
       __syncwarp();
-      if (j + 2 < nkv) ok = issue_qk(j + 2);       // into the S buffer tile j used
     }
     if (!ok && lane == 0) {
       flag(status, HYB_DEVERR_TIMEOUT);
@@ -238,92 +245,109 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     }
   } else {
     // ------------------------------------------------------------ softmax warps
-    const int r = warp * 32 + lane;                    // query row of the tile = TMEM lane
-    const uint32_t tl = tmem + ((uint32_t)(warp * 32) << 16);
+    const int quarter = warp & 3, hf = warp >> 2;      // TMEM lane quarter, column half
+    const int r = quarter * 32 + lane;                 // query row of the tile = TMEM lane
+    const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     const int qp = pos0 + r;                           // absolute query position
-    float m_used = -INFINITY, l = 0.f;
+    const int c0h = hf * 64;                           // this thread's 64 columns
+    float m_used = -INFINITY, l = 0.f;                 // l: this half's share of the row sum
     bool ok = true;
+    // swap a value with the other half of this row (exchange number idx); bounded wait
+    auto pair_swap = [&](int idx, float v, float& other) -> bool {
+      bars->red[idx & 1][hf][r] = v;
+      mbar_arrive(&bars->pair[quarter][idx & 1]);
+      if (!__all_sync(0xffffffffu, mbar_wait(&bars->pair[quarter][idx & 1], (idx >> 1) & 1)))
+        return false;
+      other = bars->red[idx & 1][hf ^ 1][r];
+      return true;
+    };
     for (int j = 0; j < nkv && ok; ++j) {
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->sfull[j & 1], (j >> 1) & 1));
       if (!ok) break;
       tc_fence_after();
-      float x[kBN];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(tl + (j & 1) * 128 + c * 32, x + c * 32);
+      float x[64];
+      tmem_ld32(tl + (j & 1) * 128 + c0h, x);
+      tmem_ld32(tl + (j & 1) * 128 + c0h + 32, x + 32);
       tmem_ld_wait();
-      const int kbase = j * kBN;
-      const bool masked = kbase + kBN - 1 > pos0 || kbase + kBN > kv_end;
+      const int kbase = j * kBN + c0h;
+      const bool masked = kbase + 63 > pos0 || kbase + 64 > kv_end;
       if (masked) {
 #pragma unroll
-        for (int c = 0; c < kBN; ++c) {
+        for (int c = 0; c < 64; ++c) {
           const int kp = kbase + c;
           x[c] = (kp <= qp && kp < kv_end) ? x[c] : -INFINITY;
         }
       }
-      // row max of the raw scores (scale > 0 keeps the order): 8 independent chains
+      // partial max of the raw scores (scale > 0 keeps the order): 8 independent chains
       float mp[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mp[i] = x[i];
 #pragma unroll
-      for (int c = 8; c < kBN; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * scale_log2;
+      for (int c = 8; c < 64; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
+      float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                       fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      float mx_other;
+      ok = pair_swap(j, mx, mx_other);
+      if (!ok) break;
+      mx = fmaxf(mx, mx_other) * scale_log2;
       const float m_new = fmaxf(m_used, mx);
       const bool grow = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new != -INFINITY);
       const float m_tgt = grow ? m_new : m_used;
       // exponentials of this tile first: they do not depend on P V of the previous tile.
       // p = 2^(x * scale_log2 - m) as one fma per element; sum in 8 independent chains.
-      uint32_t w[kBN / 2];
+      uint32_t w[32];
       float sp[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) sp[i] = 0.f;
 #pragma unroll
-      for (int c = 0; c < kBN / 2; ++c) {
+      for (int c = 0; c < 32; ++c) {
         const float p0 = fast_exp2(fmaf(x[2 * c], scale_log2, -m_tgt));
         const float p1 = fast_exp2(fmaf(x[2 * c + 1], scale_log2, -m_tgt));
         sp[c & 7] += p0 + p1;
         w[c] = pack_bf16(p0, p1);
       }
       const float ls = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-      if (j > 0) {                                     // P V_{j-1} done: P buffer and O free
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone, (j - 1) & 1));
+      if (j >= 2) {                                    // P V_{j-2} done: P buffer j&1 free
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone[j & 1], ((j - 2) >> 1) & 1));
+        if (!ok) break;
+      }
+      if (j >= 1 && __any_sync(0xffffffffu, grow)) {   // rescale O once P V_{j-1} is in
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone[(j - 1) & 1], ((j - 1) >> 1) & 1));
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, grow)) {           // warp-wide TMEM access, per-row factor
-          const float alpha = (grow && m_used != -INFINITY) ? fast_exp2(m_used - m_new) : 1.f;
+        const float alpha = (grow && m_used != -INFINITY) ? fast_exp2(m_used - m_new) : 1.f;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float o[32];
-            tmem_ld32(tl + kColO + c * 32, o);
-            tmem_ld_wait();
+        for (int c = 0; c < 2; ++c) {                  // warp-wide TMEM access, per-row factor
+          float o[32];
+          tmem_ld32(tl + kColO + c0h + c * 32, o);
+          tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] *= alpha;
-            tmem_st32(tl + kColO + c * 32, o);
-          }
-          tmem_st_wait();
-          if (grow) l *= alpha;
+          for (int e = 0; e < 32; ++e) o[e] *= alpha;
+          tmem_st32(tl + kColO + c0h + c * 32, o);
         }
+        if (grow) l *= alpha;
       }
       m_used = m_tgt;
       l += ls;
-#pragma unroll
-      for (int c16 = 0; c16 < 16; ++c16)
-        *reinterpret_cast<uint4*>(p_s + (c16 >> 3) * kSubQ + sw128_off(r, c16 & 7)) =
-            make_uint4(w[4 * c16], w[4 * c16 + 1], w[4 * c16 + 2], w[4 * c16 + 3]);
-      fence_async_smem();
+      tc_fence_after();
+      tmem_st32u(tl + kColP + (j & 1) * 64 + hf * 32, w);   // keys c0h..c0h+63 as bf16 pairs
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->pfull);
+      mbar_arrive(&bars->pfull[j & 1]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone, (nkv - 1) & 1));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone[(nkv - 1) & 1], ((nkv - 1) >> 1) & 1));
+    float l_other = 0.f;
+    if (ok) ok = pair_swap(nkv, l, l_other);           // row sum = both halves' shares
     if (ok) {
+      const float lt = l + l_other;
       tc_fence_after();
       const bool store = q0 + r < n;
-      const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = out + ((int64_t)(t0 + q0 + r) * H + h) * kD;
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+      __nv_bfloat16* orow = out + ((int64_t)(t0 + q0 + r) * H + h) * kD + c0h;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float o[32];
-        tmem_ld32(tl + kColO + c * 32, o);
+        tmem_ld32(tl + kColO + c0h + c * 32, o);
         tmem_ld_wait();
         if (store) {
 #pragma unroll
