@@ -204,6 +204,11 @@ def _time(fn, stream, iters, warmup=3):
     return e0.elapsed_time(e1) / iters
 
 
+def _traffic(kernel, src):
+    rec = traffic_record(kernel, src)
+    return int(rec["bytes_per_launch"]) if rec else None
+
+
 def _roof(bound, achieved, peak, unit, kernel, alg, traffic=None, **extra):
     r = {"kernel": kernel, "bound": bound, "achieved": round(achieved, 1), "peak": peak, "unit": unit,
          "frac": round(achieved / peak, 4), "traffic": traffic, "algorithmic": alg}
@@ -344,8 +349,10 @@ def row_prefill(hyb, device, stream, iters, seed=0):
            "ms": {"slot_mapping": round(t_slot, 4), "kv_append": round(t_app, 4), "prefill_causal": round(t_pf, 4),
                   "linear_chunked_prefill": round(t_lin, 4)},
            "roofline": _roof("tensor", pf_flops / (t_pf * 1e-3) / 1e12, tf, "TFLOP/s", "prefill_tc_kernel (causal, paged)",
-                             pf_flops, peak_source="measured bf16_tflops (burst)"),
+                             pf_flops, traffic=_traffic("prefill_tc", "prefill_tc.cu"),
+                             peak_source="measured bf16_tflops (burst)"),
            "linear_chunked_prefill": _roof("hbm", lin_gbs, hbm, "GB/s", "linear_prefill_tc_kernel", lin_bytes,
+                                           traffic=_traffic("linear_prefill_tc", "linear_tc.cu"),
                                            tflops=round(lin_tf, 1), tensor_frac=round(lin_tf / tf, 4),
                                            arithmetic_intensity=round(ai, 1),
                                            frac_of_min_peak_ai_bw=round(lin_tf / min(tf, ai * hbm / 1e3), 4)),
