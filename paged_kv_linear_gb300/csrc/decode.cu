@@ -6,9 +6,11 @@
 //
 // Design (GB300): the work is pure HBM streaming -- every (block, head) K and V tile is
 // a contiguous 16 x D run of the [NB][H][16][D] pool (4 KiB each at D=128, bf16), read
-// once. A CTA owns one (row, head, split) and 4 warps; each warp walks every 4th block of
-// the split through its own 3-stage ring in shared memory, filled by the TMA engine
-// (cp.async.bulk, one 4 KiB copy per tile, completion on an mbarrier). Scores and the
+// once. A CTA owns one (row, head, split of 32 blocks) and 4 warps; each warp walks every
+// 4th block of the split through its own 2-stage ring in shared memory, filled by the TMA
+// engine (cp.async.bulk, one 4 KiB copy per tile, completion on an mbarrier). The small
+// ring (64 KiB per CTA) fits three CTAs per SM, which on GB300 streams faster than deeper
+// rings with fewer resident CTAs (measured over warps x stages x split sizes). Scores and the
 // online softmax run in fp32 on the CUDA cores with warp shuffles; partial states
 // (m, l, acc[D]) of the 4 warps merge in shared memory, and splits merge in a second
 // small kernel (log-sum-exp combine). The split size is a constant number of blocks, so
@@ -24,9 +26,18 @@ namespace hyb {
 
 namespace {
 
-constexpr int kNW = 4;           // warps per CTA
-constexpr int kNST = 3;          // ring stages per warp
-constexpr int kBPS = 32;         // KV blocks per split (constant: batch-invariant results)
+#ifndef HYB_DECODE_NW
+#define HYB_DECODE_NW 4
+#endif
+#ifndef HYB_DECODE_NST
+#define HYB_DECODE_NST 2
+#endif
+#ifndef HYB_DECODE_BPS
+#define HYB_DECODE_BPS 32
+#endif
+constexpr int kNW = HYB_DECODE_NW;    // warps per CTA
+constexpr int kNST = HYB_DECODE_NST;  // ring stages per warp
+constexpr int kBPS = HYB_DECODE_BPS;  // KV blocks per split (constant: batch-invariant results)
 
 template <typename T>
 struct Elt;
