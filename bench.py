@@ -293,12 +293,24 @@ def row_hybrid_32layer(hyb, device, stream, iters, seed=0):
     step()
     launches = hyb.hyb_launch_count(reset=True)
     t = _time(step, stream, iters)
+    # the same step captured once into a CUDA graph and replayed (no per-launch host work)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        step()                                   # every first-call set-up done before capture
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    t_graph = _time(graph.replay, stream, iters)
     n_full, n_lin = int((lt == 0).sum()), int((lt == 1).sum())
     alg = n_full * (int(db.seq_lens.sum()) * H * D * 4 + 2 * B * H * D * 2) + n_lin * B * H * D * D * 8
     res = {"workload": "hybrid_32layer: [full,full,full,linear] x 8, batch 64, 80% ~lognormal(128) / 20% ~lognormal(2048)",
            "value": round(B * 32 / (t * 1e-3), 1), "unit": UNIT, "ms_per_step": round(t, 4),
            "launches_per_step": int(launches),
-           "roofline": _roof("hbm", alg / (t * 1e-3) / 1e9, hbm, "GB/s", "whole 32-layer step (dispatch)", alg)}
+           "roofline": _roof("hbm", alg / (t * 1e-3) / 1e9, hbm, "GB/s", "whole 32-layer step (dispatch)", alg),
+           "cuda_graph": {"value": round(B * 32 / (t_graph * 1e-3), 1), "ms_per_step": round(t_graph, 4),
+                          "roofline": _roof("hbm", alg / (t_graph * 1e-3) / 1e9, hbm, "GB/s",
+                                            "whole 32-layer step (graph replay)", alg)}}
+    del graph
     del keep, ios
     torch.cuda.empty_cache()
     return res

@@ -374,3 +374,58 @@ def test_dispatch_layers_use_only_their_own_pools(hyb, devstatus):
             s = int(sm[b])
             assert np.array_equal(kh[s // 16, :, s % 16], to_host(layers[l]["k"])[b])
     assert devstatus() == (0, 0)
+
+
+def test_dispatch_step_captured_in_cuda_graph_replays_bit_identically(hyb, devstatus):
+    """A whole decode step (slot mapping + 4-layer dispatch) captured into a CUDA graph and
+    replayed gives the same bytes as the eager calls (no allocation or synchronisation
+    inside the step; first-call set-up happens before capture)."""
+    H, D, B = 4, 128, 3
+    lt = [0, 0, 1, 0]
+    case = DecodeStep(41, [200, 33, 700], H, D, W.BF16)
+    d = case.dims(hyb)
+    g = W.rng(42)
+    bt, lens = to_dev(case.pool.block_tables), to_dev(case.lens)
+    cu, ctx = to_dev(case.cu), to_dev(case.ctx)
+    slots = to_dev(np.arange(B, dtype=np.int32))
+    ins = [[to_dev(W.rows(g, (B, H, D), D, W.BF16)) for _ in range(3)] for _ in lt]
+    st0 = W.synthetic_state(g, B, H, D, case.lens)
+
+    def make_state():
+        caches = [(to_dev(case.kc), to_dev(case.vc)) if t == 0 else None for t in lt]
+        pools = [to_dev(st0) if t == 1 else None for t in lt]
+        outs = [empty_rows((B, H, D), W.BF16) for _ in lt]
+        ios = [hyb.layer_io(outs[l], *ins[l], *(caches[l] or (None, None)), pools[l], B) for l in range(len(lt))]
+        return caches, pools, outs, ios
+
+    slot = torch.empty(B, dtype=torch.int64, device="cuda")
+    ws = torch.empty(1 << 20, dtype=torch.uint8, device="cuda")
+    meta = hyb.batch_meta(B, B, seq_lens=lens, block_tables=bt, slot_mapping=slot, state_slots=slots, max_seq_len=700)
+    s = torch.cuda.Stream()
+
+    def step(ios):
+        hyb.check(hyb.hyb_slot_mapping(slot, bt, cu, ctx, B, B, d, s))
+        hyb.check(hyb.hyb_layer_dispatch(lt, len(lt), 0, ios, meta, d, 64, ws, 1 << 20, s))
+
+    eager = make_state()
+    with torch.cuda.stream(s):
+        step(eager[3])
+    s.synchronize()
+    graphed = make_state()
+    warm = make_state()
+    with torch.cuda.stream(s):
+        step(warm[3])                            # first-call set-up outside the capture
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        step(graphed[3])
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager[2], graphed[2]):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    for a, b in zip(eager[0] + eager[1], graphed[0] + graphed[1]):
+        if a is None:
+            continue
+        for x, y in (zip(a, b) if isinstance(a, tuple) else [(a, b)]):
+            assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
+    assert devstatus() == (0, 0)
