@@ -51,9 +51,9 @@ def lib():
             L.oracle_slot_mapping.restype = i32
             L.oracle_kv_append.argtypes = [p, p, p, i32, i32, i32, i32, i32, p, p]
             L.oracle_kv_append.restype = None
-            L.oracle_full_decode.argtypes = [p, p, p, p, i32, p, i32, i32, i32, i32, i32, f64, p]
+            L.oracle_full_decode.argtypes = [p, p, p, p, i32, p, i32, i32, i32, i32, i32, f64, i32, p]
             L.oracle_full_decode.restype = None
-            L.oracle_full_prefill.argtypes = [p, p, p, p, i32, p, p, i32, i32, i32, i32, i32, f64, p, i32, p]
+            L.oracle_full_prefill.argtypes = [p, p, p, p, i32, p, p, i32, i32, i32, i32, i32, f64, i32, p, i32, p]
             L.oracle_full_prefill.restype = None
             L.oracle_linear_recurrence.argtypes = [p, p, p, p, i32, i32, i32, i32, p, p, p, p, p]
             L.oracle_linear_recurrence.restype = None
@@ -111,7 +111,7 @@ def kv_append(k, v, slot_map, k_cache, v_cache, block_size=BLOCK_SIZE):
                            _ptr(k_cache), _ptr(v_cache))
 
 
-def full_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, block_size=BLOCK_SIZE):
+def full_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, block_size=BLOCK_SIZE, window=0):
     q, dt = _elem(q)
     B, H, D = q.shape
     kc, _ = _elem(k_cache)
@@ -120,12 +120,12 @@ def full_decode(q, k_cache, v_cache, block_tables, seq_lens, scale, block_size=B
     sl = _c(seq_lens, np.int32)
     out = np.zeros((B, H, D), dtype=np.float64)
     lib().oracle_full_decode(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(sl), B, H, D,
-                             block_size, dt, float(scale), _ptr(out))
+                             block_size, dt, float(scale), int(window), _ptr(out))
     return out
 
 
 def full_prefill(q, k_cache, v_cache, block_tables, cu_q_lens, ctx_lens, scale, rows=None,
-                 block_size=BLOCK_SIZE):
+                 block_size=BLOCK_SIZE, window=0):
     q, dt = _elem(q)
     T, H, D = q.shape
     kc, _ = _elem(k_cache)
@@ -138,7 +138,7 @@ def full_prefill(q, k_cache, v_cache, block_tables, cu_q_lens, ctx_lens, scale, 
     out = np.zeros((n, H, D), dtype=np.float64)
     lib().oracle_full_prefill(_ptr(q), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1], _ptr(cu),
                               _ptr(_c(ctx_lens, np.int32)), B, H, D, block_size, dt, float(scale),
-                              _ptr(r), 0 if r is None else len(r), _ptr(out))
+                              int(window), _ptr(r), 0 if r is None else len(r), _ptr(out))
     return out
 
 

@@ -97,21 +97,21 @@ static double paged(const void *cache, const int32_t *bt, int MB, int b, int h, 
   return ld(cache, ((blk * H + h) * bs + p % bs) * (int64_t)D + d, dtype);
 }
 
-/* softmax(scale * q.K_p) V_p over p in [0, n), q given as doubles; two plain passes */
+/* softmax(scale * q.K_p) V_p over p in [lo, n), q given as doubles; two plain passes */
 static void attend(const double *q, const void *kc, const void *vc, const int32_t *bt, int MB,
-                   int b, int h, int64_t n, int H, int D, int bs, int dtype, double scale,
-                   double *s, double *o) {
+                   int b, int h, int64_t lo, int64_t n, int H, int D, int bs, int dtype,
+                   double scale, double *s, double *o) {
   for (int d = 0; d < D; ++d) o[d] = 0.0;
-  if (n <= 0) return;
+  if (n <= lo) return;
   double m = -INFINITY;
-  for (int64_t p = 0; p < n; ++p) {
+  for (int64_t p = lo; p < n; ++p) {
     double dot = 0.0;
     for (int d = 0; d < D; ++d) dot += q[d] * paged(kc, bt, MB, b, h, p, d, H, D, bs, dtype);
     s[p] = scale * dot;
     if (s[p] > m) m = s[p];
   }
   double den = 0.0;
-  for (int64_t p = 0; p < n; ++p) {
+  for (int64_t p = lo; p < n; ++p) {
     double w = exp(s[p] - m);
     den += w;
     for (int d = 0; d < D; ++d) o[d] += w * paged(vc, bt, MB, b, h, p, d, H, D, bs, dtype);
@@ -123,10 +123,11 @@ static void attend(const double *q, const void *kc, const void *vc, const int32_
  * [KV §2.3]: decode uses a PagedAttention-type kernel whose inputs are Q, K, V and
  * the block table. Per (b, h): o = sum_p softmax_p(scale * q.K_p) V_p over the
  * seq_lens[b] cached positions (the token of this step has already been appended).
- * seq_len 0 gives a zero row. out: fp64 [B][H][D]. */
+ * seq_len 0 gives a zero row. window > 0 keeps only the last `window` positions
+ * (sliding-window attention, the model-side alternative of [KV §1.3]). out: fp64 [B][H][D]. */
 void oracle_full_decode(const void *q, const void *k_cache, const void *v_cache,
                         const int32_t *block_tables, int MB, const int32_t *seq_lens, int B,
-                        int H, int D, int bs, int dtype, double scale, double *out) {
+                        int H, int D, int bs, int dtype, double scale, int window, double *out) {
   int64_t nmax = 1;
   for (int b = 0; b < B; ++b) if (seq_lens[b] > nmax) nmax = seq_lens[b];
 #pragma omp parallel
@@ -137,8 +138,10 @@ void oracle_full_decode(const void *q, const void *k_cache, const void *v_cache,
     for (int b = 0; b < B; ++b)
       for (int h = 0; h < H; ++h) {
         for (int d = 0; d < D; ++d) qd[d] = ld(q, ((int64_t)b * H + h) * D + d, dtype);
-        attend(qd, k_cache, v_cache, block_tables, MB, b, h, seq_lens[b], H, D, bs, dtype,
-               scale, s, out + ((int64_t)b * H + h) * D);
+        const int64_t n = seq_lens[b];
+        const int64_t lo = (window > 0 && n > window) ? n - window : 0;
+        attend(qd, k_cache, v_cache, block_tables, MB, b, h, lo, n, H, D, bs, dtype, scale, s,
+               out + ((int64_t)b * H + h) * D);
       }
     free(s);
     free(qd);
@@ -150,12 +153,14 @@ void oracle_full_decode(const void *q, const void *k_cache, const void *v_cache,
  * causal softmax attention. Token j of request b (packed row t = cu_q_lens[b] + j)
  * sits at absolute position i = ctx_lens[b] + j and attends to cached positions
  * p <= i (the call's own keys were appended to the cache first).
+ * window > 0 keeps only the positions p > i - window (sliding window).
  * rows == NULL: out fp64 [T][H][D]. Otherwise only the packed rows listed are
  * computed and out is [nrows][H][D]. */
 void oracle_full_prefill(const void *q, const void *k_cache, const void *v_cache,
                          const int32_t *block_tables, int MB, const int32_t *cu_q_lens,
                          const int32_t *ctx_lens, int B, int H, int D, int bs, int dtype,
-                         double scale, const int32_t *rows, int nrows, double *out) {
+                         double scale, int window, const int32_t *rows, int nrows,
+                         double *out) {
   int T = cu_q_lens[B];
   int n_out = rows ? nrows : T;
   int64_t nmax = 1;
@@ -175,8 +180,9 @@ void oracle_full_prefill(const void *q, const void *k_cache, const void *v_cache
         while (b + 1 < B && cu_q_lens[b + 1] <= t) ++b;
         int64_t i = (int64_t)(ctx_lens ? ctx_lens[b] : 0) + (t - cu_q_lens[b]);
         for (int d = 0; d < D; ++d) qd[d] = ld(q, ((int64_t)t * H + h) * D + d, dtype);
-        attend(qd, k_cache, v_cache, block_tables, MB, b, h, i + 1, H, D, bs, dtype, scale, s,
-               out + ((int64_t)r * H + h) * D);
+        const int64_t lo = (window > 0 && i + 1 > window) ? i + 1 - window : 0;
+        attend(qd, k_cache, v_cache, block_tables, MB, b, h, lo, i + 1, H, D, bs, dtype, scale,
+               s, out + ((int64_t)r * H + h) * D);
       }
     free(s);
     free(qd);

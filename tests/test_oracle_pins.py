@@ -203,6 +203,74 @@ def test_prefill_matches_causal_sdpa(ctx):
     np.testing.assert_array_equal(oracle.full_prefill(q, kc, vc, pool.block_tables, cuq, ctx, scale, rows), out[rows])
 
 
+# ------------------------------------------------- sliding-window Full attention
+# [KV §1.3] names sliding-window attention as the model-side alternative to paged KV:
+# a query at absolute position i sees only the keys at positions i - W < p <= i.
+@pytest.mark.parametrize("window", [1, 5, 16, 17, 40])
+def test_window_decode_matches_banded_sdpa(window):
+    lens = [1, 5, 16, 17, 33, 64]
+    H, D = 2, 16
+    pool, kc, vc, k, v, cu, _ = _paged_setup(21, lens, H, D, W.BF16)
+    q = W.rows(W.rng(22), (len(lens), H, D), D, W.BF16)
+    scale = 1 / math.sqrt(D)
+    out = oracle.full_decode(q, kc, vc, pool.block_tables, lens, scale, window=window)
+    for b, n in enumerate(lens):
+        K = _f64(k[cu[b]:cu[b + 1]]).transpose(1, 0, 2)
+        V = _f64(v[cu[b]:cu[b + 1]]).transpose(1, 0, 2)
+        mask = np.where(np.arange(n)[None, :] > n - 1 - window, 0.0, -np.inf)
+        ref = _sdpa(_f64(q[b])[:, None, :], K, V, scale, mask)[:, 0, :]
+        np.testing.assert_allclose(out[b], ref, rtol=1e-12, atol=1e-14)
+
+
+@pytest.mark.parametrize("window,ctx", [(1, [0, 0]), (7, [16, 5]), (16, [0, 40]), (33, [16, 5])])
+def test_window_prefill_matches_banded_causal_sdpa(window, ctx):
+    H, D = 2, 16
+    qlens = [5, 37]
+    tot = [c + n for c, n in zip(ctx, qlens)]
+    pool, kc, vc, k, v, cu_all, _ = _paged_setup(23, tot, H, D, W.BF16)
+    cuq = W.cu_from_lens(qlens)
+    q = W.rows(W.rng(24), (int(cuq[-1]), H, D), D, W.BF16)
+    scale = 1 / math.sqrt(D)
+    out = oracle.full_prefill(q, kc, vc, pool.block_tables, cuq, ctx, scale, window=window)
+    for b in range(2):
+        K = _f64(k[cu_all[b]:cu_all[b + 1]]).transpose(1, 0, 2)
+        V = _f64(v[cu_all[b]:cu_all[b + 1]]).transpose(1, 0, 2)
+        Q = _f64(q[cuq[b]:cuq[b + 1]]).transpose(1, 0, 2)
+        pos = ctx[b] + np.arange(qlens[b])
+        p = np.arange(tot[b])[None, :]
+        mask = np.where((p <= pos[:, None]) & (p > pos[:, None] - window), 0.0, -np.inf)
+        ref = _sdpa(Q, K, V, scale, mask).transpose(1, 0, 2)
+        np.testing.assert_allclose(out[cuq[b]:cuq[b + 1]], ref, rtol=1e-12, atol=1e-14)
+
+
+def test_window_covering_every_key_is_full_attention_bit_exact():
+    H, D = 2, 16
+    lens = [3, 16, 31]
+    pool, kc, vc, k, v, cu, _ = _paged_setup(25, lens, H, D, W.F32)
+    q = W.rows(W.rng(26), (len(lens), H, D), D, W.F32)
+    full = oracle.full_decode(q, kc, vc, pool.block_tables, lens, 0.25)
+    for window in (31, 32, 1000):
+        assert np.array_equal(oracle.full_decode(q, kc, vc, pool.block_tables, lens, 0.25,
+                                                 window=window), full)
+    qp = W.rows(W.rng(27), (int(cu[-1]), H, D), D, W.F32)
+    fullp = oracle.full_prefill(qp, kc, vc, pool.block_tables, cu, [0, 0, 0], 0.25)
+    assert np.array_equal(oracle.full_prefill(qp, kc, vc, pool.block_tables, cu, [0, 0, 0], 0.25,
+                                              window=31), fullp)
+
+
+def test_window_one_returns_own_value():
+    """W = 1: each query sees only its own position, so the output is that value row."""
+    H, D = 2, 16
+    lens = [4, 20]
+    pool, kc, vc, k, v, cu, _ = _paged_setup(28, lens, H, D, W.BF16)
+    q = W.rows(W.rng(29), (int(cu[-1]), H, D), D, W.BF16)
+    out = oracle.full_prefill(q, kc, vc, pool.block_tables, cu, [0, 0], 0.25, window=1)
+    assert np.array_equal(out, _f64(v))
+    qd = W.rows(W.rng(30), (2, H, D), D, W.BF16)
+    outd = oracle.full_decode(qd, kc, vc, pool.block_tables, lens, 0.25, window=1)
+    assert np.array_equal(outd, _f64(v[cu[1:] - 1]))
+
+
 def test_prefill_last_row_equals_decode_on_same_prefix():
     H, D = 2, 16
     pool, kc, vc, k, v, cu, _ = _paged_setup(11, [20, 7], H, D, W.BF16)
