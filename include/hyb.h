@@ -62,7 +62,7 @@ typedef enum {
 } hyb_status_t;
 
 typedef enum { HYB_F32 = 0, HYB_BF16 = 1 } hyb_dtype_t;
-typedef enum { HYB_FULL = 0, HYB_LINEAR = 1 } hyb_layer_type_t;
+typedef enum { HYB_FULL = 0, HYB_LINEAR = 1, HYB_SLIDING = 2 } hyb_layer_type_t;
 typedef enum { HYB_MODE_DECODE = 0, HYB_MODE_PREFILL = 1 } hyb_mode_t;
 
 /* bits of the device status word */
@@ -82,7 +82,15 @@ typedef struct {
   int32_t max_blocks_per_seq;  /* columns of block_tables                               */
   int32_t dtype;               /* hyb_dtype_t of q/k/v/out and of the caches            */
   float scale;                 /* softmax scale (the pages give none; 1/sqrt(D) usual)  */
+  int32_t window;              /* 0: every earlier key; W > 0: sliding window, a query  */
+                               /* at position i sees keys p with i - W < p <= i         */
 } hyb_attn_dims_t;
+
+/* Sliding window [KV §1.3: rewriting the model to sliding-window attention is one of
+ * the routes the page lists]. With d->window = W > 0 the decode and prefill calls below
+ * attend only to the last W positions up to and including the query's own. Entries of
+ * block_tables for blocks that end before the window of a request's earliest query in
+ * the call are never read: an allocator may release those blocks and store -1 there. */
 
 /* -------------------------------------------------------------------------
  * A1. Slot mapping [KV §2.1: 16-token blocks reached through a page table].
@@ -114,6 +122,7 @@ hyb_status_t hyb_paged_kv_append(const void* k, const void* v, const int64_t* sl
  * token appended this step):
  *     out[b][h][:] = sum_{p<n} softmax_p(scale * q[b][h].K_p) V_p
  * where K_p, V_p are read at block_tables[b][p/16], offset p%16. n = 0 gives zeros.
+ * d->window = W > 0 restricts p to n - W <= p < n (see "Sliding window" above).
  * max_seq_len (host) must be >= every seq_lens[b]; a longer sequence sets
  * HYB_DEVERR_BAD_LENGTH and is truncated. The kernel splits each sequence into
  * ranges of blocks (split-K) and merges the partial softmax states; `workspace`
@@ -158,6 +167,7 @@ hyb_status_t hyb_paged_attn_decode_noalloc(void* out, const void* q, const void*
  *     out[t][h][:] = sum_{p<=i} softmax_p(scale * q[t][h].K_p) V_p
  * K/V are read from the paged cache, so the call's own rows must be appended first
  * (hyb_paged_kv_append) and a cached prefix (ctx_lens[b] > 0) is attended to as well.
+ * d->window = W > 0 restricts p to i - W < p <= i (see "Sliding window" above).
  * ctx_lens may be NULL (all 0). T (host) = cu_q_lens[B], the rows of q and out;
  * max_q_len (host) >= every request's row count.
  * bf16 with D = 128 runs the tensor-core kernel; other supported (dtype, D) pairs run
@@ -214,7 +224,7 @@ hyb_status_t hyb_linear_attn_chunked_prefill(void* out, const void* q, const voi
  * split memory pools, per-forward metadata of seq lens, block tables and state
  * buffers handed to each op together with the layer type; VL §3.2: an execution
  * plan built per layer type; VL §5.2: each layer has its own cache].
- * layer_types (host, [L]) holds HYB_FULL / HYB_LINEAR. layers (host, [L]) gives
+ * layer_types (host, [L]) holds HYB_FULL / HYB_LINEAR / HYB_SLIDING. layers (host, [L]) gives
  * each layer's own buffers; meta (host struct of device pointers) is shared by all
  * layers of the batch. Layers run in order on `stream`:
  *   decode  (mode 0): FULL   -> hyb_paged_kv_append(k, v @ slot_mapping) +
@@ -222,8 +232,12 @@ hyb_status_t hyb_linear_attn_chunked_prefill(void* out, const void* q, const voi
  *                     LINEAR -> hyb_linear_attn_step(state_slots)
  *   prefill (mode 1): FULL   -> hyb_paged_kv_append + hyb_paged_attn_prefill_causal
  *                     LINEAR -> hyb_linear_attn_chunked_prefill(reset, chunk_size)
+ * A SLIDING layer runs as a FULL layer with window = layers[l].window (> 0); FULL
+ * layers attend to every earlier key, and d->window must be 0.
  * Every layer's arguments are checked before the first launch. Results equal the
- * per-op calls bit for bit. workspace serves the decode calls (see A3).
+ * per-op calls bit for bit. workspace serves the decode calls (see A3) and must hold
+ * hyb_paged_attn_decode_workspace_size() bytes for the largest window among the layers
+ * (window 0 when any FULL layer is present).
  * ------------------------------------------------------------------------- */
 typedef struct {
   void* out;                 /* [T][H][D]                                   */
@@ -234,7 +248,7 @@ typedef struct {
   void* v_cache;             /* FULL: this layer's own V pool, else NULL    */
   float* state_pool;         /* LINEAR: this layer's own state pool         */
   int32_t num_state_slots;   /* LINEAR: slots in state_pool                 */
-  int32_t reserved;
+  int32_t window;            /* SLIDING: its window W > 0; otherwise 0      */
 } hyb_layer_io_t;
 
 typedef struct {

@@ -18,7 +18,7 @@ from ._build import LIB, build  # noqa: F401  (build() compiles libhyb.so in-tre
 
 HYB_OK, HYB_ERR_INVALID_ARG, HYB_ERR_UNSUPPORTED, HYB_ERR_CUDA, HYB_ERR_DEVICE_CHECK = range(5)
 HYB_F32, HYB_BF16 = 0, 1
-HYB_FULL, HYB_LINEAR = 0, 1
+HYB_FULL, HYB_LINEAR, HYB_SLIDING = 0, 1, 2
 HYB_MODE_DECODE, HYB_MODE_PREFILL = 0, 1
 HYB_DEVERR_BAD_BLOCK, HYB_DEVERR_BAD_SLOT, HYB_DEVERR_BAD_STATE = 0x1, 0x2, 0x4
 HYB_DEVERR_TIMEOUT, HYB_DEVERR_MISALIGNED, HYB_DEVERR_BAD_LENGTH = 0x8, 0x10, 0x20
@@ -28,13 +28,13 @@ BLOCK_SIZE = 16
 class hyb_attn_dims_t(C.Structure):
     _fields_ = [("num_heads", C.c_int32), ("head_dim", C.c_int32), ("block_size", C.c_int32),
                 ("num_blocks", C.c_int32), ("max_blocks_per_seq", C.c_int32),
-                ("dtype", C.c_int32), ("scale", C.c_float)]
+                ("dtype", C.c_int32), ("scale", C.c_float), ("window", C.c_int32)]
 
 
 class hyb_layer_io_t(C.Structure):
     _fields_ = [("out", C.c_void_p), ("q", C.c_void_p), ("k", C.c_void_p), ("v", C.c_void_p),
                 ("k_cache", C.c_void_p), ("v_cache", C.c_void_p), ("state_pool", C.c_void_p),
-                ("num_state_slots", C.c_int32), ("reserved", C.c_int32)]
+                ("num_state_slots", C.c_int32), ("window", C.c_int32)]
 
 
 class hyb_batch_meta_t(C.Structure):
@@ -124,13 +124,13 @@ def dtype_code(torch_dtype) -> int:
 
 
 def dims(num_heads, head_dim, num_blocks, max_blocks_per_seq, dtype=HYB_BF16, scale=None,
-         block_size=BLOCK_SIZE) -> hyb_attn_dims_t:
+         block_size=BLOCK_SIZE, window=0) -> hyb_attn_dims_t:
     if not isinstance(dtype, int):
         dtype = dtype_code(dtype)
     if scale is None:
         scale = head_dim ** -0.5
     return hyb_attn_dims_t(num_heads, head_dim, block_size, num_blocks, max_blocks_per_seq,
-                           dtype, scale)
+                           dtype, scale, window)
 
 
 def check(status: int, what: str = "hyb call") -> None:
@@ -202,9 +202,9 @@ def hyb_linear_attn_chunked_prefill(out, q, k, v, cu_seqlens, ctx_lens, state_po
 
 
 def layer_io(out=None, q=None, k=None, v=None, k_cache=None, v_cache=None, state_pool=None,
-             num_state_slots=0) -> hyb_layer_io_t:
+             num_state_slots=0, window=0) -> hyb_layer_io_t:
     return hyb_layer_io_t(_p(out), _p(q), _p(k), _p(v), _p(k_cache), _p(v_cache),
-                          _p(state_pool), num_state_slots, 0)
+                          _p(state_pool), num_state_slots, window)
 
 
 def batch_meta(B, T, seq_lens=None, block_tables=None, slot_mapping=None, cu_q_lens=None,

@@ -83,7 +83,7 @@ hyb_status_t check_dims(const hyb_attn_dims_t* d) {
   if (d->block_size != kBlockSize) return HYB_ERR_UNSUPPORTED;
   if (d->dtype != HYB_BF16 && d->dtype != HYB_F32) return HYB_ERR_INVALID_ARG;
   if ((d->head_dim * esize_of(d->dtype)) % 16 != 0) return HYB_ERR_UNSUPPORTED;
-  if (!std::isfinite(d->scale)) return HYB_ERR_INVALID_ARG;
+  if (!std::isfinite(d->scale) || d->window < 0) return HYB_ERR_INVALID_ARG;
   if ((int64_t)d->num_blocks * kBlockSize > INT32_MAX) return HYB_ERR_UNSUPPORTED;
   return HYB_OK;
 }
@@ -123,7 +123,7 @@ hyb_status_t check_decode(const void* out, const void* q, const void* kc, const 
   if (!out || !q || !kc || !vc || !bt || !seq_lens) return HYB_ERR_INVALID_ARG;
   if (!al16(out) || !al16(q) || !al16(kc) || !al16(vc) || !al(bt, 4) || !al(seq_lens, 4))
     return HYB_ERR_INVALID_ARG;
-  const DecodePlan p = plan_decode(B, d->num_heads, d->head_dim, max_seq_len);
+  const DecodePlan p = plan_decode(B, d->num_heads, d->head_dim, max_seq_len, d->window);
   if (p.ws_bytes > 0 && (!ws || ws_bytes < p.ws_bytes || !al16(ws))) return HYB_ERR_INVALID_ARG;
   return HYB_OK;
 }
@@ -181,11 +181,11 @@ hyb_status_t run_decode(void* out, const void* q, const void* kc, const void* vc
                         const int32_t* bt, const int32_t* seq_lens, int B, int max_seq_len,
                         const hyb_attn_dims_t* d, void* ws, unsigned* status, cudaStream_t s) {
   if (B == 0) return HYB_OK;
-  const DecodePlan p = plan_decode(B, d->num_heads, d->head_dim, max_seq_len);
+  const DecodePlan p = plan_decode(B, d->num_heads, d->head_dim, max_seq_len, d->window);
   return cuda_status(launch_paged_decode(out, q, kc, vc, bt, seq_lens, nullptr, nullptr, B, 0,
                                          d->num_heads, d->head_dim, d->dtype, d->num_blocks,
-                                         d->max_blocks_per_seq, max_seq_len, d->scale, p, ws,
-                                         status, s));
+                                         d->max_blocks_per_seq, max_seq_len, d->scale,
+                                         d->window, p, ws, status, s));
 }
 
 hyb_status_t run_prefill(void* out, const void* q, const void* kc, const void* vc,
@@ -196,13 +196,13 @@ hyb_status_t run_prefill(void* out, const void* q, const void* kc, const void* v
   if (prefill_tc_supported(d->dtype, d->head_dim))
     return cuda_status(launch_prefill_tc(out, q, kc, vc, bt, cu, ctx, B, T, max_q_len,
                                          d->num_heads, d->num_blocks, d->max_blocks_per_seq,
-                                         d->scale, status, s));
+                                         d->scale, d->window, status, s));
   const DecodePlan none{1 << 30, 1, 0};
   return cuda_status(launch_paged_decode(out, q, kc, vc, bt, nullptr, cu, ctx, B, max_q_len,
                                          d->num_heads, d->head_dim, d->dtype, d->num_blocks,
                                          d->max_blocks_per_seq,
-                                         d->max_blocks_per_seq * kBlockSize, d->scale, none,
-                                         nullptr, status, s));
+                                         d->max_blocks_per_seq * kBlockSize, d->scale,
+                                         d->window, none, nullptr, status, s));
 }
 
 hyb_status_t run_linear_prefill(void* out, const void* q, const void* k, const void* v,
@@ -255,7 +255,8 @@ hyb_status_t hyb_paged_kv_append(const void* k, const void* v, const int64_t* sl
 size_t hyb_paged_attn_decode_workspace_size(int32_t B, int32_t max_seq_len,
                                             const hyb_attn_dims_t* d) {
   if (!d || B <= 0 || max_seq_len <= 0 || d->num_heads <= 0 || d->head_dim <= 0) return 0;
-  return plan_decode(B, d->num_heads, d->head_dim, max_seq_len).ws_bytes;
+  if (d->window < 0) return 0;
+  return plan_decode(B, d->num_heads, d->head_dim, max_seq_len, d->window).ws_bytes;
 }
 
 hyb_status_t hyb_paged_attn_decode(void* out, const void* q, const void* k_cache,
@@ -326,6 +327,7 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
   if (mode != HYB_MODE_DECODE && mode != HYB_MODE_PREFILL) return HYB_ERR_INVALID_ARG;
   hyb_status_t st = check_dims(d);
   if (st != HYB_OK) return st;
+  if (d->window != 0) return HYB_ERR_INVALID_ARG;     // windows come from the layer types
   const int B = meta->B, T = meta->T, H = d->num_heads, D = d->head_dim, dt = d->dtype;
   if (B < 0 || T < 0) return HYB_ERR_INVALID_ARG;
   if (mode == HYB_MODE_DECODE && T != B) return HYB_ERR_INVALID_ARG;
@@ -333,18 +335,22 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
   std::set<const void*> seen;   // each layer owns its caches / state pool [VL §5.2]
   for (int l = 0; l < L; ++l) {
     const hyb_layer_io_t& io = layers[l];
-    if (layer_types[l] == HYB_FULL) {
+    const int lt = layer_types[l];
+    if (lt == HYB_SLIDING ? io.window <= 0 : io.window != 0) return HYB_ERR_INVALID_ARG;
+    if (lt == HYB_FULL || lt == HYB_SLIDING) {
       if (!io.k_cache || !io.v_cache || !seen.insert(io.k_cache).second ||
           !seen.insert(io.v_cache).second)
         return HYB_ERR_INVALID_ARG;
-      st = check_append(io.k, io.v, meta->slot_mapping, T, io.k_cache, io.v_cache, d);
+      hyb_attn_dims_t dl = *d;
+      dl.window = io.window;
+      st = check_append(io.k, io.v, meta->slot_mapping, T, io.k_cache, io.v_cache, &dl);
       if (st != HYB_OK) return st;
       st = mode == HYB_MODE_DECODE
                ? check_decode(io.out, io.q, io.k_cache, io.v_cache, meta->block_tables,
-                              meta->seq_lens, B, meta->max_seq_len, d, workspace, ws_bytes)
+                              meta->seq_lens, B, meta->max_seq_len, &dl, workspace, ws_bytes)
                : check_prefill(io.out, io.q, io.k_cache, io.v_cache, meta->block_tables,
-                               meta->cu_q_lens, meta->ctx_lens, B, T, meta->max_q_len, d);
-    } else if (layer_types[l] == HYB_LINEAR) {
+                               meta->cu_q_lens, meta->ctx_lens, B, T, meta->max_q_len, &dl);
+    } else if (lt == HYB_LINEAR) {
       if (!io.state_pool || !seen.insert(io.state_pool).second) return HYB_ERR_INVALID_ARG;
       st = mode == HYB_MODE_DECODE
                ? check_linear_common(io.out, io.q, io.k, io.v, io.state_pool, io.num_state_slots,
@@ -364,15 +370,17 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
   // 2) run the plan in layer order
   for (int l = 0; l < L; ++l) {
     const hyb_layer_io_t& io = layers[l];
-    if (layer_types[l] == HYB_FULL) {
+    if (layer_types[l] == HYB_FULL || layer_types[l] == HYB_SLIDING) {
+      hyb_attn_dims_t dl = *d;
+      dl.window = io.window;
       st = cuda_status(launch_kv_append(io.k, io.v, meta->slot_mapping, T, H, D, esize_of(dt),
                                         d->num_blocks, io.k_cache, io.v_cache, sw, s));
       if (st != HYB_OK) return st;
       st = mode == HYB_MODE_DECODE
                ? run_decode(io.out, io.q, io.k_cache, io.v_cache, meta->block_tables,
-                            meta->seq_lens, B, meta->max_seq_len, d, workspace, sw, s)
+                            meta->seq_lens, B, meta->max_seq_len, &dl, workspace, sw, s)
                : run_prefill(io.out, io.q, io.k_cache, io.v_cache, meta->block_tables,
-                             meta->cu_q_lens, meta->ctx_lens, B, T, meta->max_q_len, d, sw, s);
+                             meta->cu_q_lens, meta->ctx_lens, B, T, meta->max_q_len, &dl, sw, s);
     } else {
       st = mode == HYB_MODE_DECODE
                ? cuda_status(launch_linear_step(io.out, io.q, io.k, io.v, io.state_pool,

@@ -17,7 +17,12 @@
 // a request's result does not depend on the rest of the batch.
 //
 // The same kernel serves as the CUDA-core causal prefill for shapes without a
-// tensor-core kernel (PREFILL = true: one row per packed query token, n = position + 1).
+// tensor-core kernel (PREFILL = true: one row per packed query token, n = position + 1,
+// one CTA walks all of the row's blocks).
+//
+// Sliding window (window > 0): a row sees keys [n - window, n). The splits cover only the
+// blocks from the one holding n - window; earlier blocks and their block-table entries are
+// never read, so an allocator may have released them.
 #include <cuda_bf16.h>
 
 #include "hyb_internal.cuh"
@@ -68,6 +73,18 @@ __device__ __forceinline__ int clamp_len(int n, int max_len, int MB) {
   return n > cap ? cap : n;
 }
 
+// First key a row of n keys attends to.
+__device__ __forceinline__ int window_lo(int n, int window) {
+  return (window > 0 && n > window) ? n - window : 0;
+}
+
+// Splits of a decode row: ranges of kBPS blocks from the window's first block.
+__device__ __forceinline__ int decode_splits(int n, int window) {
+  const int nblk = (n + kBlockSize - 1) / kBlockSize;
+  const int blk_lo = window_lo(n, window) / kBlockSize;
+  return max(1, (nblk - blk_lo + kBPS - 1) / kBPS);
+}
+
 template <typename T, int D>
 struct DecodeShape {
   static constexpr int VEC = Elt<T>::VEC;
@@ -85,8 +102,8 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
                     const T* __restrict__ vc, const int32_t* __restrict__ bt,
                     const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu,
                     const int32_t* __restrict__ ctx, int max_q, int H, int NB, int MB,
-                    int max_len, float scale_log2, int max_splits, float* __restrict__ ws_acc,
-                    float2* __restrict__ ws_ml, unsigned* status) {
+                    int max_len, float scale_log2, int window, int max_splits,
+                    float* __restrict__ ws_acc, float2* __restrict__ ws_ml, unsigned* status) {
   using E = Elt<T>;
   using S = DecodeShape<T, D>;
   constexpr int VEC = S::VEC, LPR = S::LPR, TPI = S::TPI, ITER = S::ITER, TILE = S::TILE;
@@ -106,10 +123,12 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
   const int n = clamp_len(n_raw, max_len, MB);
   if (n != (n_raw < 0 ? 0 : n_raw) && split == 0 && threadIdx.x == 0)
     flag(status, n_raw > max_len ? HYB_DEVERR_BAD_LENGTH : HYB_DEVERR_BAD_BLOCK);
+  const int lo = window_lo(n, window);      // keys [lo, n)
   const int nblk = (n + kBlockSize - 1) / kBlockSize;
-  const int nsplit = max(1, (nblk + kBPS - 1) / kBPS);
+  const int nsplit = PREFILL ? 1 : decode_splits(n, window);
   if (split >= nsplit) return;
-  const int blk_begin = split * kBPS, blk_end = min(nblk, blk_begin + kBPS);
+  const int blk_begin = lo / kBlockSize + split * kBPS;
+  const int blk_end = PREFILL ? nblk : min(nblk, blk_begin + kBPS);
 
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -184,12 +203,12 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
         for (int e = 0; e < VEC; ++e) d = fmaf(qf[e], kf[e], d);
 #pragma unroll
         for (int o = LPR / 2; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-        s[it] = (tok0 + tk < n) ? d : -INFINITY;
+        s[it] = (tok0 + tk < n && tok0 + tk >= lo) ? d : -INFINITY;
         mt = fmaxf(mt, s[it]);
       }
 #pragma unroll
       for (int o = LPR; o < 32; o <<= 1) mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, o));
-      const float m_new = fmaxf(m, mt);  // finite: a tile's first token is always < n
+      const float m_new = fmaxf(m, mt);  // finite: every tile holds a key in [lo, n)
       const float alpha = fast_exp2(m - m_new);
       float ls = 0.f;
 #pragma unroll
@@ -199,7 +218,7 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
         const int tk = rr + it * TPI;
         const float p = fast_exp2(s[it] - m_new);
         ls += p;
-        if (tok0 + tk < n) {             // rows past the sequence may hold anything (NaN)
+        if (tok0 + tk < n && tok0 + tk >= lo) {   // other rows may hold anything (NaN)
           float vf[VEC];
           E::unpack(*reinterpret_cast<const uint4*>(Vs + tk * D + c * VEC), vf);
 #pragma unroll
@@ -275,12 +294,11 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
 template <typename T, int D>
 __global__ void __launch_bounds__(128)
 decode_combine_kernel(T* __restrict__ out, const int32_t* __restrict__ seq_lens, int H, int MB,
-                      int max_len, int max_splits, const float* __restrict__ ws_acc,
+                      int max_len, int window, int max_splits, const float* __restrict__ ws_acc,
                       const float2* __restrict__ ws_ml) {
   const int r = blockIdx.x, h = blockIdx.y;
   const int n = clamp_len(seq_lens[r], max_len, MB);
-  const int nblk = (n + kBlockSize - 1) / kBlockSize;
-  const int nsplit = max(1, (nblk + kBPS - 1) / kBPS);
+  const int nsplit = decode_splits(n, window);
   if (nsplit <= 1) return;
   const int64_t rh = (int64_t)r * H + h;
   const float2* ml = ws_ml + rh * max_splits;
@@ -304,7 +322,7 @@ template <typename T, int D>
 cudaError_t launch_typed(void* out, const void* q, const void* kc, const void* vc,
                          const int32_t* bt, const int32_t* seq_lens, const int32_t* cu,
                          const int32_t* ctx, int R, int max_q, int H, int NB, int MB,
-                         int max_len, float scale, const DecodePlan& plan, void* ws,
+                         int max_len, float scale, int window, const DecodePlan& plan, void* ws,
                          unsigned* status, cudaStream_t s) {
   using Sh = DecodeShape<T, D>;
   const bool prefill = cu != nullptr;
@@ -321,26 +339,28 @@ cudaError_t launch_typed(void* out, const void* q, const void* kc, const void* v
   if (prefill)
     paged_decode_kernel<T, D, true><<<grid, kNW * 32, Sh::SMEM, s>>>(
         (T*)out, (const T*)q, (const T*)kc, (const T*)vc, bt, seq_lens, cu, ctx, max_q, H, NB,
-        MB, max_len, scale_log2, max_splits, ws_acc, ws_ml, status);
+        MB, max_len, scale_log2, window, max_splits, ws_acc, ws_ml, status);
   else
     paged_decode_kernel<T, D, false><<<grid, kNW * 32, Sh::SMEM, s>>>(
         (T*)out, (const T*)q, (const T*)kc, (const T*)vc, bt, seq_lens, cu, ctx, max_q, H, NB,
-        MB, max_len, scale_log2, max_splits, ws_acc, ws_ml, status);
+        MB, max_len, scale_log2, window, max_splits, ws_acc, ws_ml, status);
   count_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess || max_splits == 1) return e;
   decode_combine_kernel<T, D><<<dim3(R, H), 128, 0, s>>>((T*)out, seq_lens, H, MB, max_len,
-                                                          max_splits, ws_acc, ws_ml);
+                                                          window, max_splits, ws_acc, ws_ml);
   count_launch();
   return cudaGetLastError();
 }
 
 }  // namespace
 
-DecodePlan plan_decode(int B, int H, int D, int max_seq_len) {
+DecodePlan plan_decode(int B, int H, int D, int max_seq_len, int window) {
   DecodePlan p;
   p.blocks_per_split = kBPS;
-  const int nblk = (std::max(max_seq_len, 0) + kBlockSize - 1) / kBlockSize;
+  int nblk = (std::max(max_seq_len, 0) + kBlockSize - 1) / kBlockSize;
+  // `window` keys starting anywhere inside a block touch at most (window + 14) / 16 + 1 blocks
+  if (window > 0) nblk = std::min(nblk, (window + kBlockSize - 2) / kBlockSize + 1);
   p.max_splits = std::max(1, (nblk + kBPS - 1) / kBPS);
   p.ws_bytes = p.max_splits > 1 ? (size_t)B * H * p.max_splits * ((size_t)D * 4 + 8) : 0;
   return p;
@@ -355,14 +375,14 @@ bool decode_supported(int dtype, int D) {
 cudaError_t launch_paged_decode(void* out, const void* q, const void* kc, const void* vc,
                                 const int32_t* bt, const int32_t* seq_lens, const int32_t* cu,
                                 const int32_t* ctx, int R, int max_q, int H, int D, int dtype,
-                                int NB, int MB, int max_len, float scale,
+                                int NB, int MB, int max_len, float scale, int window,
                                 const DecodePlan& plan, void* ws, unsigned* status,
                                 cudaStream_t s) {
   if (R == 0 || (cu && max_q == 0)) return cudaSuccess;
 #define HYB_DEC(T, DD)                                                                       \
   if (D == DD)                                                                               \
     return launch_typed<T, DD>(out, q, kc, vc, bt, seq_lens, cu, ctx, R, max_q, H, NB, MB,    \
-                               max_len, scale, plan, ws, status, s);
+                               max_len, scale, window, plan, ws, status, s);
   if (dtype == HYB_BF16) {
     HYB_DEC(__nv_bfloat16, 16)
     HYB_DEC(__nv_bfloat16, 32)

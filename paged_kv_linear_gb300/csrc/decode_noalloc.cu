@@ -16,6 +16,7 @@
 // issue them on one stream, one after another.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <mutex>
 
 #include "hyb_internal.cuh"
@@ -62,6 +63,7 @@ hyb_status_t hyb_paged_attn_decode_noalloc(void* out, const void* q, const void*
   if (d->num_heads <= 0 || d->head_dim <= 0 || d->num_blocks <= 0 || d->max_blocks_per_seq <= 0)
     return HYB_ERR_INVALID_ARG;
   if (d->dtype != HYB_BF16 && d->dtype != HYB_F32) return HYB_ERR_INVALID_ARG;
+  if (d->window < 0 || !std::isfinite(d->scale)) return HYB_ERR_INVALID_ARG;
   if (d->block_size != hyb::kBlockSize || d->num_heads > 65535 || max_seq_len > (1 << 24) ||
       !hyb::decode_supported(d->dtype, d->head_dim) ||
       (int64_t)d->num_blocks * hyb::kBlockSize > INT32_MAX)
@@ -73,15 +75,16 @@ hyb_status_t hyb_paged_attn_decode_noalloc(void* out, const void* q, const void*
   if (!aligned(out, 16) || !aligned(q, 16) || !aligned(k_cache, 16) || !aligned(v_cache, 16) ||
       !aligned(block_tables, 4) || !aligned(seq_lens, 4))
     return HYB_ERR_INVALID_ARG;
-  const hyb::DecodePlan plan = hyb::plan_decode(B, d->num_heads, d->head_dim, max_seq_len);
+  const hyb::DecodePlan plan = hyb::plan_decode(B, d->num_heads, d->head_dim, max_seq_len,
+                                                 d->window);
   if (plan.ws_bytes > kNoAllocScratchBytes) return HYB_ERR_UNSUPPORTED;   // too big: no launch
   void* scratch = scratch_address();
   unsigned* status = hyb::status_word();
   if (!scratch || !status) return HYB_ERR_CUDA;
   const cudaError_t e = hyb::launch_paged_decode(
       out, q, k_cache, v_cache, block_tables, seq_lens, nullptr, nullptr, B, 0, d->num_heads,
-      d->head_dim, d->dtype, d->num_blocks, d->max_blocks_per_seq, max_seq_len, d->scale, plan,
-      scratch, status, (cudaStream_t)stream);
+      d->head_dim, d->dtype, d->num_blocks, d->max_blocks_per_seq, max_seq_len, d->scale,
+      d->window, plan, scratch, status, (cudaStream_t)stream);
   return e == cudaSuccess ? HYB_OK : HYB_ERR_CUDA;
 }
 

@@ -30,15 +30,17 @@ struct DecodePlan {
   int max_splits;         // grid.x
   size_t ws_bytes;        // workspace needed (0 if max_splits == 1)
 };
-DecodePlan plan_decode(int B, int H, int D, int max_seq_len);
+// window > 0: each row attends to at most `window` keys (sliding window)
+DecodePlan plan_decode(int B, int H, int D, int max_seq_len, int window);
 bool decode_supported(int dtype, int D);
 // decode mode (cu == nullptr): row r < R is request r and attends to seq_lens[r] keys.
 // prefill mode (cu != nullptr): R = B requests; query j < max_q of request b is packed row
 // cu[b] + j and attends to ctx[b] + j + 1 keys (no split-K; no workspace).
+// window > 0 keeps the last `window` of those keys.
 cudaError_t launch_paged_decode(void* out, const void* q, const void* kc, const void* vc,
                                 const int32_t* bt, const int32_t* seq_lens, const int32_t* cu,
                                 const int32_t* ctx, int R, int max_q, int H, int D, int dtype,
-                                int NB, int MB, int max_len, float scale,
+                                int NB, int MB, int max_len, float scale, int window,
                                 const DecodePlan& plan, void* ws, unsigned* status,
                                 cudaStream_t s);
 
@@ -61,7 +63,7 @@ bool prefill_tc_supported(int dtype, int D);
 cudaError_t launch_prefill_tc(void* out, const void* q, const void* kc, const void* vc,
                               const int32_t* bt, const int32_t* cu, const int32_t* ctx, int B,
                               int T, int max_q_len, int H, int NB, int MB, float scale,
-                              unsigned* status, cudaStream_t s);
+                              int window, unsigned* status, cudaStream_t s);
 
 }  // namespace hyb
 

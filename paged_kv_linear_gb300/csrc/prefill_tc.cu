@@ -22,6 +22,12 @@
 // final division by the row sum). S is double-buffered so Q K^T of tile j+2 and P V of
 // tile j run on the tensor core while the softmax threads exponentiate tile j+1; they wait
 // for P V only to reuse a P buffer (two tiles back) or to rescale O.
+//
+// Sliding window (window > 0, a query at position i sees keys i - window < p <= i): the
+// key tiles start at the one holding the window start of the tile's first query, blocks
+// before that start are neither looked up nor loaded (their V rows are zeroed in shared
+// memory instead), and the mask adds the lower bound. A row can then see no key at all in
+// its first tiles; its exponent base is held at 0 until it sees one, so those P are 0.
 #include <cuda_bf16.h>
 
 #include "tc.cuh"
@@ -60,7 +66,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                   const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ out,
                   const int32_t* __restrict__ bt, const int32_t* __restrict__ cu,
                   const int32_t* __restrict__ ctx, int H, int NB, int MB, float scale_log2,
-                  unsigned* status) {
+                  int window, unsigned* status) {
   const int qt = gridDim.x - 1 - blockIdx.x;           // heavy tiles first
   const int h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -72,6 +78,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
   const int kv_end = c0 + q0 + rows;                   // keys the tile's last query sees
   const int nkv = (kv_end + kBN - 1) / kBN;
   const int pos0 = c0 + q0;                            // position of the tile's first query
+  const int key_lo = window > 0 ? max(0, pos0 - window + 1) : 0;   // first key any row sees
+  const int jlo = key_lo / kBN;                        // first key tile
+  const int nloc = nkv - jlo;                          // key tiles this CTA walks
+  const int blk_lo = key_lo / 16;                      // first block looked up and loaded
   const int32_t* btrow = bt + (int64_t)b * MB;
   if ((kv_end + 15) / 16 > MB) {
     if (tid == 0) flag(status, HYB_DEVERR_BAD_BLOCK);
@@ -132,11 +142,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       }
     }
     int ids = -1;                                      // block ids of 4 tiles, one per lane
-    for (int j = 0; j < nkv; ++j) {
-      if ((j & 3) == 0) {
-        const int lb = j * 8 + lane;
+    for (int jj = 0; jj < nloc; ++jj) {                // jj: local tile index, j = jlo + jj
+      if ((jj & 3) == 0) {
+        const int lb = (jlo + jj) * 8 + lane;
         ids = -1;
-        if (lb * 16 < kv_end) {
+        if (lb >= blk_lo && lb * 16 < kv_end) {
           ids = btrow[lb];
           if (ids < 0 || ids >= NB) {
             flag(status, HYB_DEVERR_BAD_BLOCK);
@@ -148,12 +158,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       int nbox = 0;
 #pragma unroll
       for (int bi = 0; bi < 8; ++bi) {
-        blk[bi] = __shfl_sync(0xffffffffu, ids, (j & 3) * 8 + bi);
+        blk[bi] = __shfl_sync(0xffffffffu, ids, (jj & 3) * 8 + bi);
         nbox += blk[bi] >= 0 ? 2 : 0;
       }
-      const int slot = j % depth;
-      if (j >= depth) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&emptyb[slot], ((j - depth) / depth) & 1));
+      const int slot = jj % depth;
+      if (jj >= depth) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&emptyb[slot], ((jj - depth) / depth) & 1));
         if (!ok) break;
       }
       if (lane == 0) {
@@ -167,7 +177,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
             tma_load_2d(dst + kSubQ + bi * 2048, map, 64, y, &fullb[slot]);
           }
       }
-      issued = j + 1;
+      issued = jj + 1;
     }
     if (!ok && lane == 0) {                            // let the loads in flight land
       flag(status, HYB_DEVERR_TIMEOUT);
@@ -181,7 +191,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const uint64_t qdesc = sw128_desc(smem_u32(q_s), 16, 1024);
     const uint64_t kdesc = sw128_desc(smem_u32(sm + kOffK), 16, 1024);
     const uint64_t vdesc = sw128_desc(smem_u32(sm + kOffV), kSubQ, 1024);
-    auto issue_qk = [&](int j) -> bool {           // S[j%2] = Q K_j^T
+    auto issue_qk = [&](int j) -> bool {           // S[j%2] = Q K_j^T (j: local tile index)
       const int ks = j % kNK;
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->kfull[ks], (j / kNK) & 1))) return false;
       if (lane == 0) {
@@ -201,27 +211,35 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     };
     ok = __all_sync(0xffffffffu, mbar_wait(&bars->qfull, 0));
     if (ok) ok = issue_qk(0);
-    if (ok && nkv > 1) ok = issue_qk(1);
-    for (int j = 0; j < nkv && ok; ++j) {
+    if (ok && nloc > 1) ok = issue_qk(1);
+    for (int j = 0; j < nloc && ok; ++j) {           // local tile index; keys from (jlo+j)*128
       const int vs = j % kNV;
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->pfull[j & 1], (j >> 1) & 1));
       if (!ok) break;
       // softmax of tile j is done with S buffer j&1: queue Q K_{j+2} first so the softmax
       // threads have their next-but-one scores early (an MMA issue blocks while the tensor
       // core is busy, so issue order is execution order)
-      if (j + 2 < nkv) {
+      if (j + 2 < nloc) {
         ok = issue_qk(j + 2);
         if (!ok) break;
       }
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->vfull[vs], (j / kNV) & 1));
       if (!ok) break;
       uint8_t* v_s = sm + kOffV + vs * kTile;
-      if ((j + 1) * kBN > kv_end) {                // last tile: V rows past kv_end := 0
-        const int first = kv_end - j * kBN;
-        for (int e = lane; e < (kBN - first) * 16; e += 32) {
-          const int r = first + e / 16, sb = (e >> 3) & 1, ch = e & 7;
-          *reinterpret_cast<uint4*>(v_s + sb * kSubQ + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-        }
+      // V rows that were not loaded := 0 (P is 0 there, but stale shared memory may hold
+      // NaN): rows past kv_end in the last tile, rows before the window's first block
+      const int kb = (jlo + j) * kBN;
+      const int head = j == 0 ? blk_lo * 16 - kb : 0;
+      const int tail = kv_end - kb;
+      if (head > 0 || tail < kBN) {
+        auto zero_rows = [&](int r0, int r1) {
+          for (int e = lane; e < (r1 - r0) * 16; e += 32) {
+            const int r = r0 + e / 16, sb = (e >> 3) & 1, ch = e & 7;
+            *reinterpret_cast<uint4*>(v_s + sb * kSubQ + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+          }
+        };
+        if (head > 0) zero_rows(0, head);
+        if (tail < kBN) zero_rows(tail, kBN);
         fence_async_smem();
       }
       __syncwarp();
@@ -249,6 +267,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const int r = quarter * 32 + lane;                 // query row of the tile = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     const int qp = pos0 + r;                           // absolute query position
+    const int qlo = window > 0 ? qp - window : -1;     // keys kp > qlo are in the window
     const int c0h = hf * 64;                           // this thread's 64 columns
     float m_used = -INFINITY, l = 0.f;                 // l: this half's share of the row sum
     bool ok = true;
@@ -261,7 +280,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       other = bars->red[idx & 1][hf ^ 1][r];
       return true;
     };
-    for (int j = 0; j < nkv && ok; ++j) {
+    for (int j = 0; j < nloc && ok; ++j) {            // local tile index; keys from (jlo+j)*128
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->sfull[j & 1], (j >> 1) & 1));
       if (!ok) break;
       tc_fence_after();
@@ -269,13 +288,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       tmem_ld32(tl + (j & 1) * 128 + c0h, x);
       tmem_ld32(tl + (j & 1) * 128 + c0h + 32, x + 32);
       tmem_ld_wait();
-      const int kbase = j * kBN + c0h;
-      const bool masked = kbase + 63 > pos0 || kbase + 64 > kv_end;
+      const int kbase = (jlo + j) * kBN + c0h;
+      const bool masked = kbase + 63 > pos0 || kbase + 64 > kv_end ||
+                          (window > 0 && kbase <= pos0 + kBM - 1 - window);
       if (masked) {
 #pragma unroll
         for (int c = 0; c < 64; ++c) {
           const int kp = kbase + c;
-          x[c] = (kp <= qp && kp < kv_end) ? x[c] : -INFINITY;
+          x[c] = (kp <= qp && kp < kv_end && kp > qlo) ? x[c] : -INFINITY;
         }
       }
       // partial max of the raw scores (scale > 0 keeps the order): 8 independent chains
@@ -293,6 +313,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       const float m_new = fmaxf(m_used, mx);
       const bool grow = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new != -INFINITY);
       const float m_tgt = grow ? m_new : m_used;
+      const float m_sub = m_tgt == -INFINITY ? 0.f : m_tgt;   // no key seen yet: P = 0
       // exponentials of this tile first: they do not depend on P V of the previous tile.
       // p = 2^(x * scale_log2 - m) as one fma per element; sum in 8 independent chains.
       uint32_t w[32];
@@ -301,8 +322,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       for (int i = 0; i < 8; ++i) sp[i] = 0.f;
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = fast_exp2(fmaf(x[2 * c], scale_log2, -m_tgt));
-        const float p1 = fast_exp2(fmaf(x[2 * c + 1], scale_log2, -m_tgt));
+        const float p0 = fast_exp2(fmaf(x[2 * c], scale_log2, -m_sub));
+        const float p1 = fast_exp2(fmaf(x[2 * c + 1], scale_log2, -m_sub));
         sp[c & 7] += p0 + p1;
         w[c] = pack_bf16(p0, p1);
       }
@@ -335,9 +356,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       tc_fence_before();
       mbar_arrive(&bars->pfull[j & 1]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone[(nkv - 1) & 1], ((nkv - 1) >> 1) & 1));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone[(nloc - 1) & 1], ((nloc - 1) >> 1) & 1));
     float l_other = 0.f;
-    if (ok) ok = pair_swap(nkv, l, l_other);           // row sum = both halves' shares
+    if (ok) ok = pair_swap(nloc, l, l_other);          // row sum = both halves' shares
     if (ok) {
       const float lt = l + l_other;
       tc_fence_after();
@@ -378,7 +399,7 @@ bool prefill_tc_supported(int dtype, int D) { return dtype == HYB_BF16 && D == k
 cudaError_t launch_prefill_tc(void* out, const void* q, const void* kc, const void* vc,
                               const int32_t* bt, const int32_t* cu, const int32_t* ctx, int B,
                               int T, int max_q_len, int H, int NB, int MB, float scale,
-                              unsigned* status, cudaStream_t s) {
+                              int window, unsigned* status, cudaStream_t s) {
   if (B == 0 || max_q_len == 0 || T <= 0) return cudaSuccess;
   CUtensorMap mq, mk, mv;
   const uint64_t qdims[3] = {(uint64_t)kD, (uint64_t)H, (uint64_t)T};
@@ -396,7 +417,7 @@ cudaError_t launch_prefill_tc(void* out, const void* q, const void* kc, const vo
   dim3 grid((max_q_len + kBM - 1) / kBM, H, B);
   prefill_tc_kernel<<<grid, kThreads, kSmem, s>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(out), bt,
                                                   cu, ctx, H, NB, MB, scale * 1.4426950408889634f,
-                                                  status);
+                                                  window, status);
   count_launch();
   return cudaGetLastError();
 }

@@ -85,7 +85,7 @@ def test_dispatch_rejects_shared_caches_and_bad_types(hyb):
     # two Full layers sharing one cache (the failure the vLLM page reports for shared caches)
     assert hyb.hyb_layer_dispatch([0, 0], 2, 0, [a, a], meta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
     # unknown layer type
-    assert hyb.hyb_layer_dispatch([2], 1, 0, [a], meta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_layer_dispatch([3], 1, 0, [a], meta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
     # decode with T != B
     meta_bad = hyb.batch_meta(2, 3, seq_lens=f, block_tables=f, slot_mapping=f, max_seq_len=32)
     assert hyb.hyb_layer_dispatch([0], 1, 0, [a], meta_bad, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
@@ -94,3 +94,43 @@ def test_dispatch_rejects_shared_caches_and_bad_types(hyb):
     assert hyb.hyb_layer_dispatch([1], 1, 0, [lin], meta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
     # empty plan is a no-op
     assert hyb.hyb_layer_dispatch([], 0, 0, [], meta, d, 64, None, 0, 0) == hyb.HYB_OK
+
+
+def test_sliding_window_arguments(hyb):
+    f = 1 << 20
+    d = hyb.dims(32, 128, 1000, 256)
+    # a negative window is rejected by every Full-attention entry point
+    dn = hyb.dims(32, 128, 1000, 256, window=-1)
+    assert hyb.hyb_paged_kv_append(f, f, f, 4, f, f + 256, dn, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_paged_attn_decode(f, f, f, f, f, f, 2, 64, dn, f, 1 << 20, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_paged_attn_decode_noalloc(f, f, f, f, f, f, 2, 64, dn, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_paged_attn_prefill_causal(f, f, f, f, f, f, None, 2, 64, 32, dn, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_paged_attn_decode_workspace_size(2, 4096, dn) == 0
+    # the decode workspace covers only the blocks a window can touch: (W + 14) // 16 + 1
+    full = hyb.hyb_paged_attn_decode_workspace_size(8, 4096, d)
+    w1000 = hyb.hyb_paged_attn_decode_workspace_size(8, 4096, hyb.dims(32, 128, 1000, 256, window=1000))
+    w512 = hyb.hyb_paged_attn_decode_workspace_size(8, 4096, hyb.dims(32, 128, 1000, 256, window=512))
+    w8k = hyb.hyb_paged_attn_decode_workspace_size(8, 4096, hyb.dims(32, 128, 1000, 256, window=8192))
+    per_split = 8 * 32 * (128 * 4 + 8)
+    assert full == 8 * per_split and w8k == full          # 256 blocks -> 8 splits of 32
+    assert w1000 == 2 * per_split                         # 63 blocks -> 2 splits
+    assert w512 == 2 * per_split                          # 33 blocks (unaligned start) -> 2
+    assert hyb.hyb_paged_attn_decode_workspace_size(8, 4096, hyb.dims(32, 128, 1000, 256, window=497)) == 0
+
+
+def test_dispatch_sliding_layer_arguments(hyb):
+    d = hyb.dims(4, 16, 10, 4, dtype=hyb.HYB_F32)
+    f = 1 << 20
+    meta = hyb.batch_meta(2, 2, seq_lens=f, block_tables=f, slot_mapping=f, state_slots=f, max_seq_len=32)
+    def io(window, off=0):
+        return hyb.layer_io(out=f, q=f, k=f, v=f, k_cache=f + 4096 + off, v_cache=f + 8192 + off,
+                            window=window)
+    # a SLIDING layer needs a window > 0; FULL and LINEAR layers carry none
+    assert hyb.hyb_layer_dispatch([2], 1, 0, [io(0)], meta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_layer_dispatch([2], 1, 0, [io(-5)], meta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_layer_dispatch([0], 1, 0, [io(8)], meta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
+    # the dims' own window must be 0: windows come from the layer types
+    dw = hyb.dims(4, 16, 10, 4, dtype=hyb.HYB_F32, window=8)
+    assert hyb.hyb_layer_dispatch([2], 1, 0, [io(8)], meta, dw, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
+    # a SLIDING layer shares no cache with a FULL one
+    assert hyb.hyb_layer_dispatch([0, 2], 2, 0, [io(0), io(8)], meta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
