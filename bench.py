@@ -46,7 +46,8 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--workload", default="decode_single_layer",
-                    choices=["decode_single_layer", "hybrid_32layer", "prefill_chunked", "long_context_decode"],
+                    choices=["decode_single_layer", "hybrid_32layer", "prefill_chunked", "long_context_decode",
+                             "sliding_window"],
                     help="decode_single_layer is the headline; the others are timed alone (e.g. for profiling)")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements of the other workloads")
     return ap.parse_args()
@@ -374,8 +375,67 @@ def row_prefill(hyb, device, stream, iters, seed=0):
     return res
 
 
+def row_sliding_window(hyb, device, stream, iters, seed=0):
+    """Sliding-window Full layers: decode of 8 requests x 131072 cached tokens with window
+    8192 (only the window's blocks are read), and tensor-core causal prefill of 8 x 8192
+    prompts with window 4096."""
+    import torch
+    hbm, tf, _ = measured_peaks()
+    Wd, Wp = 8192, 4096
+    db = W.decode_long_context(seed)
+    B, H, D, NB = db.B, db.H, db.D, db.pool.num_blocks
+    d = hyb.dims(H, D, NB, db.pool.max_blocks, W.BF16, window=Wd)
+    kc = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), 71, D)
+    vc = W.device_rows_(torch.empty_like(kc), 72, D)
+    g = W.rng(seed + 7)
+    q = torch.from_numpy(W.rows(g, (B, H, D), D, W.BF16).view(np.int16)).to(device).view(torch.bfloat16)
+    out = torch.empty_like(q)
+    bt = torch.from_numpy(db.pool.block_tables).to(device)
+    lens = torch.from_numpy(db.seq_lens).to(device)
+    n = int(db.seq_lens.max())
+    ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, n, d)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=device)
+    sh = stream.cuda_stream
+    t_dec = _time(lambda: hyb.check(hyb.hyb_paged_attn_decode(out, q, kc, vc, bt, lens, B, n, d, ws, ws_n, sh)), stream, iters)
+    dec_bytes = int(np.minimum(db.seq_lens, Wd).sum()) * H * D * 4 + 2 * B * H * D * 2
+    del kc, vc
+    torch.cuda.empty_cache()
+
+    pb = W.prefill_chunked(seed)
+    B, H, D, NB = len(pb.q_lens), pb.H, pb.D, pb.pool.num_blocks
+    cu_h = W.cu_from_lens(pb.q_lens)
+    T = int(cu_h[-1])
+    dp = hyb.dims(H, D, NB, pb.pool.max_blocks, W.BF16, window=Wp)
+    qp = W.device_rows_(torch.empty((T, H, D), dtype=torch.bfloat16, device=device), 73, D)
+    kcp = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), 74, D)
+    vcp = W.device_rows_(torch.empty_like(kcp), 75, D)
+    outp = torch.empty_like(qp)
+    btp = torch.from_numpy(pb.pool.block_tables).to(device)
+    cu = torch.from_numpy(cu_h).to(device)
+    L = int(pb.q_lens.max())
+    t_pf = _time(lambda: hyb.check(hyb.hyb_paged_attn_prefill_causal(outp, qp, kcp, vcp, btp, cu, None, B, T, L, dp, sh)),
+                 stream, iters)
+    st_, fl = hyb.hyb_device_status(clear=True)
+    if st_ != 0:
+        raise RuntimeError(f"device-side check flags {fl:#x}")
+    keys = sum(float(np.minimum(np.arange(1, m + 1), Wp).sum()) for m in pb.q_lens)
+    pf_flops = 4.0 * H * D * keys                                          # QK^T + PV inside the band
+    res = {"workload": "sliding_window: decode 8 x 131072 cached tokens with window 8192; "
+                       "prefill 8 x 8192 prompts with window 4096; H=32, D=128",
+           "value": round(B * 1 / (t_dec * 1e-3), 1), "unit": "req-tokens/s per layer (windowed decode)",
+           "ms": {"paged_decode_window": round(t_dec, 4), "prefill_causal_window": round(t_pf, 4)},
+           "roofline": _roof("hbm", dec_bytes / (t_dec * 1e-3) / 1e9, hbm, "GB/s",
+                             "paged_decode, window 8192 (split-K + combine)", dec_bytes),
+           "prefill_window": _roof("tensor", pf_flops / (t_pf * 1e-3) / 1e12, tf, "TFLOP/s",
+                                   "prefill_tc_kernel, window 4096", pf_flops,
+                                   peak_source="measured bf16_tflops (burst)")}
+    del qp, kcp, vcp, outp
+    torch.cuda.empty_cache()
+    return res
+
+
 ROWS = {"long_context_decode": row_long_context, "hybrid_32layer": row_hybrid_32layer,
-        "prefill_chunked": row_prefill}
+        "prefill_chunked": row_prefill, "sliding_window": row_sliding_window}
 
 
 def bench_ours(args, dist):

@@ -96,7 +96,8 @@ struct DecodeShape {
   static_assert(LPR >= 2 && LPR <= 32 && ITER >= 1, "unsupported head_dim");
 };
 
-template <typename T, int D, bool PREFILL>
+// WINDOW = false compiles the lower key bound away (window must then be 0).
+template <typename T, int D, bool PREFILL, bool WINDOW>
 __global__ void __launch_bounds__(kNW * 32)
 paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __restrict__ kc,
                     const T* __restrict__ vc, const int32_t* __restrict__ bt,
@@ -123,9 +124,9 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
   const int n = clamp_len(n_raw, max_len, MB);
   if (n != (n_raw < 0 ? 0 : n_raw) && split == 0 && threadIdx.x == 0)
     flag(status, n_raw > max_len ? HYB_DEVERR_BAD_LENGTH : HYB_DEVERR_BAD_BLOCK);
-  const int lo = window_lo(n, window);      // keys [lo, n)
+  const int lo = WINDOW ? window_lo(n, window) : 0;   // keys [lo, n)
   const int nblk = (n + kBlockSize - 1) / kBlockSize;
-  const int nsplit = PREFILL ? 1 : decode_splits(n, window);
+  const int nsplit = PREFILL ? 1 : decode_splits(n, WINDOW ? window : 0);
   if (split >= nsplit) return;
   const int blk_begin = lo / kBlockSize + split * kBPS;
   const int blk_end = PREFILL ? nblk : min(nblk, blk_begin + kBPS);
@@ -203,7 +204,7 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
         for (int e = 0; e < VEC; ++e) d = fmaf(qf[e], kf[e], d);
 #pragma unroll
         for (int o = LPR / 2; o >= 1; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
-        s[it] = (tok0 + tk < n && tok0 + tk >= lo) ? d : -INFINITY;
+        s[it] = (tok0 + tk < n && (!WINDOW || tok0 + tk >= lo)) ? d : -INFINITY;
         mt = fmaxf(mt, s[it]);
       }
 #pragma unroll
@@ -218,7 +219,7 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
         const int tk = rr + it * TPI;
         const float p = fast_exp2(s[it] - m_new);
         ls += p;
-        if (tok0 + tk < n && tok0 + tk >= lo) {   // other rows may hold anything (NaN)
+        if (tok0 + tk < n && (!WINDOW || tok0 + tk >= lo)) {   // others may hold NaN
           float vf[VEC];
           E::unpack(*reinterpret_cast<const uint4*>(Vs + tk * D + c * VEC), vf);
 #pragma unroll
@@ -325,10 +326,15 @@ cudaError_t launch_typed(void* out, const void* q, const void* kc, const void* v
                          int max_len, float scale, int window, const DecodePlan& plan, void* ws,
                          unsigned* status, cudaStream_t s) {
   using Sh = DecodeShape<T, D>;
-  const bool prefill = cu != nullptr;
-  const void* fn = prefill ? (const void*)paged_decode_kernel<T, D, true>
-                           : (const void*)paged_decode_kernel<T, D, false>;
-  cudaError_t e = set_smem(fn, Sh::SMEM);
+  const bool prefill = cu != nullptr, win = window > 0;
+  using K = void (*)(T*, const T*, const T*, const T*, const int32_t*, const int32_t*,
+                     const int32_t*, const int32_t*, int, int, int, int, int, float, int, int,
+                     float*, float2*, unsigned*);
+  const K kern = prefill ? (win ? paged_decode_kernel<T, D, true, true>
+                                : paged_decode_kernel<T, D, true, false>)
+                         : (win ? paged_decode_kernel<T, D, false, true>
+                                : paged_decode_kernel<T, D, false, false>);
+  cudaError_t e = set_smem((const void*)kern, Sh::SMEM);
   if (e != cudaSuccess) return e;
   const int max_splits = prefill ? 1 : plan.max_splits;
   float* ws_acc = static_cast<float*>(ws);
@@ -336,14 +342,9 @@ cudaError_t launch_typed(void* out, const void* q, const void* kc, const void* v
       static_cast<char*>(ws) + (size_t)R * H * max_splits * D * sizeof(float));
   dim3 grid(prefill ? R * max_q : R, H, max_splits);
   const float scale_log2 = scale * 1.4426950408889634f;
-  if (prefill)
-    paged_decode_kernel<T, D, true><<<grid, kNW * 32, Sh::SMEM, s>>>(
-        (T*)out, (const T*)q, (const T*)kc, (const T*)vc, bt, seq_lens, cu, ctx, max_q, H, NB,
-        MB, max_len, scale_log2, window, max_splits, ws_acc, ws_ml, status);
-  else
-    paged_decode_kernel<T, D, false><<<grid, kNW * 32, Sh::SMEM, s>>>(
-        (T*)out, (const T*)q, (const T*)kc, (const T*)vc, bt, seq_lens, cu, ctx, max_q, H, NB,
-        MB, max_len, scale_log2, window, max_splits, ws_acc, ws_ml, status);
+  kern<<<grid, kNW * 32, Sh::SMEM, s>>>((T*)out, (const T*)q, (const T*)kc, (const T*)vc, bt,
+                                        seq_lens, cu, ctx, max_q, H, NB, MB, max_len, scale_log2,
+                                        window, max_splits, ws_acc, ws_ml, status);
   count_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess || max_splits == 1) return e;
