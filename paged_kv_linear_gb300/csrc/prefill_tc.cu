@@ -5,29 +5,31 @@
 // FlashAttention-type kernel; the result it must equal is causal softmax attention, here
 // read through the per-request block table (§2.1) so a cached prefix is attended as well.
 //
-// GB300 design. One CTA per (128-query tile, head, request); heavy (late) query tiles are
-// scheduled first. Warp roles: two TMA warps (K ring, V ring), an MMA warp and eight
-// softmax warps. K and V come straight from the paged pool: each 128-key tile is eight
-// 16-token blocks, each fetched with two TMA boxes (16 rows x 64 columns, SW128) at the row
-// the block table names, into a 3-deep K ring and a 2-deep V ring; each TMA warp reads the
-// block ids 32 at a time (four tiles) and shares them with shuffles. Per key tile:
-//   S = Q K^T     128 x 128 x 128  A = Q (K-major), B = K (K-major)    -> TMEM, 2 buffers
-//   O += P V      128 x 128 x 128  A = P (TMEM),    B = V (MN-major)   -> TMEM
-// Each query row is split over two softmax threads (two warps, 64 columns each) that swap
-// their partial row max through shared memory once per tile. They apply the causal/length
-// mask, keep the running max and sum, and write bf16 P back into TMEM (two buffers), where
-// P V reads it as its A operand: P never touches shared memory, which leaves the tensor
-// core's shared-memory bandwidth to Q, K and V. O stays in TMEM; a row is rescaled only
-// when its running max grows by more than 2^8 (exponents stay <= 2^8, exact after the
-// final division by the row sum). S is double-buffered so Q K^T of tile j+2 and P V of
-// tile j run on the tensor core while the softmax threads exponentiate tile j+1; they wait
-// for P V only to reuse a P buffer (two tiles back) or to rescale O.
+// GB300 design. One CTA per (pair of 128-query tiles, head, request); heavy (late) pairs
+// are scheduled first. Warp roles: two TMA warps (K ring, V ring), one MMA warp and two
+// softmax warpgroups, one per query tile, one thread per query row (the row's max and sum
+// stay in that thread). K and V come straight from the paged pool: each 128-key tile is
+// eight 16-token blocks, each fetched with two TMA boxes (16 rows x 64 columns, SW128) at
+// the row the block table names; each TMA warp reads the block ids 32 at a time and shares
+// them with shuffles. Per key tile j and query tile t:
+//   S_t = Q_t K_j^T   128 x 128 x 128  A = Q_t (K-major), B = K_j (K-major)  -> TMEM
+//   O_t += P_t V_j    128 x 128 x 128  A = P_t (TMEM),    B = V_j (MN-major) -> TMEM
+// TMEM holds S_0 | S_1 | O_0 | O_1 (4 x 128 columns). The softmax threads read S_t, write
+// bf16 P_t into the first 64 columns of the same S_t region, and P V reads it from there:
+// P never touches shared memory. The MMA warp issues, per key tile,
+//   P_0 V_j, Q_0 K_{j+1}^T, P_1 V_j, Q_1 K_{j+1}^T
+// so the tensor core works on one query tile while the other tile's softmax runs; the
+// tensor pipe executes in issue order, so Q_t K_{j+1}^T overwrites P_t only after P_t V_j
+// has read it, and its completion (the "S full" barrier) also tells the softmax threads
+// that O_t is up to date. O stays in TMEM; a row is rescaled only when its running max
+// grows by more than 2^8 (exponents stay <= 2^8, exact after the final division).
 //
-// Sliding window (window > 0, a query at position i sees keys i - window < p <= i): the
-// key tiles start at the one holding the window start of the tile's first query, blocks
-// before that start are neither looked up nor loaded (their V rows are zeroed in shared
-// memory instead), and the mask adds the lower bound. A row can then see no key at all in
-// its first tiles; its exponent base is held at 0 until it sees one, so those P are 0.
+// Sliding window (window > 0, a query at position i sees keys i - window < p <= i): each
+// query tile walks the key tiles from the one holding its first query's window start;
+// blocks before the pair's window start are neither looked up nor loaded (their V rows are
+// zeroed in shared memory instead), and the mask adds the lower bound. A row can see no
+// key at all in its first tile; its exponent base is held at 0 until it sees one, so those
+// P are 0.
 #include <cuda_bf16.h>
 
 #include "tc.cuh"
@@ -38,17 +40,17 @@ namespace {
 constexpr int kBM = 128, kBN = 128, kD = 128;
 constexpr int kSubQ = 128 * 128;             // [128 rows][64 cols] bf16 sub-tile = 16 KiB
 constexpr int kTile = 2 * kSubQ;             // [128][128] bf16 = 32 KiB
-constexpr int kNK = 3, kNV = 2;              // K and V ring depths
-constexpr int kOffQ = 0;
-constexpr int kOffK = kOffQ + kTile;
+constexpr int kNK = 2, kNV = 2;              // K and V ring depths
+constexpr int kOffQ = 0;                     // two query tiles
+constexpr int kOffK = kOffQ + 2 * kTile;
 constexpr int kOffV = kOffK + kNK * kTile;
 constexpr int kOffBar = kOffV + kNV * kTile;
-constexpr int kSmem = kOffBar + 4096 + 1024;
-constexpr int kNSW = 8;                      // softmax warps: 2 per TMEM lane quarter
+constexpr int kSmem = kOffBar + 1024 + 1024;  // barriers + 1 KiB alignment slack
+constexpr int kNSW = 8;                      // softmax warps: 4 per query tile
 constexpr int kWarpTmaK = kNSW, kWarpTmaV = kNSW + 1, kWarpMma = kNSW + 2;
 constexpr int kThreads = (kNSW + 3) * 32;
-constexpr uint32_t kTmemCols = 512;          // S0 | S1 | O | P0 | P1 (P: bf16 pairs)
-constexpr uint32_t kColO = 256, kColP = 384;
+constexpr uint32_t kTmemCols = 512;          // S_0/P_0 | S_1/P_1 | O_0 | O_1
+constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;
 
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0, 0);
@@ -56,9 +58,12 @@ constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 0, 1);   // A = P from TMEM
 
 struct Bars {
   uint64_t qfull, kfull[kNK], kempty[kNK], vfull[kNV], vempty[kNV];
-  uint64_t sfull[2], pfull[2], odone[2], drain;   // handshakes per tile parity
-  uint64_t pair[4][2];                       // the two warps of a lane quarter, per parity
-  float red[2][2][kBM];                      // row-half partial max per parity; final sums
+  uint64_t sfull[2], pfull[2], odone[2], drain;    // per query tile
+};
+
+// Key-tile range [lo, hi) of one query tile and its key bound.
+struct TileRange {
+  int lo, hi, kv_end;
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -67,21 +72,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                   const int32_t* __restrict__ bt, const int32_t* __restrict__ cu,
                   const int32_t* __restrict__ ctx, int H, int NB, int MB, float scale_log2,
                   int window, unsigned* status) {
-  const int qt = gridDim.x - 1 - blockIdx.x;           // heavy tiles first
+  const int pt = gridDim.x - 1 - blockIdx.x;           // heavy pairs first
   const int h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = cu[b], n = cu[b + 1] - t0;
-  const int q0 = qt * kBM;
+  const int q0 = pt * 2 * kBM;                         // first query of the pair
   if (q0 >= n) return;
   const int c0 = ctx ? ctx[b] : 0;
-  const int rows = min(kBM, n - q0);
-  const int kv_end = c0 + q0 + rows;                   // keys the tile's last query sees
-  const int nkv = (kv_end + kBN - 1) / kBN;
-  const int pos0 = c0 + q0;                            // position of the tile's first query
-  const int key_lo = window > 0 ? max(0, pos0 - window + 1) : 0;   // first key any row sees
-  const int jlo = key_lo / kBN;                        // first key tile
-  const int nloc = nkv - jlo;                          // key tiles this CTA walks
-  const int blk_lo = key_lo / 16;                      // first block looked up and loaded
+  const bool two = q0 + kBM < n;                       // second query tile present
+  TileRange tr[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    const int qt = q0 + t * kBM;
+    const int rows = max(0, min(kBM, n - qt));
+    const int key_lo = window > 0 ? max(0, c0 + qt - window + 1) : 0;
+    tr[t].kv_end = c0 + qt + rows;                     // keys the tile's last query sees
+    tr[t].hi = (tr[t].kv_end + kBN - 1) / kBN;
+    tr[t].lo = key_lo / kBN;
+  }
+  if (!two) tr[1].lo = tr[1].hi = tr[0].hi;            // empty range
+  const int jA = tr[0].lo, jB = two ? tr[1].hi : tr[0].hi;   // union of the two ranges
+  const int nloc = jB - jA;
+  const int kv_end = two ? tr[1].kv_end : tr[0].kv_end;
+  const int blk_lo = (window > 0 ? max(0, c0 + q0 - window + 1) : 0) / 16;
   const int32_t* btrow = bt + (int64_t)b * MB;
   if ((kv_end + 15) / 16 > MB) {
     if (tid == 0) flag(status, HYB_DEVERR_BAD_BLOCK);
@@ -99,17 +112,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       mbar_init(&bars->qfull, 1);
       for (int i = 0; i < kNK; ++i) { mbar_init(&bars->kfull[i], 1); mbar_init(&bars->kempty[i], 1); }
       for (int i = 0; i < kNV; ++i) { mbar_init(&bars->vfull[i], 1); mbar_init(&bars->vempty[i], 1); }
-      mbar_init(&bars->sfull[0], 1);
-      mbar_init(&bars->sfull[1], 1);
-      mbar_init(&bars->pfull[0], kNSW * 32);
-      mbar_init(&bars->pfull[1], kNSW * 32);
-      mbar_init(&bars->odone[0], 1);
-      mbar_init(&bars->odone[1], 1);
-      mbar_init(&bars->drain, 1);
-      for (int qq = 0; qq < 4; ++qq) {
-        mbar_init(&bars->pair[qq][0], 64);
-        mbar_init(&bars->pair[qq][1], 64);
+      for (int t = 0; t < 2; ++t) {
+        mbar_init(&bars->sfull[t], 1);
+        mbar_init(&bars->pfull[t], 128);
+        mbar_init(&bars->odone[t], 1);
       }
+      mbar_init(&bars->drain, 1);
       fence_mbar_init();
     }
     __syncwarp();
@@ -123,7 +131,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 
   if (warp == kWarpTmaK || warp == kWarpTmaV) {
     // ------------------------------------------------------------ TMA warps (K ring, V ring)
-    // Two independent producers so K can run ahead of V (K is needed one tile earlier).
+    // Two independent producers so K can run ahead of V (K is needed one step earlier).
     const bool isk = warp == kWarpTmaK;
     const CUtensorMap* map = isk ? &tk : &tv;
     const int depth = isk ? kNK : kNV;
@@ -134,17 +142,20 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     int issued = 0;
     if (lane == 0) {
       tma_prefetch_desc(map);
-      if (isk) {
+      if (isk) {                                       // both query tiles (rows past T read 0)
         tma_prefetch_desc(&tq);
-        mbar_expect_tx(&bars->qfull, kTile);
-        tma_load_3d(q_s, &tq, 0, h, t0 + q0, &bars->qfull);
-        tma_load_3d(q_s + kSubQ, &tq, 64, h, t0 + q0, &bars->qfull);
+        mbar_expect_tx(&bars->qfull, 2 * kTile);
+#pragma unroll
+        for (int t = 0; t < 2; ++t) {
+          tma_load_3d(q_s + t * kTile, &tq, 0, h, t0 + q0 + t * kBM, &bars->qfull);
+          tma_load_3d(q_s + t * kTile + kSubQ, &tq, 64, h, t0 + q0 + t * kBM, &bars->qfull);
+        }
       }
     }
     int ids = -1;                                      // block ids of 4 tiles, one per lane
-    for (int jj = 0; jj < nloc; ++jj) {                // jj: local tile index, j = jlo + jj
+    for (int jj = 0; jj < nloc; ++jj) {                // local tile index, key tile jA + jj
       if ((jj & 3) == 0) {
-        const int lb = (jlo + jj) * 8 + lane;
+        const int lb = (jA + jj) * 8 + lane;
         ids = -1;
         if (lb >= blk_lo && lb * 16 < kv_end) {
           ids = btrow[lb];
@@ -187,49 +198,43 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA warp
     bool ok = true;
-    // descriptors built once; every MMA below adds a compile-time offset
+    // descriptors built once; every MMA below adds a compile-time or per-tile offset
     const uint64_t qdesc = sw128_desc(smem_u32(q_s), 16, 1024);
     const uint64_t kdesc = sw128_desc(smem_u32(sm + kOffK), 16, 1024);
     const uint64_t vdesc = sw128_desc(smem_u32(sm + kOffV), kSubQ, 1024);
-    auto issue_qk = [&](int j) -> bool {           // S[j%2] = Q K_j^T (j: local tile index)
-      const int ks = j % kNK;
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->kfull[ks], (j / kNK) & 1))) return false;
+    auto active = [&](int t, int j) { return j >= tr[t].lo && j < tr[t].hi; };
+    auto issue_qk = [&](int t, int ks) {               // S_t = Q_t K^T, K from ring slot ks
       if (lane == 0) {
         tc_fence_after();
+        const uint64_t qd = desc_add(qdesc, t * kTile);
         const uint64_t kd = desc_add(kdesc, ks * kTile);
-        const uint32_t sd = tmem + (j & 1) * 128;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
           const uint32_t off = (k >> 2) * kSubQ + (k & 3) * 32;
-          tc_mma(sd, desc_add(qdesc, off), desc_add(kd, off), kIdescQK, k > 0);
+          tc_mma(tmem + t * 128, desc_add(qd, off), desc_add(kd, off), kIdescQK, k > 0);
         }
-        tc_commit(&bars->sfull[j & 1]);
-        tc_commit(&bars->kempty[ks]);
+        tc_commit(&bars->sfull[t]);
       }
       __syncwarp();
-      return true;
     };
+    int npv[2] = {0, 0};                               // P V products issued per query tile
     ok = __all_sync(0xffffffffu, mbar_wait(&bars->qfull, 0));
-    if (ok) ok = issue_qk(0);
-    if (ok && nloc > 1) ok = issue_qk(1);
-    for (int j = 0; j < nloc && ok; ++j) {           // local tile index; keys from (jlo+j)*128
-      const int vs = j % kNV;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->pfull[j & 1], (j >> 1) & 1));
-      if (!ok) break;
-      // softmax of tile j is done with S buffer j&1: queue Q K_{j+2} first so the softmax
-      // threads have their next-but-one scores early (an MMA issue blocks while the tensor
-      // core is busy, so issue order is execution order)
-      if (j + 2 < nloc) {
-        ok = issue_qk(j + 2);
-        if (!ok) break;
-      }
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->vfull[vs], (j / kNV) & 1));
+    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->kfull[0], 0));
+    if (ok) {
+      for (int t = 0; t < 2; ++t)
+        if (active(t, jA)) issue_qk(t, 0);
+      if (lane == 0) tc_commit(&bars->kempty[0]);
+      __syncwarp();
+    }
+    for (int jj = 0; jj < nloc && ok; ++jj) {
+      const int j = jA + jj, vs = jj % kNV, ks1 = (jj + 1) % kNK;
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->vfull[vs], (jj / kNV) & 1));
       if (!ok) break;
       uint8_t* v_s = sm + kOffV + vs * kTile;
       // V rows that were not loaded := 0 (P is 0 there, but stale shared memory may hold
       // NaN): rows past kv_end in the last tile, rows before the window's first block
-      const int kb = (jlo + j) * kBN;
-      const int head = j == 0 ? blk_lo * 16 - kb : 0;
+      const int kb = j * kBN;
+      const int head = jj == 0 ? blk_lo * 16 - kb : 0;
       const int tail = kv_end - kb;
       if (head > 0 || tail < kBN) {
         auto zero_rows = [&](int r0, int r1) {
@@ -243,16 +248,40 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         fence_async_smem();
       }
       __syncwarp();
-      if (lane == 0) {
-        tc_fence_after();
-        const uint64_t vd = desc_add(vdesc, vs * kTile);
-        const uint32_t pt = tmem + kColP + (j & 1) * 64;
+      bool kready = false;
+      for (int t = 0; t < 2 && ok; ++t) {
+        const bool now = active(t, j), next = active(t, j + 1);
+        if (now) {                                     // O_t += P_t V_j once P_t is written
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->pfull[t], npv[t] & 1));
+          if (!ok) break;
+          if (lane == 0) {
+            tc_fence_after();
+            const uint64_t vd = desc_add(vdesc, vs * kTile);
+            const uint32_t pt_col = tmem + t * 128;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)                // O += P V_j, P read from TMEM buffer j&1
-          tc_mma_ta(tmem + kColO, pt + k * 8, desc_add(vd, k * 2048), kIdescPV,
-                    (j > 0 || k > 0) ? 1u : 0u);
-        tc_commit(&bars->odone[j & 1]);
+            for (int k = 0; k < 8; ++k)
+              tc_mma_ta(tmem + kColO + t * 128, pt_col + k * 8, desc_add(vd, k * 2048), kIdescPV,
+                        (npv[t] > 0 || k > 0) ? 1u : 0u);
+          }
+          __syncwarp();
+          ++npv[t];
+        }
+        if (next) {                                    // then S_t = Q_t K_{j+1}^T (overwrites P_t)
+          if (!kready) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->kfull[ks1], ((jj + 1) / kNK) & 1));
+            if (!ok) break;
+            kready = true;
+          }
+          issue_qk(t, ks1);
+        } else if (now) {
+          if (lane == 0) tc_commit(&bars->odone[t]);   // O_t complete
+          __syncwarp();
+        }
+      }
+      if (!ok) break;
+      if (lane == 0) {
         tc_commit(&bars->vempty[vs]);
+        if (kready) tc_commit(&bars->kempty[ks1]);
       }
       __syncwarp();
     }
@@ -262,113 +291,95 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       mbar_wait(&bars->drain, 0, 100000000ull);
     }
   } else {
-    // ------------------------------------------------------------ softmax warps
-    const int quarter = warp & 3, hf = warp >> 2;      // TMEM lane quarter, column half
+    // ------------------------------------------------------------ softmax warpgroups
+    const int t = warp >> 2, quarter = warp & 3;       // query tile, TMEM lane quarter
     const int r = quarter * 32 + lane;                 // query row of the tile = TMEM lane
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
+    const uint32_t s_col = tl + t * 128, o_col = tl + kColO + t * 128;
+    const int pos0 = c0 + q0 + t * kBM;                // position of the tile's first query
     const int qp = pos0 + r;                           // absolute query position
     const int qlo = window > 0 ? qp - window : -1;     // keys kp > qlo are in the window
-    const int c0h = hf * 64;                           // this thread's 64 columns
-    float m_used = -INFINITY, l = 0.f;                 // l: this half's share of the row sum
+    const int tkv_end = tr[t].kv_end;
+    float m_used = -INFINITY, l = 0.f;
     bool ok = true;
-    // swap a value with the other half of this row (exchange number idx); bounded wait
-    auto pair_swap = [&](int idx, float v, float& other) -> bool {
-      bars->red[idx & 1][hf][r] = v;
-      mbar_arrive(&bars->pair[quarter][idx & 1]);
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->pair[quarter][idx & 1], (idx >> 1) & 1)))
-        return false;
-      other = bars->red[idx & 1][hf ^ 1][r];
-      return true;
-    };
-    for (int j = 0; j < nloc && ok; ++j) {            // local tile index; keys from (jlo+j)*128
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->sfull[j & 1], (j >> 1) & 1));
+    int it = 0;
+    for (int j = tr[t].lo; j < tr[t].hi && ok; ++j, ++it) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->sfull[t], it & 1));
       if (!ok) break;
       tc_fence_after();
-      float x[64];
-      tmem_ld32(tl + (j & 1) * 128 + c0h, x);
-      tmem_ld32(tl + (j & 1) * 128 + c0h + 32, x + 32);
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(s_col + c * 32, x + c * 32);
       tmem_ld_wait();
-      const int kbase = (jlo + j) * kBN + c0h;
-      const bool masked = kbase + 63 > pos0 || kbase + 64 > kv_end ||
+      const int kbase = j * kBN;
+      const bool masked = kbase + kBN - 1 > pos0 || kbase + kBN > tkv_end ||
                           (window > 0 && kbase <= pos0 + kBM - 1 - window);
       if (masked) {
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
+        for (int c = 0; c < 128; ++c) {
           const int kp = kbase + c;
-          x[c] = (kp <= qp && kp < kv_end && kp > qlo) ? x[c] : -INFINITY;
+          x[c] = (kp <= qp && kp < tkv_end && kp > qlo) ? x[c] : -INFINITY;
         }
       }
-      // partial max of the raw scores (scale > 0 keeps the order): 8 independent chains
+      // row max of the raw scores (scale > 0 keeps the order): 8 independent chains
       float mp[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mp[i] = x[i];
 #pragma unroll
-      for (int c = 8; c < 64; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
-      float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                       fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
-      float mx_other;
-      ok = pair_swap(j, mx, mx_other);
-      if (!ok) break;
-      mx = fmaxf(mx, mx_other) * scale_log2;
+      for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * scale_log2;
       const float m_new = fmaxf(m_used, mx);
       const bool grow = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new != -INFINITY);
       const float m_tgt = grow ? m_new : m_used;
       const float m_sub = m_tgt == -INFINITY ? 0.f : m_tgt;   // no key seen yet: P = 0
-      // exponentials of this tile first: they do not depend on P V of the previous tile.
-      // p = 2^(x * scale_log2 - m) as one fma per element; sum in 8 independent chains.
-      uint32_t w[32];
+      // p = 2^(x * scale_log2 - m) as one fma per element; sum in 8 independent chains
+      uint32_t w[64];
       float sp[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) sp[i] = 0.f;
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
+      for (int c = 0; c < 64; ++c) {
         const float p0 = fast_exp2(fmaf(x[2 * c], scale_log2, -m_sub));
         const float p1 = fast_exp2(fmaf(x[2 * c + 1], scale_log2, -m_sub));
         sp[c & 7] += p0 + p1;
         w[c] = pack_bf16(p0, p1);
       }
       const float ls = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
-      if (j >= 2) {                                    // P V_{j-2} done: P buffer j&1 free
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone[j & 1], ((j - 2) >> 1) & 1));
-        if (!ok) break;
-      }
-      if (j >= 1 && __any_sync(0xffffffffu, grow)) {   // rescale O once P V_{j-1} is in
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone[(j - 1) & 1], ((j - 1) >> 1) & 1));
-        if (!ok) break;
-        tc_fence_after();
+      // O_t holds P V of every earlier tile: the S-full barrier that released this tile
+      // completes after them (same tensor pipe, issued before)
+      if (it >= 1 && __any_sync(0xffffffffu, grow)) {
         const float alpha = (grow && m_used != -INFINITY) ? fast_exp2(m_used - m_new) : 1.f;
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {                  // warp-wide TMEM access, per-row factor
+        for (int c = 0; c < 4; ++c) {                  // warp-wide TMEM access, per-row factor
           float o[32];
-          tmem_ld32(tl + kColO + c0h + c * 32, o);
+          tmem_ld32(o_col + c * 32, o);
           tmem_ld_wait();
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] *= alpha;
-          tmem_st32(tl + kColO + c0h + c * 32, o);
+          tmem_st32(o_col + c * 32, o);
         }
         if (grow) l *= alpha;
       }
       m_used = m_tgt;
       l += ls;
-      tc_fence_after();
-      tmem_st32u(tl + kColP + (j & 1) * 64 + hf * 32, w);   // keys c0h..c0h+63 as bf16 pairs
+      tmem_st32u(s_col, w);                            // P_t: keys 0..127 as bf16 pairs
+      tmem_st32u(s_col + 32, w + 32);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(&bars->pfull[j & 1]);
+      mbar_arrive(&bars->pfull[t]);
     }
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone[(nloc - 1) & 1], ((nloc - 1) >> 1) & 1));
-    float l_other = 0.f;
-    if (ok) ok = pair_swap(nloc, l, l_other);          // row sum = both halves' shares
-    if (ok) {
-      const float lt = l + l_other;
+    if (ok && tr[t].hi > tr[t].lo)
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone[t], 0));
+    if (ok && tr[t].hi > tr[t].lo) {
       tc_fence_after();
-      const bool store = q0 + r < n;
-      const float inv = lt > 0.f ? 1.f / lt : 0.f;
-      __nv_bfloat16* orow = out + ((int64_t)(t0 + q0 + r) * H + h) * kD + c0h;
+      const bool store = q0 + t * kBM + r < n;
+      const float inv = l > 0.f ? 1.f / l : 0.f;
+      __nv_bfloat16* orow = out + ((int64_t)(t0 + q0 + t * kBM + r) * H + h) * kD;
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
+      for (int c = 0; c < 4; ++c) {
         float o[32];
-        tmem_ld32(tl + kColO + c0h + c * 32, o);
+        tmem_ld32(o_col + c * 32, o);
         tmem_ld_wait();
         if (store) {
 #pragma unroll
@@ -382,7 +393,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
           }
         }
       }
-    } else if (lane == 0) {
+    } else if (!ok && lane == 0) {
       flag(status, HYB_DEVERR_TIMEOUT);
     }
   }
@@ -414,7 +425,7 @@ cudaError_t launch_prefill_tc(void* out, const void* q, const void* kc, const vo
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem((const void*)prefill_tc_kernel, kSmem);
   if (e != cudaSuccess) return e;
-  dim3 grid((max_q_len + kBM - 1) / kBM, H, B);
+  dim3 grid((max_q_len + 2 * kBM - 1) / (2 * kBM), H, B);
   prefill_tc_kernel<<<grid, kThreads, kSmem, s>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(out), bt,
                                                   cu, ctx, H, NB, MB, scale * 1.4426950408889634f,
                                                   window, status);
