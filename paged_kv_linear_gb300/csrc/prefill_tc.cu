@@ -47,8 +47,13 @@ constexpr int kOffV = kOffK + kNK * kTile;
 constexpr int kOffBar = kOffV + kNV * kTile;
 constexpr int kSmem = kOffBar + 1024 + 1024;  // barriers + 1 KiB alignment slack
 constexpr int kNSW = 8;                      // softmax warps: 4 per query tile
-constexpr int kWarpTmaK = kNSW, kWarpTmaV = kNSW + 1, kWarpMma = kNSW + 2;
-constexpr int kThreads = (kNSW + 3) * 32;
+constexpr int kWarpTmaK = kNSW, kWarpTmaV = kNSW + 1, kWarpMma = kNSW + 2;   // + 1 idle warp
+constexpr int kThreads = (kNSW + 4) * 32;    // three full warpgroups
+// Register split (setmaxnreg): the launch gives 384 threads x 168 registers (three warps
+// per SM sub-partition). The producer warpgroup drops to 80 and the two softmax warpgroups
+// rise to 208: 2 x 128 x 208 + 128 x 80 = 63 488 <= 64 512 registers of the launch, and
+// (208 + 208 + 80) x 32 = 15 872 <= 16 384 per sub-partition.
+constexpr uint32_t kRegsSoftmax = 208, kRegsProducer = 80;
 constexpr uint32_t kTmemCols = 512;          // S_0/P_0 | S_1/P_1 | O_0 | O_1
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;
@@ -60,6 +65,32 @@ struct Bars {
   uint64_t qfull, kfull[kNK], kempty[kNK], vfull[kNV], vempty[kNV];
   uint64_t sfull[2], pfull[2], odone[2], drain;    // per query tile
 };
+
+// Paired fp32 arithmetic (one instruction for two lanes of a float2) and a three-input max:
+// the softmax threads spend most of their issue slots on per-score work.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rc, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\tmov.b64 rc, {%6, %7};\n\t"
+      "fma.rn.f32x2 rd, ra, rb, rc;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+  float2 d;
+  asm("{\n\t.reg .b64 ra, rb, rd;\n\t"
+      "mov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+      "add.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
 
 // Key-tile range [lo, hi) of one query tile and its key bound.
 struct TileRange {
@@ -129,168 +160,172 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
   const uint32_t tmem = tmem_base;
   uint8_t* const q_s = sm + kOffQ;
 
-  if (warp == kWarpTmaK || warp == kWarpTmaV) {
-    // ------------------------------------------------------------ TMA warps (K ring, V ring)
-    // Two independent producers so K can run ahead of V (K is needed one step earlier).
-    const bool isk = warp == kWarpTmaK;
-    const CUtensorMap* map = isk ? &tk : &tv;
-    const int depth = isk ? kNK : kNV;
-    uint8_t* const ring = sm + (isk ? kOffK : kOffV);
-    uint64_t* const fullb = isk ? bars->kfull : bars->vfull;
-    uint64_t* const emptyb = isk ? bars->kempty : bars->vempty;
-    bool ok = true;
-    int issued = 0;
-    if (lane == 0) {
-      tma_prefetch_desc(map);
-      if (isk) {                                       // both query tiles (rows past T read 0)
-        tma_prefetch_desc(&tq);
-        mbar_expect_tx(&bars->qfull, 2 * kTile);
-#pragma unroll
-        for (int t = 0; t < 2; ++t) {
-          tma_load_3d(q_s + t * kTile, &tq, 0, h, t0 + q0 + t * kBM, &bars->qfull);
-          tma_load_3d(q_s + t * kTile + kSubQ, &tq, 64, h, t0 + q0 + t * kBM, &bars->qfull);
-        }
-      }
-    }
-    int ids = -1;                                      // block ids of 4 tiles, one per lane
-    for (int jj = 0; jj < nloc; ++jj) {                // local tile index, key tile jA + jj
-      if ((jj & 3) == 0) {
-        const int lb = (jA + jj) * 8 + lane;
-        ids = -1;
-        if (lb >= blk_lo && lb * 16 < kv_end) {
-          ids = btrow[lb];
-          if (ids < 0 || ids >= NB) {
-            flag(status, HYB_DEVERR_BAD_BLOCK);
-            ids = -1;
-          }
-        }
-      }
-      int blk[8];
-      int nbox = 0;
-#pragma unroll
-      for (int bi = 0; bi < 8; ++bi) {
-        blk[bi] = __shfl_sync(0xffffffffu, ids, (jj & 3) * 8 + bi);
-        nbox += blk[bi] >= 0 ? 2 : 0;
-      }
-      const int slot = jj % depth;
-      if (jj >= depth) {
-        ok = __all_sync(0xffffffffu, mbar_wait(&emptyb[slot], ((jj - depth) / depth) & 1));
-        if (!ok) break;
-      }
+  if (warp >= kNSW) {                               // producer warpgroup
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsProducer));
+    if (warp == kWarpTmaK || warp == kWarpTmaV) {
+      // ------------------------------------------------------------ TMA warps (K ring, V ring)
+      // Two independent producers so K can run ahead of V (K is needed one step earlier).
+      const bool isk = warp == kWarpTmaK;
+      const CUtensorMap* map = isk ? &tk : &tv;
+      const int depth = isk ? kNK : kNV;
+      uint8_t* const ring = sm + (isk ? kOffK : kOffV);
+      uint64_t* const fullb = isk ? bars->kfull : bars->vfull;
+      uint64_t* const emptyb = isk ? bars->kempty : bars->vempty;
+      bool ok = true;
+      int issued = 0;
       if (lane == 0) {
-        uint8_t* dst = ring + slot * kTile;
-        mbar_expect_tx(&fullb[slot], nbox * 2048);
-#pragma unroll
-        for (int bi = 0; bi < 8; ++bi)
-          if (blk[bi] >= 0) {
-            const int y = (blk[bi] * H + h) * 16;
-            tma_load_2d(dst + bi * 2048, map, 0, y, &fullb[slot]);
-            tma_load_2d(dst + kSubQ + bi * 2048, map, 64, y, &fullb[slot]);
+        tma_prefetch_desc(map);
+        if (isk) {                                       // both query tiles (rows past T read 0)
+          tma_prefetch_desc(&tq);
+          mbar_expect_tx(&bars->qfull, 2 * kTile);
+  #pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            tma_load_3d(q_s + t * kTile, &tq, 0, h, t0 + q0 + t * kBM, &bars->qfull);
+            tma_load_3d(q_s + t * kTile + kSubQ, &tq, 64, h, t0 + q0 + t * kBM, &bars->qfull);
           }
-      }
-      issued = jj + 1;
-    }
-    if (!ok && lane == 0) {                            // let the loads in flight land
-      flag(status, HYB_DEVERR_TIMEOUT);
-      for (int j = max(0, issued - depth); j < issued; ++j)
-        mbar_wait(&fullb[j % depth], (j / depth) & 1, 100000000ull);
-    }
-  } else if (warp == kWarpMma) {
-    // ------------------------------------------------------------ MMA warp
-    bool ok = true;
-    // descriptors built once; every MMA below adds a compile-time or per-tile offset
-    const uint64_t qdesc = sw128_desc(smem_u32(q_s), 16, 1024);
-    const uint64_t kdesc = sw128_desc(smem_u32(sm + kOffK), 16, 1024);
-    const uint64_t vdesc = sw128_desc(smem_u32(sm + kOffV), kSubQ, 1024);
-    auto active = [&](int t, int j) { return j >= tr[t].lo && j < tr[t].hi; };
-    auto issue_qk = [&](int t, int ks) {               // S_t = Q_t K^T, K from ring slot ks
-      if (lane == 0) {
-        tc_fence_after();
-        const uint64_t qd = desc_add(qdesc, t * kTile);
-        const uint64_t kd = desc_add(kdesc, ks * kTile);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          const uint32_t off = (k >> 2) * kSubQ + (k & 3) * 32;
-          tc_mma(tmem + t * 128, desc_add(qd, off), desc_add(kd, off), kIdescQK, k > 0);
         }
-        tc_commit(&bars->sfull[t]);
       }
-      __syncwarp();
-    };
-    int npv[2] = {0, 0};                               // P V products issued per query tile
-    ok = __all_sync(0xffffffffu, mbar_wait(&bars->qfull, 0));
-    if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->kfull[0], 0));
-    if (ok) {
-      for (int t = 0; t < 2; ++t)
-        if (active(t, jA)) issue_qk(t, 0);
-      if (lane == 0) tc_commit(&bars->kempty[0]);
-      __syncwarp();
-    }
-    for (int jj = 0; jj < nloc && ok; ++jj) {
-      const int j = jA + jj, vs = jj % kNV, ks1 = (jj + 1) % kNK;
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->vfull[vs], (jj / kNV) & 1));
-      if (!ok) break;
-      uint8_t* v_s = sm + kOffV + vs * kTile;
-      // V rows that were not loaded := 0 (P is 0 there, but stale shared memory may hold
-      // NaN): rows past kv_end in the last tile, rows before the window's first block
-      const int kb = j * kBN;
-      const int head = jj == 0 ? blk_lo * 16 - kb : 0;
-      const int tail = kv_end - kb;
-      if (head > 0 || tail < kBN) {
-        auto zero_rows = [&](int r0, int r1) {
-          for (int e = lane; e < (r1 - r0) * 16; e += 32) {
-            const int r = r0 + e / 16, sb = (e >> 3) & 1, ch = e & 7;
-            *reinterpret_cast<uint4*>(v_s + sb * kSubQ + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+      int ids = -1;                                      // block ids of 4 tiles, one per lane
+      for (int jj = 0; jj < nloc; ++jj) {                // local tile index, key tile jA + jj
+        if ((jj & 3) == 0) {
+          const int lb = (jA + jj) * 8 + lane;
+          ids = -1;
+          if (lb >= blk_lo && lb * 16 < kv_end) {
+            ids = btrow[lb];
+            if (ids < 0 || ids >= NB) {
+              flag(status, HYB_DEVERR_BAD_BLOCK);
+              ids = -1;
+            }
           }
-        };
-        if (head > 0) zero_rows(0, head);
-        if (tail < kBN) zero_rows(tail, kBN);
-        fence_async_smem();
-      }
-      __syncwarp();
-      bool kready = false;
-      for (int t = 0; t < 2 && ok; ++t) {
-        const bool now = active(t, j), next = active(t, j + 1);
-        if (now) {                                     // O_t += P_t V_j once P_t is written
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars->pfull[t], npv[t] & 1));
+        }
+        int blk[8];
+        int nbox = 0;
+  #pragma unroll
+        for (int bi = 0; bi < 8; ++bi) {
+          blk[bi] = __shfl_sync(0xffffffffu, ids, (jj & 3) * 8 + bi);
+          nbox += blk[bi] >= 0 ? 2 : 0;
+        }
+        const int slot = jj % depth;
+        if (jj >= depth) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&emptyb[slot], ((jj - depth) / depth) & 1));
           if (!ok) break;
-          if (lane == 0) {
-            tc_fence_after();
-            const uint64_t vd = desc_add(vdesc, vs * kTile);
-            const uint32_t pt_col = tmem + t * 128;
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              tc_mma_ta(tmem + kColO + t * 128, pt_col + k * 8, desc_add(vd, k * 2048), kIdescPV,
-                        (npv[t] > 0 || k > 0) ? 1u : 0u);
-          }
-          __syncwarp();
-          ++npv[t];
         }
-        if (next) {                                    // then S_t = Q_t K_{j+1}^T (overwrites P_t)
-          if (!kready) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->kfull[ks1], ((jj + 1) / kNK) & 1));
+        if (lane == 0) {
+          uint8_t* dst = ring + slot * kTile;
+          mbar_expect_tx(&fullb[slot], nbox * 2048);
+  #pragma unroll
+          for (int bi = 0; bi < 8; ++bi)
+            if (blk[bi] >= 0) {
+              const int y = (blk[bi] * H + h) * 16;
+              tma_load_2d(dst + bi * 2048, map, 0, y, &fullb[slot]);
+              tma_load_2d(dst + kSubQ + bi * 2048, map, 64, y, &fullb[slot]);
+            }
+        }
+        issued = jj + 1;
+      }
+      if (!ok && lane == 0) {                            // let the loads in flight land
+        flag(status, HYB_DEVERR_TIMEOUT);
+        for (int j = max(0, issued - depth); j < issued; ++j)
+          mbar_wait(&fullb[j % depth], (j / depth) & 1, 100000000ull);
+      }
+    } else if (warp == kWarpMma) {
+      // ------------------------------------------------------------ MMA warp
+      bool ok = true;
+      // descriptors built once; every MMA below adds a compile-time or per-tile offset
+      const uint64_t qdesc = sw128_desc(smem_u32(q_s), 16, 1024);
+      const uint64_t kdesc = sw128_desc(smem_u32(sm + kOffK), 16, 1024);
+      const uint64_t vdesc = sw128_desc(smem_u32(sm + kOffV), kSubQ, 1024);
+      auto active = [&](int t, int j) { return j >= tr[t].lo && j < tr[t].hi; };
+      auto issue_qk = [&](int t, int ks) {               // S_t = Q_t K^T, K from ring slot ks
+        if (lane == 0) {
+          tc_fence_after();
+          const uint64_t qd = desc_add(qdesc, t * kTile);
+          const uint64_t kd = desc_add(kdesc, ks * kTile);
+  #pragma unroll
+          for (int k = 0; k < 8; ++k) {
+            const uint32_t off = (k >> 2) * kSubQ + (k & 3) * 32;
+            tc_mma(tmem + t * 128, desc_add(qd, off), desc_add(kd, off), kIdescQK, k > 0);
+          }
+          tc_commit(&bars->sfull[t]);
+        }
+        __syncwarp();
+      };
+      int npv[2] = {0, 0};                               // P V products issued per query tile
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->qfull, 0));
+      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->kfull[0], 0));
+      if (ok) {
+        for (int t = 0; t < 2; ++t)
+          if (active(t, jA)) issue_qk(t, 0);
+        if (lane == 0) tc_commit(&bars->kempty[0]);
+        __syncwarp();
+      }
+      for (int jj = 0; jj < nloc && ok; ++jj) {
+        const int j = jA + jj, vs = jj % kNV, ks1 = (jj + 1) % kNK;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->vfull[vs], (jj / kNV) & 1));
+        if (!ok) break;
+        uint8_t* v_s = sm + kOffV + vs * kTile;
+        // V rows that were not loaded := 0 (P is 0 there, but stale shared memory may hold
+        // NaN): rows past kv_end in the last tile, rows before the window's first block
+        const int kb = j * kBN;
+        const int head = jj == 0 ? blk_lo * 16 - kb : 0;
+        const int tail = kv_end - kb;
+        if (head > 0 || tail < kBN) {
+          auto zero_rows = [&](int r0, int r1) {
+            for (int e = lane; e < (r1 - r0) * 16; e += 32) {
+              const int r = r0 + e / 16, sb = (e >> 3) & 1, ch = e & 7;
+              *reinterpret_cast<uint4*>(v_s + sb * kSubQ + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+            }
+          };
+          if (head > 0) zero_rows(0, head);
+          if (tail < kBN) zero_rows(tail, kBN);
+          fence_async_smem();
+        }
+        __syncwarp();
+        bool kready = false;
+        for (int t = 0; t < 2 && ok; ++t) {
+          const bool now = active(t, j), next = active(t, j + 1);
+          if (now) {                                     // O_t += P_t V_j once P_t is written
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->pfull[t], npv[t] & 1));
             if (!ok) break;
-            kready = true;
+            if (lane == 0) {
+              tc_fence_after();
+              const uint64_t vd = desc_add(vdesc, vs * kTile);
+              const uint32_t pt_col = tmem + t * 128;
+  #pragma unroll
+              for (int k = 0; k < 8; ++k)
+                tc_mma_ta(tmem + kColO + t * 128, pt_col + k * 8, desc_add(vd, k * 2048), kIdescPV,
+                          (npv[t] > 0 || k > 0) ? 1u : 0u);
+            }
+            __syncwarp();
+            ++npv[t];
           }
-          issue_qk(t, ks1);
-        } else if (now) {
-          if (lane == 0) tc_commit(&bars->odone[t]);   // O_t complete
-          __syncwarp();
+          if (next) {                                    // then S_t = Q_t K_{j+1}^T (overwrites P_t)
+            if (!kready) {
+              ok = __all_sync(0xffffffffu, mbar_wait(&bars->kfull[ks1], ((jj + 1) / kNK) & 1));
+              if (!ok) break;
+              kready = true;
+            }
+            issue_qk(t, ks1);
+          } else if (now) {
+            if (lane == 0) tc_commit(&bars->odone[t]);   // O_t complete
+            __syncwarp();
+          }
         }
+        if (!ok) break;
+        if (lane == 0) {
+          tc_commit(&bars->vempty[vs]);
+          if (kready) tc_commit(&bars->kempty[ks1]);
+        }
+        __syncwarp();
       }
-      if (!ok) break;
-      if (lane == 0) {
-        tc_commit(&bars->vempty[vs]);
-        if (kready) tc_commit(&bars->kempty[ks1]);
+      if (!ok && lane == 0) {
+        flag(status, HYB_DEVERR_TIMEOUT);
+        tc_commit(&bars->drain);
+        mbar_wait(&bars->drain, 0, 100000000ull);
       }
-      __syncwarp();
     }
-    if (!ok && lane == 0) {
-      flag(status, HYB_DEVERR_TIMEOUT);
-      tc_commit(&bars->drain);
-      mbar_wait(&bars->drain, 0, 100000000ull);
-    }
-  } else {
+  } else {                                           // softmax warpgroups
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoftmax));
     // ------------------------------------------------------------ softmax warpgroups
     const int t = warp >> 2, quarter = warp & 3;       // query tile, TMEM lane quarter
     const int r = quarter * 32 + lane;                 // query row of the tile = TMEM lane
@@ -299,11 +334,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     const int pos0 = c0 + q0 + t * kBM;                // position of the tile's first query
     const int qp = pos0 + r;                           // absolute query position
     const int qlo = window > 0 ? qp - window : -1;     // keys kp > qlo are in the window
-    const int tkv_end = tr[t].kv_end;
+    const TileRange my = t ? tr[1] : tr[0];            // (selects: no local-memory array)
+    const int tkv_end = my.kv_end;
     float m_used = -INFINITY, l = 0.f;
     bool ok = true;
     int it = 0;
-    for (int j = tr[t].lo; j < tr[t].hi && ok; ++j, ++it) {
+    for (int j = my.lo; j < my.hi && ok; ++j, ++it) {
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->sfull[t], it & 1));
       if (!ok) break;
       tc_fence_after();
@@ -321,31 +357,38 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
           x[c] = (kp <= qp && kp < tkv_end && kp > qlo) ? x[c] : -INFINITY;
         }
       }
-      // row max of the raw scores (scale > 0 keeps the order): 8 independent chains
+      // row max of the raw scores (scale > 0 keeps the order): 8 independent chains of
+      // three-input maxima
       float mp[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) mp[i] = x[i];
 #pragma unroll
-      for (int c = 8; c < 128; ++c) mp[c & 7] = fmaxf(mp[c & 7], x[c]);
-      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * scale_log2;
+      for (int c = 8; c + 16 <= 128; c += 16)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) mp[i] = max3f(mp[i], x[c + i], x[c + 8 + i]);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mp[i] = fmaxf(mp[i], x[120 + i]);
+      const float mx = max3f(max3f(mp[0], mp[1], mp[2]), max3f(mp[3], mp[4], mp[5]),
+                             fmaxf(mp[6], mp[7])) * scale_log2;
       const float m_new = fmaxf(m_used, mx);
       const bool grow = m_new > m_used + kRescaleLog2 || (m_used == -INFINITY && m_new != -INFINITY);
       const float m_tgt = grow ? m_new : m_used;
       const float m_sub = m_tgt == -INFINITY ? 0.f : m_tgt;   // no key seen yet: P = 0
-      // p = 2^(x * scale_log2 - m) as one fma per element; sum in 8 independent chains
+      // p = 2^(x * scale_log2 - m): one paired fma per two scores; sums in 4 paired chains
       uint32_t w[64];
-      float sp[8];
+      float2 sp[4];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) sp[i] = 0.f;
+      for (int i = 0; i < 4; ++i) sp[i] = make_float2(0.f, 0.f);
+      const float2 sc2 = make_float2(scale_log2, scale_log2), nm2 = make_float2(-m_sub, -m_sub);
 #pragma unroll
       for (int c = 0; c < 64; ++c) {
-        const float p0 = fast_exp2(fmaf(x[2 * c], scale_log2, -m_sub));
-        const float p1 = fast_exp2(fmaf(x[2 * c + 1], scale_log2, -m_sub));
-        sp[c & 7] += p0 + p1;
-        w[c] = pack_bf16(p0, p1);
+        const float2 y = fma2(make_float2(x[2 * c], x[2 * c + 1]), sc2, nm2);
+        const float2 p = make_float2(fast_exp2(y.x), fast_exp2(y.y));
+        sp[c & 3] = add2(sp[c & 3], p);
+        w[c] = pack_bf16(p.x, p.y);
       }
-      const float ls = ((sp[0] + sp[1]) + (sp[2] + sp[3])) + ((sp[4] + sp[5]) + (sp[6] + sp[7]));
+      const float2 s01 = add2(add2(sp[0], sp[1]), add2(sp[2], sp[3]));
+      const float ls = s01.x + s01.y;
       // O_t holds P V of every earlier tile: the S-full barrier that released this tile
       // completes after them (same tensor pipe, issued before)
       if (it >= 1 && __any_sync(0xffffffffu, grow)) {
@@ -369,9 +412,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       tc_fence_before();
       mbar_arrive(&bars->pfull[t]);
     }
-    if (ok && tr[t].hi > tr[t].lo)
+    if (ok && my.hi > my.lo)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone[t], 0));
-    if (ok && tr[t].hi > tr[t].lo) {
+    if (ok && my.hi > my.lo) {
       tc_fence_after();
       const bool store = q0 + t * kBM + r < n;
       const float inv = l > 0.f ? 1.f / l : 0.f;
