@@ -40,7 +40,7 @@ namespace {
 constexpr int kBM = 128, kBN = 128, kD = 128;
 constexpr int kSubQ = 128 * 128;             // [128 rows][64 cols] bf16 sub-tile = 16 KiB
 constexpr int kTile = 2 * kSubQ;             // [128][128] bf16 = 32 KiB
-constexpr int kNK = 2, kNV = 2;              // K and V ring depths
+constexpr int kNK = 2, kNV = 3;              // K and V ring depths (226 KiB in all)
 constexpr int kOffQ = 0;                     // two query tiles
 constexpr int kOffK = kOffQ + 2 * kTile;
 constexpr int kOffV = kOffK + kNK * kTile;
@@ -50,10 +50,10 @@ constexpr int kNSW = 8;                      // softmax warps: 4 per query tile
 constexpr int kWarpTmaK = kNSW, kWarpTmaV = kNSW + 1, kWarpMma = kNSW + 2;   // + 1 idle warp
 constexpr int kThreads = (kNSW + 4) * 32;    // three full warpgroups
 // Register split (setmaxnreg): the launch gives 384 threads x 168 registers (three warps
-// per SM sub-partition). The producer warpgroup drops to 80 and the two softmax warpgroups
-// rise to 208: 2 x 128 x 208 + 128 x 80 = 63 488 <= 64 512 registers of the launch, and
-// (208 + 208 + 80) x 32 = 15 872 <= 16 384 per sub-partition.
-constexpr uint32_t kRegsSoftmax = 208, kRegsProducer = 80;
+// per SM sub-partition). The producer warpgroup drops to 88 and the two softmax warpgroups
+// rise to 208: 2 x 128 x 208 + 128 x 88 = 64 512 <= 64 512 registers of the launch, and
+// (208 + 208 + 88) x 32 = 16 128 <= 16 384 per sub-partition.
+constexpr uint32_t kRegsSoftmax = 208, kRegsProducer = 88;
 constexpr uint32_t kTmemCols = 512;          // S_0/P_0 | S_1/P_1 | O_0 | O_1
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;
@@ -178,7 +178,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         if (isk) {                                       // both query tiles (rows past T read 0)
           tma_prefetch_desc(&tq);
           mbar_expect_tx(&bars->qfull, 2 * kTile);
-  #pragma unroll
+#pragma unroll
           for (int t = 0; t < 2; ++t) {
             tma_load_3d(q_s + t * kTile, &tq, 0, h, t0 + q0 + t * kBM, &bars->qfull);
             tma_load_3d(q_s + t * kTile + kSubQ, &tq, 64, h, t0 + q0 + t * kBM, &bars->qfull);
@@ -200,7 +200,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         }
         int blk[8];
         int nbox = 0;
-  #pragma unroll
+#pragma unroll
         for (int bi = 0; bi < 8; ++bi) {
           blk[bi] = __shfl_sync(0xffffffffu, ids, (jj & 3) * 8 + bi);
           nbox += blk[bi] >= 0 ? 2 : 0;
@@ -213,7 +213,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         if (lane == 0) {
           uint8_t* dst = ring + slot * kTile;
           mbar_expect_tx(&fullb[slot], nbox * 2048);
-  #pragma unroll
+#pragma unroll
           for (int bi = 0; bi < 8; ++bi)
             if (blk[bi] >= 0) {
               const int y = (blk[bi] * H + h) * 16;
@@ -241,7 +241,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
           tc_fence_after();
           const uint64_t qd = desc_add(qdesc, t * kTile);
           const uint64_t kd = desc_add(kdesc, ks * kTile);
-  #pragma unroll
+#pragma unroll
           for (int k = 0; k < 8; ++k) {
             const uint32_t off = (k >> 2) * kSubQ + (k & 3) * 32;
             tc_mma(tmem + t * 128, desc_add(qd, off), desc_add(kd, off), kIdescQK, k > 0);
@@ -291,11 +291,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
               tc_fence_after();
               const uint64_t vd = desc_add(vdesc, vs * kTile);
               const uint32_t pt_col = tmem + t * 128;
-  #pragma unroll
+#pragma unroll
               for (int k = 0; k < 8; ++k)
                 tc_mma_ta(tmem + kColO + t * 128, pt_col + k * 8, desc_add(vd, k * 2048), kIdescPV,
                           (npv[t] > 0 || k > 0) ? 1u : 0u);
             }
+            if (lane == 0 && (t == 1 || !active(1, j)))   // last reader of V_j: free its slot
+              tc_commit(&bars->vempty[vs]);               // as soon as this P V completes
             __syncwarp();
             ++npv[t];
           }
@@ -312,10 +314,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
           }
         }
         if (!ok) break;
-        if (lane == 0) {
-          tc_commit(&bars->vempty[vs]);
-          if (kready) tc_commit(&bars->kempty[ks1]);
-        }
+        if (lane == 0 && kready) tc_commit(&bars->kempty[ks1]);
         __syncwarp();
       }
       if (!ok && lane == 0) {
