@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--workload", default="decode_single_layer",
                     choices=["decode_single_layer", "hybrid_32layer", "prefill_chunked", "long_context_decode",
-                             "sliding_window"],
+                             "sliding_window", "state_precision"],
                     help="decode_single_layer is the headline; the others are timed alone (e.g. for profiling)")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements of the other workloads")
     return ap.parse_args()
@@ -434,8 +434,71 @@ def row_sliding_window(hyb, device, stream, iters, seed=0):
     return res
 
 
+def row_state_precision(hyb, device, stream, iters, seed=0):
+    """Linear decode step with the fp32 state the pages prescribe vs bf16 and fp16 state
+    pools: time per step on 32 requests x 32 heads x 128 x 128, and the output drift of the
+    16-bit states against the fp32 state over 16384 decode steps (4 requests x 4 heads,
+    fp32 q/k/v, zero initial state)."""
+    import torch
+    hbm, _, _ = measured_peaks()
+    B, H, D = 32, 32, 128
+    g = W.rng(seed + 11)
+    mk = lambda: torch.from_numpy(W.rows(g, (B, H, D), D, W.BF16).view(np.int16)).to(device).view(torch.bfloat16)
+    q, k, v = mk(), mk(), mk()
+    out = torch.empty_like(q)
+    slots = torch.arange(B, dtype=torch.int32, device=device)
+    st32 = W.device_state_(torch.empty((B, H, D, D), device=device), 81, np.full(B, 2048), D)
+    st16 = {sd: st32.to(torch.bfloat16 if sd == W.BF16 else torch.float16) for sd in (W.BF16, hyb.HYB_F16)}
+    sh = stream.cuda_stream
+    t = {"fp32": _time(lambda: hyb.check(hyb.hyb_linear_attn_step(out, q, k, v, st32, B, slots, B, H, D, W.BF16, sh)),
+                       stream, iters)}
+    for sd, name in ((W.BF16, "bf16"), (hyb.HYB_F16, "fp16")):
+        t[name] = _time(lambda: hyb.check(hyb.hyb_linear_attn_step_lowp(out, q, k, v, st16[sd], sd, B, slots, B, H, D,
+                                                                        W.BF16, sh)), stream, iters)
+    byt = {"fp32": B * H * D * D * 8, "bf16": B * H * D * D * 4, "fp16": B * H * D * D * 4}
+    del st32, st16
+    # drift: the same fp32 q/k/v stream through the three state types
+    Bd, Hd, T = 4, 4, 16384
+    qs = W.device_rows_(torch.empty((T, Bd, Hd, D), device=device), 82, D)
+    ks = W.device_rows_(torch.empty_like(qs), 83, D)
+    vs = W.device_rows_(torch.empty_like(qs), 84, D)
+    outs = {n: torch.empty_like(qs) for n in ("fp32", "bf16", "fp16")}
+    pools = {"fp32": torch.zeros((Bd, Hd, D, D), device=device),
+             "bf16": torch.zeros((Bd, Hd, D, D), dtype=torch.bfloat16, device=device),
+             "fp16": torch.zeros((Bd, Hd, D, D), dtype=torch.float16, device=device)}
+    sl = torch.arange(Bd, dtype=torch.int32, device=device)
+    with torch.cuda.stream(stream):
+        for i in range(T):
+            hyb.check(hyb.hyb_linear_attn_step(outs["fp32"][i], qs[i], ks[i], vs[i], pools["fp32"], Bd, sl, Bd, Hd, D,
+                                               W.F32, sh))
+            hyb.check(hyb.hyb_linear_attn_step_lowp(outs["bf16"][i], qs[i], ks[i], vs[i], pools["bf16"], W.BF16, Bd, sl,
+                                                    Bd, Hd, D, W.F32, sh))
+            hyb.check(hyb.hyb_linear_attn_step_lowp(outs["fp16"][i], qs[i], ks[i], vs[i], pools["fp16"], hyb.HYB_F16, Bd,
+                                                    sl, Bd, Hd, D, W.F32, sh))
+    stream.synchronize()
+    st_, fl = hyb.hyb_device_status(clear=True)
+    if st_ != 0:
+        raise RuntimeError(f"device-side check flags {fl:#x}")
+    drift = {}
+    for n in ("bf16", "fp16"):
+        drift[n] = {}
+        for tt in (256, 1024, 4096, 16384):
+            ref = outs["fp32"][tt - 64:tt]
+            drift[n][str(tt)] = float((outs[n][tt - 64:tt] - ref).abs().max() / ref.abs().max())
+    del qs, ks, vs, outs, pools
+    torch.cuda.empty_cache()
+    return {"workload": "state_precision: linear step, 32 requests x 32 heads x 128 x 128; drift over 16384 steps",
+            "value": round(B / (t["fp32"] * 1e-3), 1), "unit": "req-tokens/s per layer (fp32 state linear step)",
+            "ms": {n: round(x, 4) for n, x in t.items()},
+            "roofline": {n: _roof("hbm", byt[n] / (t[n] * 1e-3) / 1e9, hbm, "GB/s", f"linear step, {n} state", byt[n])
+                         for n in t},
+            "drift_vs_fp32_state": {"metric": "max |o - o_fp32| / max |o_fp32| over the 64 steps before t",
+                                    "steps": T, **drift}}
+
+
 ROWS = {"long_context_decode": row_long_context, "hybrid_32layer": row_hybrid_32layer,
-        "prefill_chunked": row_prefill, "sliding_window": row_sliding_window}
+        "prefill_chunked": row_prefill, "sliding_window": row_sliding_window,
+        "state_precision": row_state_precision}
 
 
 def bench_ours(args, dist):

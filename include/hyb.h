@@ -61,7 +61,7 @@ typedef enum {
   HYB_ERR_DEVICE_CHECK = 4   /* hyb_device_status() found a device-side check set      */
 } hyb_status_t;
 
-typedef enum { HYB_F32 = 0, HYB_BF16 = 1 } hyb_dtype_t;
+typedef enum { HYB_F32 = 0, HYB_BF16 = 1, HYB_F16 = 2 } hyb_dtype_t;   /* F16: states only */
 typedef enum { HYB_FULL = 0, HYB_LINEAR = 1, HYB_SLIDING = 2 } hyb_layer_type_t;
 typedef enum { HYB_MODE_DECODE = 0, HYB_MODE_PREFILL = 1 } hyb_mode_t;
 
@@ -193,6 +193,25 @@ hyb_status_t hyb_linear_attn_step(void* out, const void* q, const void* k, const
                                   float* state_pool, int32_t num_state_slots,
                                   const int32_t* state_slots, int32_t B, int32_t H, int32_t D,
                                   int32_t dtype, void* stream);
+
+/* -------------------------------------------------------------------------
+ * Linear decode step with a 16-bit state pool (state-precision study). The pages
+ * disagree on the state's precision: [KV §2.3] keeps it in fp32 so that it does not
+ * drift over long sequences, while the vLLM/SGLang page stores it in fp16. This entry
+ * point exists to measure that trade: same contract as hyb_linear_attn_step, but
+ * state_pool holds state_dtype = HYB_BF16 or HYB_F16 elements ([num_slots][H][D][D],
+ * 16-bit each, 8-byte aligned rows), and each element is updated as
+ *     S[i][j] <- round16(fmaf(k[i], v[j], float(S[i][j])))      (round to nearest even)
+ *     out[j]  = sum_i q[i] * float(S[i][j])                      (after the update)
+ * Half the state bytes of the fp32 step, at the cost of rounding every update to 8 (bf16)
+ * or 11 (fp16) significant bits. fp32 (hyb_linear_attn_step) is the path the pages
+ * prescribe; this one is for comparison.
+ * ------------------------------------------------------------------------- */
+hyb_status_t hyb_linear_attn_step_lowp(void* out, const void* q, const void* k, const void* v,
+                                       void* state_pool, int32_t state_dtype,
+                                       int32_t num_state_slots, const int32_t* state_slots,
+                                       int32_t B, int32_t H, int32_t D, int32_t dtype,
+                                       void* stream);
 
 /* -------------------------------------------------------------------------
  * A6. Linear attention chunked prefill [KV §2.3: state zeroed at request start and

@@ -57,6 +57,8 @@ def lib():
             L.oracle_full_prefill.restype = None
             L.oracle_linear_recurrence.argtypes = [p, p, p, p, i32, i32, i32, i32, p, p, p, p, p]
             L.oracle_linear_recurrence.restype = None
+            L.oracle_linear_recurrence_lowp.argtypes = [p, p, p, p, i32, i32, i32, i32, i32, p, p, p, p, p]
+            L.oracle_linear_recurrence_lowp.restype = None
             L.oracle_linear_chunked.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, p, p, p, p, p]
             L.oracle_linear_chunked.restype = None
             L.oracle_cache_bytes.argtypes = [i32, i32, i32, i32, i64, i32, i32, i32, p, p]
@@ -154,6 +156,25 @@ def linear_recurrence(q, k, v, cu_seqlens, state_pool=None, state_slots=None, re
     lib().oracle_linear_recurrence(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), B, H, D, dt,
                                    _ptr(_c(state_pool, np.float32)), _ptr(_c(state_slots, np.int32)),
                                    _ptr(_c(reset, np.uint8)), _ptr(out), _ptr(st))
+    return out, st
+
+
+def linear_recurrence_lowp(q, k, v, cu_seqlens, state_dtype, state_pool=None, state_slots=None,
+                           reset=None):
+    """The recurrence with a 16-bit state (state_dtype 1 = bf16, 2 = fp16): returns
+    (out fp64 [T][H][D], final states as uint16 bit patterns [B][H][D][D])."""
+    q, dt = _elem(q)
+    k, _ = _elem(k)
+    v, _ = _elem(v)
+    T, H, D = q.shape
+    cu = _c(cu_seqlens, np.int32)
+    B = len(cu) - 1
+    out = np.zeros((T, H, D), dtype=np.float64)
+    st = np.zeros((B, H, D, D), dtype=np.uint16)
+    lib().oracle_linear_recurrence_lowp(_ptr(q), _ptr(k), _ptr(v), _ptr(cu), B, H, D, dt,
+                                        int(state_dtype), _ptr(_c(state_pool, np.uint16)),
+                                        _ptr(_c(state_slots, np.int32)), _ptr(_c(reset, np.uint8)),
+                                        _ptr(out), _ptr(st))
     return out, st
 
 

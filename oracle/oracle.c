@@ -227,6 +227,76 @@ void oracle_linear_recurrence(const void *q, const void *k, const void *v, const
     }
 }
 
+/* ------------------------------------------------------ Linear recurrence, 16-bit state
+ * The state-precision comparison: the vLLM/SGLang page keeps the linear state in fp16,
+ * [KV §2.3] keeps it in fp32 so that it does not drift. Here the state is held as 16-bit
+ * values and each token updates every element as
+ *     S_ij <- round16(fmaf(k_i, v_j, S_ij))
+ * (one fp32 fused multiply-add, then one rounding to the 16-bit format, nearest with ties
+ * to even), and the output reads the rounded state: o_j = sum_i q_i S_ij, summed in fp64.
+ * state_dtype 1 = bf16, 2 = fp16. state_pool (may be NULL) and state_out hold raw 16-bit
+ * patterns, [slots][H][D][D] and [B][H][D][D]. */
+static uint16_t f32_to_bf16_rne(float f) {
+  uint32_t x;
+  memcpy(&x, &f, 4);
+  if ((x & 0x7fffffffu) > 0x7f800000u) return (uint16_t)((x >> 16) | 0x40u);   /* NaN */
+  x += 0x7fffu + ((x >> 16) & 1u);
+  return (uint16_t)(x >> 16);
+}
+static float bf16_to_f32(uint16_t u) {
+  uint32_t x = (uint32_t)u << 16;
+  float f;
+  memcpy(&f, &x, 4);
+  return f;
+}
+static uint16_t f32_to_f16_rne(float f) {   /* C's conversion to _Float16 rounds to nearest even */
+  _Float16 h = (_Float16)f;
+  uint16_t u;
+  memcpy(&u, &h, 2);
+  return u;
+}
+static float f16_to_f32(uint16_t u) {
+  _Float16 h;
+  memcpy(&h, &u, 2);
+  return (float)h;
+}
+
+void oracle_linear_recurrence_lowp(const void *q, const void *k, const void *v,
+                                   const int32_t *cu, int B, int H, int D, int dtype,
+                                   int state_dtype, const uint16_t *state_pool,
+                                   const int32_t *state_slots, const uint8_t *reset, double *out,
+                                   uint16_t *state_out) {
+#pragma omp parallel for collapse(2) schedule(dynamic, 1)
+  for (int b = 0; b < B; ++b)
+    for (int h = 0; h < H; ++h) {
+      uint16_t *S = state_out + ((int64_t)b * H + h) * D * D;
+      int zero = (state_pool == NULL) || (reset && reset[b]);
+      for (int64_t e = 0; e < (int64_t)D * D; ++e)
+        S[e] = zero ? 0 : state_pool[((int64_t)state_slots[b] * H + h) * D * D + e];
+      for (int t = cu[b]; t < cu[b + 1]; ++t) {
+        int64_t row = ((int64_t)t * H + h) * D;
+        for (int i = 0; i < D; ++i) {
+          float ki = (float)ld(k, row + i, dtype);
+          for (int j = 0; j < D; ++j) {
+            uint16_t *e = &S[(int64_t)i * D + j];
+            float vj = (float)ld(v, row + j, dtype);
+            float sf = state_dtype == 1 ? bf16_to_f32(*e) : f16_to_f32(*e);
+            float nf = fmaf(ki, vj, sf);
+            *e = state_dtype == 1 ? f32_to_bf16_rne(nf) : f32_to_f16_rne(nf);
+          }
+        }
+        for (int j = 0; j < D; ++j) {
+          double o = 0.0;
+          for (int i = 0; i < D; ++i) {
+            uint16_t e = S[(int64_t)i * D + j];
+            o += ld(q, row + i, dtype) * (double)(state_dtype == 1 ? bf16_to_f32(e) : f16_to_f32(e));
+          }
+          out[row + j] = o;
+        }
+      }
+    }
+}
+
 /* ------------------------------------------------------ A6: Linear chunk form
  * [KV §2.4]: long prompts are prefilled in chunks; a linear layer carries its state
  * from chunk to chunk and chunk boundaries sit at the same positions in every layer.

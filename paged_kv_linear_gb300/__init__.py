@@ -17,7 +17,7 @@ import ctypes as C
 from ._build import LIB, build  # noqa: F401  (build() compiles libhyb.so in-tree)
 
 HYB_OK, HYB_ERR_INVALID_ARG, HYB_ERR_UNSUPPORTED, HYB_ERR_CUDA, HYB_ERR_DEVICE_CHECK = range(5)
-HYB_F32, HYB_BF16 = 0, 1
+HYB_F32, HYB_BF16, HYB_F16 = 0, 1, 2
 HYB_FULL, HYB_LINEAR, HYB_SLIDING = 0, 1, 2
 HYB_MODE_DECODE, HYB_MODE_PREFILL = 0, 1
 HYB_DEVERR_BAD_BLOCK, HYB_DEVERR_BAD_SLOT, HYB_DEVERR_BAD_STATE = 0x1, 0x2, 0x4
@@ -66,6 +66,7 @@ def _load():
         "hyb_paged_attn_decode_noalloc": [p, p, p, p, p, p, i32, i32, p, p],
         "hyb_paged_attn_prefill_causal": [p, p, p, p, p, p, p, i32, i32, i32, p, p],
         "hyb_linear_attn_step": [p, p, p, p, p, i32, p, i32, i32, i32, i32, p],
+        "hyb_linear_attn_step_lowp": [p, p, p, p, p, i32, i32, p, i32, i32, i32, i32, p],
         "hyb_linear_attn_chunked_prefill": [p, p, p, p, p, p, p, i32, p, p, i32, i32, i32, i32,
                                             i32, i32, i32, p],
         "hyb_layer_dispatch": [p, i32, i32, p, p, p, i32, p, sz, p],
@@ -190,6 +191,14 @@ def hyb_linear_attn_step(out, q, k, v, state_pool, num_state_slots, state_slots,
     return _lib.hyb_linear_attn_step(_p(out), _p(q), _p(k), _p(v), _p(state_pool),
                                      num_state_slots, _p(state_slots), B, H, D, dtype,
                                      _s(stream))
+
+
+def hyb_linear_attn_step_lowp(out, q, k, v, state_pool, state_dtype, num_state_slots, state_slots, B, H,
+                              D, dtype, stream=None):
+    """Linear step over a 16-bit (HYB_BF16 / HYB_F16) state pool, for the state-precision
+    comparison; see include/hyb.h."""
+    return _lib.hyb_linear_attn_step_lowp(_p(out), _p(q), _p(k), _p(v), _p(state_pool), state_dtype,
+                                          num_state_slots, _p(state_slots), B, H, D, dtype, _s(stream))
 
 
 def hyb_linear_attn_chunked_prefill(out, q, k, v, cu_seqlens, ctx_lens, state_pool,

@@ -147,16 +147,17 @@ hyb_status_t check_prefill(const void* out, const void* q, const void* kc, const
   return HYB_OK;
 }
 
+// pool_align: 16 for the fp32 pool (float4 rows), 8 for a 16-bit pool (4-element rows)
 hyb_status_t check_linear_common(const void* out, const void* q, const void* k, const void* v,
-                                 const float* pool, int NS, const int32_t* slots, int B, int H,
-                                 int D, int dtype) {
+                                 const void* pool, int NS, const int32_t* slots, int B, int H,
+                                 int D, int dtype, unsigned pool_align = 16) {
   if (B < 0 || H <= 0 || D <= 0 || NS <= 0) return HYB_ERR_INVALID_ARG;
   if (dtype != HYB_BF16 && dtype != HYB_F32) return HYB_ERR_INVALID_ARG;
   if (B > 65535 || H > 65535) return HYB_ERR_UNSUPPORTED;   // grid.z / grid.y limits
   if (!linear_supported(dtype, D)) return HYB_ERR_UNSUPPORTED;
   if (B == 0) return HYB_OK;
   if (!out || !q || !k || !v || !pool || !slots) return HYB_ERR_INVALID_ARG;
-  if (!al16(out) || !al16(q) || !al16(k) || !al16(v) || !al16(pool) || !al(slots, 4))
+  if (!al16(out) || !al16(q) || !al16(k) || !al16(v) || !al(pool, pool_align) || !al(slots, 4))
     return HYB_ERR_INVALID_ARG;
   if ((int64_t)NS * H * D * D > ((int64_t)1 << 40)) return HYB_ERR_UNSUPPORTED;
   return HYB_OK;
@@ -298,6 +299,22 @@ hyb_status_t hyb_linear_attn_step(void* out, const void* q, const void* k, const
   if (!sw) return HYB_ERR_CUDA;
   return cuda_status(launch_linear_step(out, q, k, v, state_pool, num_state_slots, state_slots,
                                         B, H, D, dtype, sw, (cudaStream_t)stream));
+}
+
+hyb_status_t hyb_linear_attn_step_lowp(void* out, const void* q, const void* k, const void* v,
+                                       void* state_pool, int32_t state_dtype,
+                                       int32_t num_state_slots, const int32_t* state_slots,
+                                       int32_t B, int32_t H, int32_t D, int32_t dtype,
+                                       void* stream) {
+  if (state_dtype != HYB_BF16 && state_dtype != HYB_F16) return HYB_ERR_INVALID_ARG;
+  hyb_status_t st = check_linear_common(out, q, k, v, state_pool, num_state_slots, state_slots,
+                                        B, H, D, dtype, 8);
+  if (st != HYB_OK || B == 0) return st;
+  unsigned* sw = status_word();
+  if (!sw) return HYB_ERR_CUDA;
+  return cuda_status(launch_linear_step_lowp(out, q, k, v, state_pool, state_dtype,
+                                             num_state_slots, state_slots, B, H, D, dtype, sw,
+                                             (cudaStream_t)stream));
 }
 
 hyb_status_t hyb_linear_attn_chunked_prefill(void* out, const void* q, const void* k,

@@ -45,6 +45,11 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* kc, const 
                                 cudaStream_t s);
 
 bool linear_supported(int dtype, int D);
+// 16-bit state pool (state_dtype HYB_BF16 or HYB_F16), same shapes as launch_linear_step
+cudaError_t launch_linear_step_lowp(void* out, const void* q, const void* k, const void* v,
+                                    void* pool, int state_dtype, int NS, const int32_t* slots,
+                                    int B, int H, int D, int dtype, unsigned* status,
+                                    cudaStream_t s);
 cudaError_t launch_linear_step(void* out, const void* q, const void* k, const void* v,
                                float* pool, int NS, const int32_t* slots, int B, int H, int D,
                                int dtype, unsigned* status, cudaStream_t s);

@@ -18,6 +18,7 @@
 // states from evicting other data from L2. Column partial sums of q.S reduce in shared
 // memory.
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 
 #include "hyb_internal.cuh"
 
@@ -108,6 +109,85 @@ linear_step_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __rest
   }
 }
 
+// 16-bit state elements for the state-precision comparison: widen exactly, round once (RNE).
+template <typename S>
+struct State16;
+template <>
+struct State16<__nv_bfloat16> {
+  __device__ static float get(uint32_t w, int hi) { return hi ? bf16_hi(w) : bf16_lo(w); }
+  __device__ static uint32_t pack(float lo, float hi) {
+    const __nv_bfloat162 p = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&p);
+  }
+};
+template <>
+struct State16<__half> {
+  __device__ static float get(uint32_t w, int hi) {
+    return __half2float(__ushort_as_half((unsigned short)(hi ? w >> 16 : w & 0xffffu)));
+  }
+  __device__ static uint32_t pack(float lo, float hi) {
+    const __half2 p = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&p);
+  }
+};
+
+// Same decomposition as linear_step_kernel; each thread's 4 state columns are one 8-byte
+// load and store.
+template <typename T, typename S16, int D>
+__global__ void __launch_bounds__(StepShape<D>::THREADS)
+linear_step_lowp_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __restrict__ k,
+                        const T* __restrict__ v, uint16_t* __restrict__ pool, int NS,
+                        const int32_t* __restrict__ slots, int H, unsigned* status) {
+  using Sh = StepShape<D>;
+  using Q = State16<S16>;
+  constexpr int COLS = Sh::COLS, TPR = Sh::TPR, RPP = Sh::RPP, PASSES = Sh::PASSES;
+  __shared__ float red[RPP][COLS];
+
+  const int cb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
+  const int slot = slots[b];
+  if (slot < 0 || slot >= NS) {
+    if (cb == 0 && h == 0 && threadIdx.x == 0) flag(status, HYB_DEVERR_BAD_STATE);
+    return;
+  }
+  const int tc = threadIdx.x % TPR, rg = threadIdx.x / TPR;
+  const int col = cb * COLS + tc * 4;
+  const int64_t rowq = ((int64_t)b * H + h) * D;
+  uint16_t* S = pool + ((int64_t)slot * H + h) * D * D;
+
+  uint2 st[PASSES];
+#pragma unroll
+  for (int p = 0; p < PASSES; ++p)
+    st[p] = __ldcs(reinterpret_cast<const uint2*>(S + (int64_t)(rg + p * RPP) * D + col));
+  const float v0 = ldf(v + rowq + col), v1 = ldf(v + rowq + col + 1);
+  const float v2 = ldf(v + rowq + col + 2), v3 = ldf(v + rowq + col + 3);
+
+  float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+#pragma unroll
+  for (int p = 0; p < PASSES; ++p) {
+    const int i = rg + p * RPP;
+    const float ki = ldf(k + rowq + i), qi = ldf(q + rowq + i);
+    uint2 w;
+    w.x = Q::pack(fmaf(ki, v0, Q::get(st[p].x, 0)), fmaf(ki, v1, Q::get(st[p].x, 1)));
+    w.y = Q::pack(fmaf(ki, v2, Q::get(st[p].y, 0)), fmaf(ki, v3, Q::get(st[p].y, 1)));
+    __stcs(reinterpret_cast<uint2*>(S + (int64_t)i * D + col), w);
+    o0 = fmaf(qi, Q::get(w.x, 0), o0);               // the output reads the rounded state
+    o1 = fmaf(qi, Q::get(w.x, 1), o1);
+    o2 = fmaf(qi, Q::get(w.y, 0), o2);
+    o3 = fmaf(qi, Q::get(w.y, 1), o3);
+  }
+  red[rg][tc * 4 + 0] = o0;
+  red[rg][tc * 4 + 1] = o1;
+  red[rg][tc * 4 + 2] = o2;
+  red[rg][tc * 4 + 3] = o3;
+  __syncthreads();
+  for (int j = threadIdx.x; j < COLS; j += Sh::THREADS) {
+    float o = 0.f;
+#pragma unroll 8
+    for (int g = 0; g < RPP; ++g) o += red[g][j];
+    stf(out + rowq + cb * COLS + j, o);
+  }
+}
+
 // Chunked prefill on the CUDA cores (any D <= 128, bf16 or fp32, any chunk size): the
 // token recurrence, which the chunk form equals exactly in real arithmetic. One CTA per
 // (request, head), state resident in shared memory for the whole call.
@@ -169,6 +249,19 @@ cudaError_t step_typed(void* out, const void* q, const void* k, const void* v, f
   return cudaGetLastError();
 }
 
+template <typename T, typename S16, int D>
+cudaError_t step_lowp_typed(void* out, const void* q, const void* k, const void* v, void* pool,
+                            int NS, const int32_t* slots, int B, int H, unsigned* status,
+                            cudaStream_t s) {
+  using Sh = StepShape<D>;
+  dim3 grid(D / Sh::COLS, H, B);
+  linear_step_lowp_kernel<T, S16, D><<<grid, Sh::THREADS, 0, s>>>(
+      (T*)out, (const T*)q, (const T*)k, (const T*)v, static_cast<uint16_t*>(pool), NS, slots, H,
+      status);
+  count_launch();
+  return cudaGetLastError();
+}
+
 template <typename T, int D>
 cudaError_t prefill_simt_typed(void* out, const void* q, const void* k, const void* v,
                                const int32_t* cu, const int32_t* ctx, float* pool, int NS,
@@ -205,6 +298,26 @@ cudaError_t launch_linear_step(void* out, const void* q, const void* k, const vo
     HYB_STEP(float, 256)
   }
 #undef HYB_STEP
+  return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_linear_step_lowp(void* out, const void* q, const void* k, const void* v,
+                                    void* pool, int state_dtype, int NS, const int32_t* slots,
+                                    int B, int H, int D, int dtype, unsigned* status,
+                                    cudaStream_t s) {
+  if (B == 0) return cudaSuccess;
+#define HYB_LSTEP(T, S16, DD)                                                              \
+  if (D == DD)                                                                             \
+    return step_lowp_typed<T, S16, DD>(out, q, k, v, pool, NS, slots, B, H, status, s);
+#define HYB_LSTEP_D(T, S16)                                                                \
+  HYB_LSTEP(T, S16, 16) HYB_LSTEP(T, S16, 32) HYB_LSTEP(T, S16, 64) HYB_LSTEP(T, S16, 128)  \
+  HYB_LSTEP(T, S16, 256)
+  if (dtype == HYB_BF16 && state_dtype == HYB_BF16) { HYB_LSTEP_D(__nv_bfloat16, __nv_bfloat16) }
+  if (dtype == HYB_BF16 && state_dtype == HYB_F16) { HYB_LSTEP_D(__nv_bfloat16, __half) }
+  if (dtype == HYB_F32 && state_dtype == HYB_BF16) { HYB_LSTEP_D(float, __nv_bfloat16) }
+  if (dtype == HYB_F32 && state_dtype == HYB_F16) { HYB_LSTEP_D(float, __half) }
+#undef HYB_LSTEP_D
+#undef HYB_LSTEP
   return cudaErrorInvalidValue;
 }
 

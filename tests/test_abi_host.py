@@ -134,3 +134,17 @@ def test_dispatch_sliding_layer_arguments(hyb):
     assert hyb.hyb_layer_dispatch([2], 1, 0, [io(8)], meta, dw, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
     # a SLIDING layer shares no cache with a FULL one
     assert hyb.hyb_layer_dispatch([0, 2], 2, 0, [io(0), io(8)], meta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
+
+
+def test_lowp_state_step_arguments(hyb):
+    f = 1 << 20
+    # state dtype must be bf16 or fp16
+    for bad in (hyb.HYB_F32, 7):
+        assert hyb.hyb_linear_attn_step_lowp(f, f, f, f, f, bad, 4, f, 2, 4, 128, hyb.HYB_BF16, 0) == hyb.HYB_ERR_INVALID_ARG
+    # a 16-bit pool needs 8-byte alignment (4-element rows), not 16
+    assert hyb.hyb_linear_attn_step_lowp(f, f, f, f, f + 4, hyb.HYB_F16, 4, f, 2, 4, 128, hyb.HYB_BF16, 0) == hyb.HYB_ERR_INVALID_ARG
+    # no slots, unsupported head dim
+    assert hyb.hyb_linear_attn_step_lowp(f, f, f, f, f, hyb.HYB_BF16, 0, f, 2, 4, 128, hyb.HYB_BF16, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_linear_attn_step_lowp(f, f, f, f, f, hyb.HYB_BF16, 4, f, 2, 4, 48, hyb.HYB_BF16, 0) == hyb.HYB_ERR_UNSUPPORTED
+    # B = 0 is a no-op
+    assert hyb.hyb_linear_attn_step_lowp(None, None, None, None, None, hyb.HYB_BF16, 4, None, 0, 4, 128, hyb.HYB_BF16, 0) == hyb.HYB_OK

@@ -383,3 +383,60 @@ def test_linear_state_size_constant_and_reset_forgets():
     junk = W.synthetic_state(g, 1, H, D, np.array([99]))
     o_a, s_a = oracle.linear_recurrence(q, k, v, [0, 50], junk, [0], np.array([1], np.uint8))
     assert np.array_equal(o_a, oracle.linear_recurrence(q, k, v, [0, 50])[0])
+
+
+# ------------------------------------------- 16-bit linear state (state-precision study)
+def _round16(x32, state_dtype):
+    """Library rounding of fp32 values to bf16 (torch) or fp16 (numpy), as uint16 bits."""
+    if state_dtype == 1:
+        return torch.from_numpy(np.ascontiguousarray(x32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    return np.ascontiguousarray(x32).astype(np.float16).view(np.uint16)
+
+
+def _widen16(u, state_dtype):
+    u = np.ascontiguousarray(u)
+    return W.bf16_to_f32(u).astype(np.float64) if state_dtype == 1 else u.view(np.float16).astype(np.float64)
+
+
+@pytest.mark.parametrize("state_dtype", [1, 2])
+def test_lowp_state_one_token_is_rounded_product(state_dtype):
+    """Zero state + one token: S_ij = round16(k_i v_j), the fp32 product (exact for bf16
+    inputs) rounded by torch (bf16) or numpy (fp16); the output is q . S on that rounded
+    state (numpy, fp64)."""
+    H, D = 2, 16
+    g = W.rng(40)
+    q, k, v = (W.rows(g, (1, H, D), D, W.BF16) for _ in range(3))
+    out, st = oracle.linear_recurrence_lowp(q, k, v, [0, 1], state_dtype)
+    kf, vf = W.bf16_to_f32(k[0]), W.bf16_to_f32(v[0])
+    prod = (kf[:, :, None] * vf[:, None, :]).astype(np.float32)
+    ref_st = _round16(prod, state_dtype)
+    assert np.array_equal(st[0], ref_st)
+    ref_out = np.einsum("hi,hij->hj", W.bf16_to_f32(q[0]).astype(np.float64), _widen16(ref_st, state_dtype))
+    np.testing.assert_allclose(out[0], ref_out, rtol=1e-13, atol=1e-15)
+
+
+@pytest.mark.parametrize("state_dtype", [1, 2])
+def test_lowp_state_exact_when_representable(state_dtype):
+    """Inputs in {0, +-1/4, +-1/2} keep every product and partial state a multiple of 1/16
+    below 1 in magnitude, exact in bf16 and fp16: the 16-bit recurrence then equals the
+    fp64 recurrence exactly (states and outputs), over two requests of three tokens."""
+    H, D, T = 2, 8, 6
+    g = np.random.default_rng(41)
+    mk = lambda: (g.integers(-2, 3, (T, H, D)) / 4.0).astype(np.float32)
+    q, k, v = mk(), mk(), mk()
+    cu = [0, 3, 6]
+    out, st = oracle.linear_recurrence_lowp(q, k, v, cu, state_dtype)
+    ref_out, ref_st = oracle.linear_recurrence(q, k, v, cu)
+    assert np.array_equal(_widen16(st, state_dtype), ref_st)
+    assert np.array_equal(out, ref_out)
+
+
+def test_lowp_bf16_state_drops_updates_below_half_an_ulp():
+    """bf16 keeps 8 significant bits: at S = 256 an update k v = 0.5 is below half the
+    spacing (2) and the state stays 256; fp16 (spacing 0.25 at 256) keeps 256.5."""
+    one = lambda x: np.full((1, 1, 1), x, np.float32)
+    for sd, start, expect in ((1, 0x4380, 256.0), (2, 0x5C00, 256.5)):
+        pool = np.full((1, 1, 1, 1), start, np.uint16)
+        out, st = oracle.linear_recurrence_lowp(one(1.0), one(1.0), one(0.5), [0, 1], sd,
+                                                state_pool=pool, state_slots=[0])
+        assert _widen16(st, sd)[0, 0, 0, 0] == expect and out[0, 0, 0] == expect
