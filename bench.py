@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--workload", default="decode_single_layer",
                     choices=["decode_single_layer", "hybrid_32layer", "prefill_chunked", "long_context_decode",
-                             "sliding_window", "state_precision"],
+                             "sliding_window", "state_precision", "block32"],
                     help="decode_single_layer is the headline; the others are timed alone (e.g. for profiling)")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements of the other workloads")
     return ap.parse_args()
@@ -496,9 +496,67 @@ def row_state_precision(hyb, device, stream, iters, seed=0):
                                     "steps": T, **drift}}
 
 
+def row_block32(hyb, device, stream, iters, seed=0):
+    """32-token blocks (the vLLM/SGLang page's size): paged decode of the 32-request batch
+    (lengths 128..4096) and tensor-core causal prefill of 8 x 8192 prompts, each pool laid
+    out in 32-token blocks."""
+    import torch
+    hbm, tf, _ = measured_peaks()
+    bs = 32
+    g = W.rng(seed + 13)
+    lens = W.lens_uniform(g, 32, 128, 4096)
+    pool = W.block_pool(g, lens, block_size=bs)
+    B, H, D, NB = 32, 32, 128, pool.num_blocks
+    d = hyb.dims(H, D, NB, pool.max_blocks, W.BF16, block_size=bs)
+    kc = W.device_rows_(torch.empty((NB, H, bs, D), dtype=torch.bfloat16, device=device), 91, D)
+    vc = W.device_rows_(torch.empty_like(kc), 92, D)
+    q = torch.from_numpy(W.rows(g, (B, H, D), D, W.BF16).view(np.int16)).to(device).view(torch.bfloat16)
+    out = torch.empty_like(q)
+    bt = torch.from_numpy(pool.block_tables).to(device)
+    ln = torch.from_numpy(lens).to(device)
+    n = int(lens.max())
+    ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, n, d)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=device)
+    sh = stream.cuda_stream
+    t_dec = _time(lambda: hyb.check(hyb.hyb_paged_attn_decode(out, q, kc, vc, bt, ln, B, n, d, ws, ws_n, sh)),
+                  stream, iters)
+    dec_bytes = int(lens.sum()) * H * D * 4 + 2 * B * H * D * 2
+    del kc, vc
+    pb = W.prefill_chunked(seed)
+    Bp = len(pb.q_lens)
+    cu_h = W.cu_from_lens(pb.q_lens)
+    T = int(cu_h[-1])
+    ppool = W.block_pool(W.rng(seed + 14), pb.q_lens, block_size=bs)
+    dp = hyb.dims(H, D, ppool.num_blocks, ppool.max_blocks, W.BF16, block_size=bs)
+    qp = W.device_rows_(torch.empty((T, H, D), dtype=torch.bfloat16, device=device), 93, D)
+    kcp = W.device_rows_(torch.empty((ppool.num_blocks, H, bs, D), dtype=torch.bfloat16, device=device), 94, D)
+    vcp = W.device_rows_(torch.empty_like(kcp), 95, D)
+    outp = torch.empty_like(qp)
+    btp = torch.from_numpy(ppool.block_tables).to(device)
+    cu = torch.from_numpy(cu_h).to(device)
+    L = int(pb.q_lens.max())
+    t_pf = _time(lambda: hyb.check(hyb.hyb_paged_attn_prefill_causal(outp, qp, kcp, vcp, btp, cu, None, Bp, T, L, dp, sh)),
+                 stream, iters)
+    st_, fl = hyb.hyb_device_status(clear=True)
+    if st_ != 0:
+        raise RuntimeError(f"device-side check flags {fl:#x}")
+    nq = pb.q_lens.astype(np.float64)
+    pf_flops = 4.0 * H * D * float((nq * (nq + 1) / 2).sum())
+    del qp, kcp, vcp, outp
+    torch.cuda.empty_cache()
+    return {"workload": "block32: decode 32 requests x U{128..4096} and prefill 8 x 8192, H=32, D=128, 32-token blocks",
+            "value": round(B / (t_dec * 1e-3), 1), "unit": "req-tokens/s per layer (decode, 32-token blocks)",
+            "ms": {"paged_decode": round(t_dec, 4), "prefill_causal": round(t_pf, 4)},
+            "roofline": _roof("hbm", dec_bytes / (t_dec * 1e-3) / 1e9, hbm, "GB/s",
+                              "paged_decode, 32-token blocks (split-K + combine)", dec_bytes),
+            "prefill": _roof("tensor", pf_flops / (t_pf * 1e-3) / 1e12, tf, "TFLOP/s",
+                             "prefill_tc_kernel, 32-token blocks", pf_flops,
+                             peak_source="measured bf16_tflops (burst)")}
+
+
 ROWS = {"long_context_decode": row_long_context, "hybrid_32layer": row_hybrid_32layer,
         "prefill_chunked": row_prefill, "sliding_window": row_sliding_window,
-        "state_precision": row_state_precision}
+        "state_precision": row_state_precision, "block32": row_block32}
 
 
 def bench_ours(args, dist):

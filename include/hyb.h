@@ -30,10 +30,11 @@
  * Layouts
  * -------
  *   packed rows q, k, v, out  [T][H][D], row t = token t (decode: T = B)
- *   paged K cache, V cache    [num_blocks][H][block_size][D]; block_size = 16 [KV §2.1]
- *                             element (blk, h, s, d) at ((blk*H + h)*16 + s)*D + d
+ *   paged K cache, V cache    [num_blocks][H][bs][D], bs = block_size: 16 [KV §2.1], 32 [VL],
+ *                             or any power of two from 16 to 256
+ *                             element (blk, h, s, d) at ((blk*H + h)*bs + s)*D + d
  *   block_tables              int32 [B][max_blocks_per_seq]; logical -> physical block
- *   slot_mapping              int64 [T]; slot = blk*16 + offset; -1 = skip the token
+ *   slot_mapping              int64 [T]; slot = blk*bs + offset; -1 = skip the token
  *   state pool                fp32 [num_slots][H][D][D]; S[i][j], i = key dim, j = value dim
  *   state_slots               int32 [B]; request b uses state pool slot state_slots[b]
  *   cu_q_lens / cu_seqlens    int32 [B+1]; request b owns packed rows [cu[b], cu[b+1])
@@ -77,7 +78,7 @@ typedef enum { HYB_MODE_DECODE = 0, HYB_MODE_PREFILL = 1 } hyb_mode_t;
 typedef struct {
   int32_t num_heads;           /* H (query heads = KV heads; the pages use one H)      */
   int32_t head_dim;            /* D                                                     */
-  int32_t block_size;          /* must be 16 [KV §2.1]                                  */
+  int32_t block_size;          /* bs: 16 [KV §2.1], 32 [VL]; a power of two, 16..256   */
   int32_t num_blocks;          /* physical blocks in each of the K and V pools          */
   int32_t max_blocks_per_seq;  /* columns of block_tables                               */
   int32_t dtype;               /* hyb_dtype_t of q/k/v/out and of the caches            */
@@ -93,11 +94,11 @@ typedef struct {
  * the call are never read: an allocator may release those blocks and store -1 there. */
 
 /* -------------------------------------------------------------------------
- * A1. Slot mapping [KV §2.1: 16-token blocks reached through a page table].
+ * A1. Slot mapping [KV §2.1: fixed-size token blocks reached through a page table].
  * For packed row t of request b (cu_q_lens[b] <= t < cu_q_lens[b+1]) at absolute
  * position p = ctx_lens[b] + (t - cu_q_lens[b]):
- *     slot_mapping[t] = block_tables[b][p / 16] * 16 + p % 16
- * A negative block id yields slot -1. p / 16 >= max_blocks_per_seq or a block id
+ *     slot_mapping[t] = block_tables[b][p / bs] * bs + p % bs
+ * A negative block id yields slot -1. p / bs >= max_blocks_per_seq or a block id
  * >= num_blocks sets HYB_DEVERR_BAD_BLOCK and yields -1. ctx_lens may be NULL (all 0).
  * Decode is the case cu_q_lens = {0,1,...,B}, ctx_lens = seq_lens - 1.
  * ------------------------------------------------------------------------- */
@@ -108,7 +109,7 @@ hyb_status_t hyb_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables
 /* -------------------------------------------------------------------------
  * A2. KV append [KV §2.1: every token's key and value vectors are kept].
  * For each t < T with slot s = slot_mapping[t] >= 0 and every head h, copies
- * k[t][h][:] to k_cache[s/16][h][s%16][:] and v likewise (bitwise). s >= num_blocks*16
+ * k[t][h][:] to k_cache[s/bs][h][s%bs][:] and v likewise (bitwise). s >= num_blocks*bs
  * sets HYB_DEVERR_BAD_SLOT and is skipped. T = 0 is a no-op.
  * ------------------------------------------------------------------------- */
 hyb_status_t hyb_paged_kv_append(const void* k, const void* v, const int64_t* slot_mapping,
@@ -121,7 +122,7 @@ hyb_status_t hyb_paged_kv_append(const void* k, const void* v, const int64_t* sl
  * For each request b and head h, with n = seq_lens[b] (which already counts the
  * token appended this step):
  *     out[b][h][:] = sum_{p<n} softmax_p(scale * q[b][h].K_p) V_p
- * where K_p, V_p are read at block_tables[b][p/16], offset p%16. n = 0 gives zeros.
+ * where K_p, V_p are read at block_tables[b][p/bs], offset p%bs. n = 0 gives zeros.
  * d->window = W > 0 restricts p to n - W <= p < n (see "Sliding window" above).
  * max_seq_len (host) must be >= every seq_lens[b]; a longer sequence sets
  * HYB_DEVERR_BAD_LENGTH and is truncated. The kernel splits each sequence into

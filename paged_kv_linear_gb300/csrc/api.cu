@@ -80,11 +80,12 @@ hyb_status_t check_dims(const hyb_attn_dims_t* d) {
   if (!d) return HYB_ERR_INVALID_ARG;
   if (d->num_heads <= 0 || d->head_dim <= 0 || d->num_blocks <= 0 || d->max_blocks_per_seq <= 0)
     return HYB_ERR_INVALID_ARG;
-  if (d->block_size != kBlockSize) return HYB_ERR_UNSUPPORTED;
+  if (!block_size_ok(d->block_size)) return HYB_ERR_UNSUPPORTED;
   if (d->dtype != HYB_BF16 && d->dtype != HYB_F32) return HYB_ERR_INVALID_ARG;
   if ((d->head_dim * esize_of(d->dtype)) % 16 != 0) return HYB_ERR_UNSUPPORTED;
   if (!std::isfinite(d->scale) || d->window < 0) return HYB_ERR_INVALID_ARG;
-  if ((int64_t)d->num_blocks * kBlockSize > INT32_MAX) return HYB_ERR_UNSUPPORTED;
+  // slots and the pool rows the tensor maps address (blocks x heads x tokens) are int32
+  if ((int64_t)d->num_blocks * d->num_heads * d->block_size > INT32_MAX) return HYB_ERR_UNSUPPORTED;
   return HYB_OK;
 }
 
@@ -116,7 +117,7 @@ hyb_status_t check_decode(const void* out, const void* q, const void* kc, const 
   if (st != HYB_OK) return st;
   if (B < 0 || max_seq_len < 0) return HYB_ERR_INVALID_ARG;
   if (d->num_heads > 65535) return HYB_ERR_UNSUPPORTED;
-  if ((int64_t)max_seq_len > (int64_t)d->max_blocks_per_seq * kBlockSize) return HYB_ERR_INVALID_ARG;
+  if ((int64_t)max_seq_len > (int64_t)d->max_blocks_per_seq * d->block_size) return HYB_ERR_INVALID_ARG;
   if (max_seq_len > (1 << 24)) return HYB_ERR_UNSUPPORTED;   // grid.z = splits <= 65535
   if (!decode_supported(d->dtype, d->head_dim)) return HYB_ERR_UNSUPPORTED;
   if (B == 0) return HYB_OK;
@@ -135,7 +136,7 @@ hyb_status_t check_prefill(const void* out, const void* q, const void* kc, const
   if (st != HYB_OK) return st;
   if (B < 0 || T < 0 || max_q_len < 0 || max_q_len > T) return HYB_ERR_INVALID_ARG;
   if (d->num_heads > 65535 || B > 65535) return HYB_ERR_UNSUPPORTED;
-  if ((int64_t)max_q_len > (int64_t)d->max_blocks_per_seq * kBlockSize) return HYB_ERR_INVALID_ARG;
+  if ((int64_t)max_q_len > (int64_t)d->max_blocks_per_seq * d->block_size) return HYB_ERR_INVALID_ARG;
   if (!prefill_tc_supported(d->dtype, d->head_dim) && !decode_supported(d->dtype, d->head_dim))
     return HYB_ERR_UNSUPPORTED;
   if (B == 0 || max_q_len == 0) return HYB_OK;
@@ -185,8 +186,8 @@ hyb_status_t run_decode(void* out, const void* q, const void* kc, const void* vc
   const DecodePlan p = plan_decode(B, d->num_heads, d->head_dim, max_seq_len, d->window);
   return cuda_status(launch_paged_decode(out, q, kc, vc, bt, seq_lens, nullptr, nullptr, B, 0,
                                          d->num_heads, d->head_dim, d->dtype, d->num_blocks,
-                                         d->max_blocks_per_seq, max_seq_len, d->scale,
-                                         d->window, p, ws, status, s));
+                                         d->max_blocks_per_seq, d->block_size, max_seq_len,
+                                         d->scale, d->window, p, ws, status, s));
 }
 
 hyb_status_t run_prefill(void* out, const void* q, const void* kc, const void* vc,
@@ -197,12 +198,12 @@ hyb_status_t run_prefill(void* out, const void* q, const void* kc, const void* v
   if (prefill_tc_supported(d->dtype, d->head_dim))
     return cuda_status(launch_prefill_tc(out, q, kc, vc, bt, cu, ctx, B, T, max_q_len,
                                          d->num_heads, d->num_blocks, d->max_blocks_per_seq,
-                                         d->scale, d->window, status, s));
+                                         d->block_size, d->scale, d->window, status, s));
   const DecodePlan none{1 << 30, 1, 0};
   return cuda_status(launch_paged_decode(out, q, kc, vc, bt, nullptr, cu, ctx, B, max_q_len,
                                          d->num_heads, d->head_dim, d->dtype, d->num_blocks,
-                                         d->max_blocks_per_seq,
-                                         d->max_blocks_per_seq * kBlockSize, d->scale,
+                                         d->max_blocks_per_seq, d->block_size,
+                                         d->max_blocks_per_seq * d->block_size, d->scale,
                                          d->window, none, nullptr, status, s));
 }
 
@@ -237,7 +238,7 @@ hyb_status_t hyb_slot_mapping(int64_t* slot_mapping, const int32_t* block_tables
   unsigned* sw = status_word();
   if (!sw) return HYB_ERR_CUDA;
   return cuda_status(launch_slot_mapping(slot_mapping, block_tables, cu_q_lens, ctx_lens, B, T,
-                                         d->max_blocks_per_seq, d->num_blocks, sw,
+                                         d->max_blocks_per_seq, d->num_blocks, d->block_size, sw,
                                          (cudaStream_t)stream));
 }
 
@@ -249,8 +250,8 @@ hyb_status_t hyb_paged_kv_append(const void* k, const void* v, const int64_t* sl
   unsigned* sw = status_word();
   if (!sw) return HYB_ERR_CUDA;
   return cuda_status(launch_kv_append(k, v, slot_mapping, T, d->num_heads, d->head_dim,
-                                      esize_of(d->dtype), d->num_blocks, k_cache, v_cache, sw,
-                                      (cudaStream_t)stream));
+                                      esize_of(d->dtype), d->num_blocks, d->block_size, k_cache,
+                                      v_cache, sw, (cudaStream_t)stream));
 }
 
 size_t hyb_paged_attn_decode_workspace_size(int32_t B, int32_t max_seq_len,
@@ -391,7 +392,8 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
       hyb_attn_dims_t dl = *d;
       dl.window = io.window;
       st = cuda_status(launch_kv_append(io.k, io.v, meta->slot_mapping, T, H, D, esize_of(dt),
-                                        d->num_blocks, io.k_cache, io.v_cache, sw, s));
+                                        d->num_blocks, d->block_size, io.k_cache, io.v_cache, sw,
+                                        s));
       if (st != HYB_OK) return st;
       st = mode == HYB_MODE_DECODE
                ? run_decode(io.out, io.q, io.k_cache, io.v_cache, meta->block_tables,

@@ -65,11 +65,12 @@ struct Elt<float> {
   __device__ static void store(float* p, float x) { *p = x; }
 };
 
-// Length handled for a row after host/device bound checks (identical in both kernels).
-__device__ __forceinline__ int clamp_len(int n, int max_len, int MB) {
+// Length handled for a row after host/device bound checks (identical in both kernels);
+// MBt = block-table capacity in 16-token sub-tiles.
+__device__ __forceinline__ int clamp_len(int n, int max_len, int MBt) {
   n = n < 0 ? 0 : n;
   n = n > max_len ? max_len : n;
-  const int cap = MB * kBlockSize;
+  const int cap = MBt * kBlockSize;
   return n > cap ? cap : n;
 }
 
@@ -103,7 +104,7 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
                     const T* __restrict__ vc, const int32_t* __restrict__ bt,
                     const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu,
                     const int32_t* __restrict__ ctx, int max_q, int H, int NB, int MB,
-                    int max_len, float scale_log2, int window, int max_splits,
+                    int rsh, int max_len, float scale_log2, int window, int max_splits,
                     float* __restrict__ ws_acc, float2* __restrict__ ws_ml, unsigned* status) {
   using E = Elt<T>;
   using S = DecodeShape<T, D>;
@@ -121,7 +122,7 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
     b = r = blockIdx.x;
     n_raw = seq_lens[r];
   }
-  const int n = clamp_len(n_raw, max_len, MB);
+  const int n = clamp_len(n_raw, max_len, MB << rsh);
   if (n != (n_raw < 0 ? 0 : n_raw) && split == 0 && threadIdx.x == 0)
     flag(status, n_raw > max_len ? HYB_DEVERR_BAD_LENGTH : HYB_DEVERR_BAD_BLOCK);
   const int lo = WINDOW ? window_lo(n, window) : 0;   // keys [lo, n)
@@ -149,9 +150,11 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
 
   const int first = blk_begin + warp;   // this warp's logical blocks: first + i*kNW
   const int ntiles = first < blk_end ? (blk_end - first + kNW - 1) / kNW : 0;
+  // 16-token sub-tile s lives in block btrow[s >> rsh], rows (s & sub_mask) * 16 onwards
   const int32_t* btrow = bt + (int64_t)b * MB;
-  const int64_t head_off = (int64_t)h * kBlockSize * D;
-  const int64_t blk_stride = (int64_t)H * kBlockSize * D;
+  const int sub_mask = (1 << rsh) - 1;
+  const int64_t head_off = (int64_t)h * (kBlockSize << rsh) * D;
+  const int64_t blk_stride = (int64_t)H * (kBlockSize << rsh) * D;
 
   if (lane == 0) {
 #pragma unroll
@@ -161,13 +164,15 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
   __syncwarp();
 
   auto issue = [&](int i) {              // lane 0 only
-    const int pb = btrow[first + i * kNW];
+    const int sub = first + i * kNW;
+    const int pb = btrow[sub >> rsh];
     if (pb < 0 || pb >= NB) return;      // the consumer flags and skips it
     const int st = i % kNST;
     uint8_t* dst = ring + st * 2 * TILE;
+    const int64_t off = pb * blk_stride + head_off + (int64_t)(sub & sub_mask) * kBlockSize * D;
     mbar_expect_tx(&bars[st], 2 * TILE);
-    bulk_g2s(dst, kc + pb * blk_stride + head_off, TILE, &bars[st]);
-    bulk_g2s(dst + TILE, vc + pb * blk_stride + head_off, TILE, &bars[st]);
+    bulk_g2s(dst, kc + off, TILE, &bars[st]);
+    bulk_g2s(dst + TILE, vc + off, TILE, &bars[st]);
   };
   if (lane == 0)
     for (int i = 0; i < min(kNST, ntiles); ++i) issue(i);
@@ -180,7 +185,7 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
 
   for (int i = 0; i < ntiles; ++i) {
     const int st = i % kNST;
-    const int pb = btrow[first + i * kNW];
+    const int pb = btrow[(first + i * kNW) >> rsh];
     if (pb < 0 || pb >= NB) {
       if (lane == 0) flag(status, HYB_DEVERR_BAD_BLOCK);
     } else {
@@ -240,7 +245,7 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
     if (lane == 0) {
       flag(status, HYB_DEVERR_TIMEOUT);
       for (int j = failed_at; j < min(failed_at + kNST, ntiles); ++j) {
-        const int pb = btrow[first + j * kNW];
+        const int pb = btrow[(first + j * kNW) >> rsh];
         if (pb >= 0 && pb < NB) {
           const int st = j % kNST;
           mbar_wait(&bars[st], (phase >> st) & 1u, 100000000ull);
@@ -294,11 +299,11 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
 // Merges the splits of one (request, head): out = sum_s 2^(m_s-M) acc_s / sum_s 2^(m_s-M) l_s.
 template <typename T, int D>
 __global__ void __launch_bounds__(128)
-decode_combine_kernel(T* __restrict__ out, const int32_t* __restrict__ seq_lens, int H, int MB,
+decode_combine_kernel(T* __restrict__ out, const int32_t* __restrict__ seq_lens, int H, int MBt,
                       int max_len, int window, int max_splits, const float* __restrict__ ws_acc,
                       const float2* __restrict__ ws_ml) {
   const int r = blockIdx.x, h = blockIdx.y;
-  const int n = clamp_len(seq_lens[r], max_len, MB);
+  const int n = clamp_len(seq_lens[r], max_len, MBt);
   const int nsplit = decode_splits(n, window);
   if (nsplit <= 1) return;
   const int64_t rh = (int64_t)r * H + h;
@@ -323,13 +328,14 @@ template <typename T, int D>
 cudaError_t launch_typed(void* out, const void* q, const void* kc, const void* vc,
                          const int32_t* bt, const int32_t* seq_lens, const int32_t* cu,
                          const int32_t* ctx, int R, int max_q, int H, int NB, int MB,
-                         int max_len, float scale, int window, const DecodePlan& plan, void* ws,
-                         unsigned* status, cudaStream_t s) {
+                         int bs, int max_len, float scale, int window, const DecodePlan& plan,
+                         void* ws, unsigned* status, cudaStream_t s) {
   using Sh = DecodeShape<T, D>;
   const bool prefill = cu != nullptr, win = window > 0;
   using K = void (*)(T*, const T*, const T*, const T*, const int32_t*, const int32_t*,
-                     const int32_t*, const int32_t*, int, int, int, int, int, float, int, int,
-                     float*, float2*, unsigned*);
+                     const int32_t*, const int32_t*, int, int, int, int, int, int, float, int,
+                     int, float*, float2*, unsigned*);
+  const int rsh = log2_int(bs / kBlockSize);
   const K kern = prefill ? (win ? paged_decode_kernel<T, D, true, true>
                                 : paged_decode_kernel<T, D, true, false>)
                          : (win ? paged_decode_kernel<T, D, false, true>
@@ -343,12 +349,12 @@ cudaError_t launch_typed(void* out, const void* q, const void* kc, const void* v
   dim3 grid(prefill ? R * max_q : R, H, max_splits);
   const float scale_log2 = scale * 1.4426950408889634f;
   kern<<<grid, kNW * 32, Sh::SMEM, s>>>((T*)out, (const T*)q, (const T*)kc, (const T*)vc, bt,
-                                        seq_lens, cu, ctx, max_q, H, NB, MB, max_len, scale_log2,
+                                        seq_lens, cu, ctx, max_q, H, NB, MB, rsh, max_len, scale_log2,
                                         window, max_splits, ws_acc, ws_ml, status);
   count_launch();
   e = cudaGetLastError();
   if (e != cudaSuccess || max_splits == 1) return e;
-  decode_combine_kernel<T, D><<<dim3(R, H), 128, 0, s>>>((T*)out, seq_lens, H, MB, max_len,
+  decode_combine_kernel<T, D><<<dim3(R, H), 128, 0, s>>>((T*)out, seq_lens, H, MB << rsh, max_len,
                                                           window, max_splits, ws_acc, ws_ml);
   count_launch();
   return cudaGetLastError();
@@ -376,13 +382,13 @@ bool decode_supported(int dtype, int D) {
 cudaError_t launch_paged_decode(void* out, const void* q, const void* kc, const void* vc,
                                 const int32_t* bt, const int32_t* seq_lens, const int32_t* cu,
                                 const int32_t* ctx, int R, int max_q, int H, int D, int dtype,
-                                int NB, int MB, int max_len, float scale, int window,
+                                int NB, int MB, int bs, int max_len, float scale, int window,
                                 const DecodePlan& plan, void* ws, unsigned* status,
                                 cudaStream_t s) {
   if (R == 0 || (cu && max_q == 0)) return cudaSuccess;
 #define HYB_DEC(T, DD)                                                                       \
   if (D == DD)                                                                               \
-    return launch_typed<T, DD>(out, q, kc, vc, bt, seq_lens, cu, ctx, R, max_q, H, NB, MB,    \
+    return launch_typed<T, DD>(out, q, kc, vc, bt, seq_lens, cu, ctx, R, max_q, H, NB, MB, bs, \
                                max_len, scale, window, plan, ws, status, s);
   if (dtype == HYB_BF16) {
     HYB_DEC(__nv_bfloat16, 16)

@@ -64,11 +64,11 @@ hyb_status_t hyb_paged_attn_decode_noalloc(void* out, const void* q, const void*
     return HYB_ERR_INVALID_ARG;
   if (d->dtype != HYB_BF16 && d->dtype != HYB_F32) return HYB_ERR_INVALID_ARG;
   if (d->window < 0 || !std::isfinite(d->scale)) return HYB_ERR_INVALID_ARG;
-  if (d->block_size != hyb::kBlockSize || d->num_heads > 65535 || max_seq_len > (1 << 24) ||
+  if (!hyb::block_size_ok(d->block_size) || d->num_heads > 65535 || max_seq_len > (1 << 24) ||
       !hyb::decode_supported(d->dtype, d->head_dim) ||
-      (int64_t)d->num_blocks * hyb::kBlockSize > INT32_MAX)
+      (int64_t)d->num_blocks * d->num_heads * d->block_size > INT32_MAX)
     return HYB_ERR_UNSUPPORTED;
-  if ((int64_t)max_seq_len > (int64_t)d->max_blocks_per_seq * hyb::kBlockSize)
+  if ((int64_t)max_seq_len > (int64_t)d->max_blocks_per_seq * d->block_size)
     return HYB_ERR_INVALID_ARG;
   if (B == 0) return HYB_OK;
   if (!out || !q || !k_cache || !v_cache || !block_tables || !seq_lens) return HYB_ERR_INVALID_ARG;
@@ -83,8 +83,8 @@ hyb_status_t hyb_paged_attn_decode_noalloc(void* out, const void* q, const void*
   if (!scratch || !status) return HYB_ERR_CUDA;
   const cudaError_t e = hyb::launch_paged_decode(
       out, q, k_cache, v_cache, block_tables, seq_lens, nullptr, nullptr, B, 0, d->num_heads,
-      d->head_dim, d->dtype, d->num_blocks, d->max_blocks_per_seq, max_seq_len, d->scale,
-      d->window, plan, scratch, status, (cudaStream_t)stream);
+      d->head_dim, d->dtype, d->num_blocks, d->max_blocks_per_seq, d->block_size, max_seq_len,
+      d->scale, d->window, plan, scratch, status, (cudaStream_t)stream);
   return e == cudaSuccess ? HYB_OK : HYB_ERR_CUDA;
 }
 

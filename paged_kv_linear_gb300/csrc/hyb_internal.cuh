@@ -9,7 +9,11 @@
 
 namespace hyb {
 
-constexpr int kBlockSize = 16;   // tokens per KV block [KV §2.1]
+// Kernels walk the cache in 16-token sub-tiles (the block size of [KV §2.1]); a block of
+// bs tokens (a power of two from 16 to 256) is bs / 16 consecutive sub-tiles.
+constexpr int kBlockSize = 16;
+constexpr bool block_size_ok(int bs) { return bs >= 16 && bs <= 256 && (bs & (bs - 1)) == 0; }
+inline int log2_int(int x) { int r = 0; while ((1 << r) < x) ++r; return r; }
 
 // ------------------------------------------------------------------ host side
 void count_launch();                       // per-thread launch counter (hyb_launch_count)
@@ -19,11 +23,11 @@ cudaError_t set_smem(const void* fn, int bytes);   // opt-in dynamic shared memo
 
 // kernel launchers (each returns the launch's cudaError_t)
 cudaError_t launch_slot_mapping(int64_t* slot, const int32_t* bt, const int32_t* cu,
-                                const int32_t* ctx, int B, int T, int MB, int NB,
+                                const int32_t* ctx, int B, int T, int MB, int NB, int bs,
                                 unsigned* status, cudaStream_t s);
 cudaError_t launch_kv_append(const void* k, const void* v, const int64_t* slot, int T, int H,
-                             int D, int esize, int NB, void* kc, void* vc, unsigned* status,
-                             cudaStream_t s);
+                             int D, int esize, int NB, int bs, void* kc, void* vc,
+                             unsigned* status, cudaStream_t s);
 
 struct DecodePlan {
   int blocks_per_split;   // KV blocks handled by one CTA
@@ -40,7 +44,7 @@ bool decode_supported(int dtype, int D);
 cudaError_t launch_paged_decode(void* out, const void* q, const void* kc, const void* vc,
                                 const int32_t* bt, const int32_t* seq_lens, const int32_t* cu,
                                 const int32_t* ctx, int R, int max_q, int H, int D, int dtype,
-                                int NB, int MB, int max_len, float scale, int window,
+                                int NB, int MB, int bs, int max_len, float scale, int window,
                                 const DecodePlan& plan, void* ws, unsigned* status,
                                 cudaStream_t s);
 
@@ -67,7 +71,7 @@ cudaError_t launch_linear_prefill_tc(void* out, const void* q, const void* k, co
 bool prefill_tc_supported(int dtype, int D);
 cudaError_t launch_prefill_tc(void* out, const void* q, const void* kc, const void* vc,
                               const int32_t* bt, const int32_t* cu, const int32_t* ctx, int B,
-                              int T, int max_q_len, int H, int NB, int MB, float scale,
+                              int T, int max_q_len, int H, int NB, int MB, int bs, float scale,
                               int window, unsigned* status, cudaStream_t s);
 
 }  // namespace hyb

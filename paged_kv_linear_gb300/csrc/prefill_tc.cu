@@ -10,8 +10,8 @@
 // softmax warpgroups, one per query tile, one thread per query row (the row's max and sum
 // stay in that thread). K and V come straight from the paged pool: each 128-key tile is
 // eight 16-token blocks, each fetched with two TMA boxes (16 rows x 64 columns, SW128) at
-// the row the block table names; each TMA warp reads the block ids 32 at a time and shares
-// them with shuffles. Per key tile j and query tile t:
+// the row the block table names (a block of bs tokens is bs / 16 such 16-row pieces); each
+// TMA warp reads the block ids 32 pieces at a time and shares the rows with shuffles. Per key tile j and query tile t:
 //   S_t = Q_t K_j^T   128 x 128 x 128  A = Q_t (K-major), B = K_j (K-major)  -> TMEM
 //   O_t += P_t V_j    128 x 128 x 128  A = P_t (TMEM),    B = V_j (MN-major) -> TMEM
 // TMEM holds S_0 | S_1 | O_0 | O_1 (4 x 128 columns). The softmax threads read S_t, write
@@ -101,8 +101,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ out,
                   const int32_t* __restrict__ bt, const int32_t* __restrict__ cu,
-                  const int32_t* __restrict__ ctx, int H, int NB, int MB, float scale_log2,
-                  int window, unsigned* status) {
+                  const int32_t* __restrict__ ctx, int H, int NB, int MB, int rsh,
+                  float scale_log2, int window, unsigned* status) {
   const int pt = gridDim.x - 1 - blockIdx.x;           // heavy pairs first
   const int h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -127,7 +127,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
   const int kv_end = two ? tr[1].kv_end : tr[0].kv_end;
   const int blk_lo = (window > 0 ? max(0, c0 + q0 - window + 1) : 0) / 16;
   const int32_t* btrow = bt + (int64_t)b * MB;
-  if ((kv_end + 15) / 16 > MB) {
+  if ((kv_end + 15) / 16 > (MB << rsh)) {             // in 16-token pieces
     if (tid == 0) flag(status, HYB_DEVERR_BAD_BLOCK);
     return;
   }
@@ -185,17 +185,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
           }
         }
       }
-      int ids = -1;                                      // block ids of 4 tiles, one per lane
+      int ids = -1;                                      // pool rows of 4 tiles' pieces, one per lane
       for (int jj = 0; jj < nloc; ++jj) {                // local tile index, key tile jA + jj
         if ((jj & 3) == 0) {
-          const int lb = (jA + jj) * 8 + lane;
+          const int lb = (jA + jj) * 8 + lane;             // 16-token piece of the sequence
           ids = -1;
           if (lb >= blk_lo && lb * 16 < kv_end) {
-            ids = btrow[lb];
-            if (ids < 0 || ids >= NB) {
-              flag(status, HYB_DEVERR_BAD_BLOCK);
-              ids = -1;
-            }
+            const int pb = btrow[lb >> rsh];
+            if (pb < 0 || pb >= NB) flag(status, HYB_DEVERR_BAD_BLOCK);
+            else ids = ((pb * H + h) << (4 + rsh)) + ((lb & ((1 << rsh) - 1)) << 4);
           }
         }
         int blk[8];
@@ -216,7 +214,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
 #pragma unroll
           for (int bi = 0; bi < 8; ++bi)
             if (blk[bi] >= 0) {
-              const int y = (blk[bi] * H + h) * 16;
+              const int y = blk[bi];
               tma_load_2d(dst + bi * 2048, map, 0, y, &fullb[slot]);
               tma_load_2d(dst + kSubQ + bi * 2048, map, 64, y, &fullb[slot]);
             }
@@ -451,14 +449,14 @@ bool prefill_tc_supported(int dtype, int D) { return dtype == HYB_BF16 && D == k
 
 cudaError_t launch_prefill_tc(void* out, const void* q, const void* kc, const void* vc,
                               const int32_t* bt, const int32_t* cu, const int32_t* ctx, int B,
-                              int T, int max_q_len, int H, int NB, int MB, float scale,
+                              int T, int max_q_len, int H, int NB, int MB, int bs, float scale,
                               int window, unsigned* status, cudaStream_t s) {
   if (B == 0 || max_q_len == 0 || T <= 0) return cudaSuccess;
   CUtensorMap mq, mk, mv;
   const uint64_t qdims[3] = {(uint64_t)kD, (uint64_t)H, (uint64_t)T};
   const uint64_t qstr[2] = {(uint64_t)kD * 2, (uint64_t)H * kD * 2};
   const uint32_t qbox[3] = {64, 1, (uint32_t)kBM};
-  const uint64_t cdims[2] = {(uint64_t)kD, (uint64_t)NB * H * 16};
+  const uint64_t cdims[2] = {(uint64_t)kD, (uint64_t)NB * H * bs};
   const uint64_t cstr[1] = {(uint64_t)kD * 2};
   const uint32_t cbox[2] = {64, 16};
   if (!encode_tmap_bf16(&mq, q, 3, qdims, qstr, qbox) ||
@@ -469,8 +467,8 @@ cudaError_t launch_prefill_tc(void* out, const void* q, const void* kc, const vo
   if (e != cudaSuccess) return e;
   dim3 grid((max_q_len + 2 * kBM - 1) / (2 * kBM), H, B);
   prefill_tc_kernel<<<grid, kThreads, kSmem, s>>>(mq, mk, mv, static_cast<__nv_bfloat16*>(out), bt,
-                                                  cu, ctx, H, NB, MB, scale * 1.4426950408889634f,
-                                                  window, status);
+                                                  cu, ctx, H, NB, MB, log2_int(bs / 16),
+                                                  scale * 1.4426950408889634f, window, status);
   count_launch();
   return cudaGetLastError();
 }

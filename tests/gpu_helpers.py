@@ -7,9 +7,12 @@ relative"); fp32
 linear states pass when, for every (request, head) matrix, max|gpu - ref| <=
 1e-3 * max|ref|. Integer and byte results (slots, cache images) must be identical.
 """
+import math
+
 import numpy as np
 import torch
 
+import oracle
 import workloads as W
 
 OUT_ATOL = 2e-2
@@ -80,8 +83,92 @@ def assert_states_close(gpu, ref, what="state"):
     return float((err / np.maximum(np.abs(r).max(axis=1), 1e-30)).max())
 
 
-def poisoned_pool(num_blocks, H, D, dtype_code):
-    shape = (num_blocks, H, W.BLOCK_SIZE, D)
+def poisoned_pool(num_blocks, H, D, dtype_code, block_size=W.BLOCK_SIZE):
+    shape = (num_blocks, H, block_size, D)
     if dtype_code == W.BF16:
         return np.full(shape, 0x7FC0, np.uint16)
     return np.full(shape, np.nan, np.float32)
+
+
+# ------------------------------------------------- paged requests with a cached prefix
+def released(block_tables, first_pos, window, block_size=W.BLOCK_SIZE):
+    """Copy of the table with -1 for every logical block that ends before the window of the
+    request's earliest query (position first_pos[b])."""
+    bt = block_tables.copy()
+    for b, p in enumerate(first_pos):
+        keep_from = max(0, int(p) - window + 1) // block_size
+        bt[b, :keep_from] = -1
+    return bt
+
+
+class PagedCase:
+    """Requests with a cached prefix (ctx rows, written by the oracle into a poisoned pool)
+    and this call's q/k/v rows (qlens per request)."""
+
+    def __init__(self, seed, qlens, ctx, H, D, dtype, block_size=W.BLOCK_SIZE):
+        g = W.rng(seed)
+        self.qlens = np.asarray(qlens, np.int32)
+        self.ctx = np.asarray(ctx, np.int32)
+        self.B, self.H, self.D, self.dtype = len(self.qlens), H, D, dtype
+        self.bs = block_size
+        self.pool = W.block_pool(g, self.qlens + self.ctx, block_size=block_size)
+        cu_ctx = W.cu_from_lens(self.ctx)
+        kp, vp = (W.rows(g, (int(cu_ctx[-1]), H, D), D, dtype) for _ in range(2))
+        self.kc = poisoned_pool(self.pool.num_blocks, H, D, dtype, block_size)
+        self.vc = self.kc.copy()
+        oracle.kv_append(kp, vp, oracle.slot_mapping(self.pool.block_tables, cu_ctx, block_size=block_size),
+                         self.kc, self.vc, block_size)
+        self.cu = W.cu_from_lens(self.qlens)
+        self.T = int(self.cu[-1])
+        self.q, self.k, self.v = (W.rows(g, (self.T, H, D), D, dtype) for _ in range(3))
+        self.scale = 1 / math.sqrt(D)
+        self.sm = oracle.slot_mapping(self.pool.block_tables, self.cu, self.ctx, block_size)
+        self.okc, self.ovc = self.kc.copy(), self.vc.copy()
+        oracle.kv_append(self.k, self.v, self.sm, self.okc, self.ovc, block_size)
+
+    def dims(self, hyb, window=0):
+        return hyb.dims(self.H, self.D, self.pool.num_blocks, self.pool.max_blocks, self.dtype,
+                        self.scale, block_size=self.bs, window=window)
+
+    def prefill_ref(self, window=0):
+        return oracle.full_prefill(self.q, self.okc, self.ovc, self.pool.block_tables, self.cu,
+                                   self.ctx, self.scale, block_size=self.bs, window=window)
+
+    def decode_ref(self, window=0):
+        """Decode rows (one per request, qlens all 1) over the appended cache."""
+        return oracle.full_decode(self.q, self.okc, self.ovc, self.pool.block_tables, self.ctx + 1,
+                                  self.scale, block_size=self.bs, window=window)
+
+    def prefill_gpu(self, hyb, window, bt):
+        """Append with the full table, attend with `bt` (possibly with released blocks)."""
+        d = self.dims(hyb, window)
+        cu_d, ctx_d = to_dev(self.cu), to_dev(self.ctx)
+        kcd, vcd = to_dev(self.kc), to_dev(self.vc)
+        slot = torch.empty(self.T, dtype=torch.int64, device="cuda")
+        hyb.check(hyb.hyb_slot_mapping(slot, to_dev(self.pool.block_tables), cu_d, ctx_d, self.B, self.T, d))
+        hyb.check(hyb.hyb_paged_kv_append(to_dev(self.k), to_dev(self.v), slot, self.T, kcd, vcd, d))
+        out = empty_rows((self.T, self.H, self.D), self.dtype)
+        hyb.check(hyb.hyb_paged_attn_prefill_causal(out, to_dev(self.q), kcd, vcd, to_dev(bt), cu_d, ctx_d,
+                                                    self.B, self.T, int(self.qlens.max()), d))
+        torch.cuda.synchronize()
+        return out, to_host(slot), to_host(kcd)
+
+
+def decode_case(seed, lens, H, D, dtype, block_size=W.BLOCK_SIZE):
+    """Decode = one new row per request at position lens[b] - 1."""
+    lens = np.asarray(lens, np.int32)
+    return PagedCase(seed, np.ones_like(lens), lens - 1, H, D, dtype, block_size)
+
+
+def decode_gpu(hyb, c, window, bt, max_seq_len=None):
+    d = c.dims(hyb, window)
+    lens = c.ctx + 1
+    msl = int(lens.max()) if max_seq_len is None else max_seq_len
+    kcd, vcd = to_dev(c.okc), to_dev(c.ovc)          # this step's rows already appended
+    ws_n = hyb.hyb_paged_attn_decode_workspace_size(c.B, msl, d)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+    out = empty_rows((c.B, c.H, c.D), c.dtype)
+    hyb.check(hyb.hyb_paged_attn_decode(out, to_dev(c.q), kcd, vcd, to_dev(bt), to_dev(lens), c.B, msl, d,
+                                        ws, ws_n))
+    torch.cuda.synchronize()
+    return out, ws_n

@@ -55,9 +55,16 @@ def test_bad_arguments_rejected_before_launch(hyb):
     assert hyb.hyb_paged_kv_append(fake + 2, fake, fake, 4, fake, fake + 256, d, 0) == hyb.HYB_ERR_INVALID_ARG
     # the same pool passed as K and V
     assert hyb.hyb_paged_kv_append(fake, fake, fake, 4, fake, fake, d, 0) == hyb.HYB_ERR_INVALID_ARG
-    # block size other than 16
-    d16 = hyb.dims(32, 128, 100, 8, block_size=32)
-    assert hyb.hyb_paged_kv_append(fake, fake, fake, 4, fake, fake + 256, d16, 0) == hyb.HYB_ERR_UNSUPPORTED
+    # block sizes other than a power of two from 16 to 256
+    for bs in (8, 24, 48, 512):
+        dbs = hyb.dims(32, 128, 100, 8, block_size=bs)
+        assert hyb.hyb_paged_kv_append(fake, fake, fake, 4, fake, fake + 256, dbs, 0) == hyb.HYB_ERR_UNSUPPORTED
+    # max_seq_len is bounded by max_blocks_per_seq x block_size
+    d32 = hyb.dims(32, 128, 100, 8, block_size=32)
+    assert hyb.hyb_paged_attn_decode(fake, fake, fake, fake, fake, fake, 2, 257, d32, fake, 1 << 20, 0) == hyb.HYB_ERR_INVALID_ARG
+    # pools whose rows (blocks x heads x block size) overflow int32
+    dbig = hyb.dims(32, 128, 1 << 20, 8, block_size=128)
+    assert hyb.hyb_paged_kv_append(fake, fake, fake, 4, fake, fake + 256, dbig, 0) == hyb.HYB_ERR_UNSUPPORTED
     # head_dim without a kernel
     d7 = hyb.dims(4, 24, 100, 8)
     assert hyb.hyb_paged_attn_decode(fake, fake, fake, fake, fake, fake, 2, 32, d7, None, 0, 0) == hyb.HYB_ERR_UNSUPPORTED

@@ -10,86 +10,11 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_helpers import (assert_out_close, empty_rows, poisoned_pool, same_bytes, to_dev,
-                         to_host)
+from gpu_helpers import (PagedCase as Case, assert_out_close, decode_case as _decode_case,
+                         decode_gpu as _decode_gpu, empty_rows, released as _released,
+                         same_bytes, to_dev, to_host)
 
 pytestmark = pytest.mark.gpu
-
-
-def _released(block_tables, first_pos, window):
-    """Copy of the table with -1 for every logical block that ends before the window of the
-    request's earliest query (position first_pos[b])."""
-    bt = block_tables.copy()
-    for b, p in enumerate(first_pos):
-        keep_from = max(0, int(p) - window + 1) // W.BLOCK_SIZE
-        bt[b, :keep_from] = -1
-    return bt
-
-
-class Case:
-    """Requests with a cached prefix (ctx rows, written by the oracle into a poisoned pool)
-    and this call's q/k/v rows (qlens per request)."""
-
-    def __init__(self, seed, qlens, ctx, H, D, dtype):
-        g = W.rng(seed)
-        self.qlens = np.asarray(qlens, np.int32)
-        self.ctx = np.asarray(ctx, np.int32)
-        self.B, self.H, self.D, self.dtype = len(self.qlens), H, D, dtype
-        self.pool = W.block_pool(g, self.qlens + self.ctx)
-        cu_ctx = W.cu_from_lens(self.ctx)
-        kp, vp = (W.rows(g, (int(cu_ctx[-1]), H, D), D, dtype) for _ in range(2))
-        self.kc = poisoned_pool(self.pool.num_blocks, H, D, dtype)
-        self.vc = self.kc.copy()
-        oracle.kv_append(kp, vp, oracle.slot_mapping(self.pool.block_tables, cu_ctx), self.kc, self.vc)
-        self.cu = W.cu_from_lens(self.qlens)
-        self.T = int(self.cu[-1])
-        self.q, self.k, self.v = (W.rows(g, (self.T, H, D), D, dtype) for _ in range(3))
-        self.scale = 1 / math.sqrt(D)
-        self.sm = oracle.slot_mapping(self.pool.block_tables, self.cu, self.ctx)
-        self.okc, self.ovc = self.kc.copy(), self.vc.copy()
-        oracle.kv_append(self.k, self.v, self.sm, self.okc, self.ovc)
-
-    def dims(self, hyb, window):
-        return hyb.dims(self.H, self.D, self.pool.num_blocks, self.pool.max_blocks, self.dtype,
-                        self.scale, window=window)
-
-    def prefill_ref(self, window):
-        return oracle.full_prefill(self.q, self.okc, self.ovc, self.pool.block_tables, self.cu,
-                                   self.ctx, self.scale, window=window)
-
-    def prefill_gpu(self, hyb, window, bt):
-        """Append with the full table, attend with `bt` (possibly with released blocks)."""
-        d = self.dims(hyb, window)
-        cu_d, ctx_d = to_dev(self.cu), to_dev(self.ctx)
-        kcd, vcd = to_dev(self.kc), to_dev(self.vc)
-        slot = torch.empty(self.T, dtype=torch.int64, device="cuda")
-        hyb.check(hyb.hyb_slot_mapping(slot, to_dev(self.pool.block_tables), cu_d, ctx_d, self.B, self.T, d))
-        hyb.check(hyb.hyb_paged_kv_append(to_dev(self.k), to_dev(self.v), slot, self.T, kcd, vcd, d))
-        out = empty_rows((self.T, self.H, self.D), self.dtype)
-        hyb.check(hyb.hyb_paged_attn_prefill_causal(out, to_dev(self.q), kcd, vcd, to_dev(bt), cu_d, ctx_d,
-                                                    self.B, self.T, int(self.qlens.max()), d))
-        torch.cuda.synchronize()
-        return out, to_host(slot), to_host(kcd)
-
-
-def _decode_case(seed, lens, H, D, dtype):
-    """Decode = one new row per request at position lens[b] - 1."""
-    lens = np.asarray(lens, np.int32)
-    return Case(seed, np.ones_like(lens), lens - 1, H, D, dtype)
-
-
-def _decode_gpu(hyb, c, window, bt, max_seq_len=None):
-    d = c.dims(hyb, window)
-    lens = c.ctx + 1
-    msl = int(lens.max()) if max_seq_len is None else max_seq_len
-    kcd, vcd = to_dev(c.okc), to_dev(c.ovc)          # this step's rows already appended
-    ws_n = hyb.hyb_paged_attn_decode_workspace_size(c.B, msl, d)
-    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
-    out = empty_rows((c.B, c.H, c.D), c.dtype)
-    hyb.check(hyb.hyb_paged_attn_decode(out, to_dev(c.q), kcd, vcd, to_dev(bt), to_dev(lens), c.B, msl, d,
-                                        ws, ws_n))
-    torch.cuda.synchronize()
-    return out, ws_n
 
 
 # ------------------------------------------------------------------------ decode
@@ -192,19 +117,20 @@ def test_window_prefill_full_workload_sampled(hyb, devstatus):
 
 
 # ---------------------------------------------------------------------- dispatch
+@pytest.mark.parametrize("bs", [16, 32])
 @pytest.mark.parametrize("mode", [0, 1])
-def test_dispatch_sliding_layers_equal_per_op_calls(hyb, devstatus, mode):
-    """Layers FULL, SLIDING(64), LINEAR, SLIDING(700): the dispatch equals the per-op calls
-    bit for bit, and the windowed layers match the oracle."""
+def test_dispatch_sliding_layers_equal_per_op_calls(hyb, devstatus, mode, bs):
+    """Layers FULL, SLIDING(64), LINEAR, SLIDING(700), 16- and 32-token blocks: the dispatch
+    equals the per-op calls bit for bit, and the windowed layers match the oracle."""
     H, D = 4, 128
     types = [hyb.HYB_FULL, hyb.HYB_SLIDING, hyb.HYB_LINEAR, hyb.HYB_SLIDING]
     windows = [0, 64, 0, 700]
     if mode == 0:
-        c = _decode_case(470, [1, 65, 900, 2000], H, D, W.BF16)
+        c = _decode_case(470, [1, 65, 900, 2000], H, D, W.BF16, bs)
     else:
-        c = Case(471, [100, 700, 33], [0, 64, 1024], H, D, W.BF16)   # Linear: chunk-aligned starts
+        c = Case(471, [100, 700, 33], [0, 64, 1024], H, D, W.BF16, bs)   # Linear: chunk-aligned starts
     B, T = c.B, c.T
-    d0 = c.dims(hyb, 0)
+    d0 = c.dims(hyb, 0)                                   # carries the block size
     bt, cu_d, ctx_d = to_dev(c.pool.block_tables), to_dev(c.cu), to_dev(c.ctx)
     lens_d = to_dev(c.ctx + c.qlens)
     slot = torch.empty(T, dtype=torch.int64, device="cuda")
@@ -253,10 +179,6 @@ def test_dispatch_sliding_layers_equal_per_op_calls(hyb, devstatus, mode):
     for l in range(4):
         assert same_bytes(to_host(outs[l]), to_host(outs2[l])), f"layer {l}"
     for l in (1, 3):
-        if mode == 0:
-            ref = oracle.full_decode(c.q, c.okc, c.ovc, c.pool.block_tables, c.ctx + 1, c.scale,
-                                     window=windows[l])
-        else:
-            ref = c.prefill_ref(windows[l])
+        ref = c.decode_ref(windows[l]) if mode == 0 else c.prefill_ref(windows[l])
         assert_out_close(outs[l], ref, f"sliding layer {l}")
     assert devstatus() == (0, 0)

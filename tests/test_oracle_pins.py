@@ -31,24 +31,24 @@ def _f64(a):
     return W.bf16_to_f32(a).astype(np.float64) if a.dtype == np.uint16 else a.astype(np.float64)
 
 
-def _paged_setup(seed, lens, H, D, dtype, poison=True, slack=1.5):
+def _paged_setup(seed, lens, H, D, dtype, poison=True, slack=1.5, block_size=W.BLOCK_SIZE):
     """Append every row of every request through the oracle's slot mapping into a shuffled
     pool. Returns (pool, kc, vc, k_rows, v_rows, cu)."""
     g = W.rng(seed)
     lens = np.asarray(lens, np.int32)
-    pool = W.block_pool(g, lens, slack=slack)
+    pool = W.block_pool(g, lens, slack=slack, block_size=block_size)
     cu = W.cu_from_lens(lens)
     T = int(cu[-1])
     k = W.rows(g, (T, H, D), D, dtype)
     v = W.rows(g, (T, H, D), D, dtype)
-    shape = (pool.num_blocks, H, W.BLOCK_SIZE, D)
+    shape = (pool.num_blocks, H, block_size, D)
     if dtype == W.BF16:
         kc = np.full(shape, 0x7FC0 if poison else 0, np.uint16)
     else:
         kc = np.full(shape, np.nan if poison else 0, np.float32)
     vc = kc.copy()
-    sm = oracle.slot_mapping(pool.block_tables, cu)
-    oracle.kv_append(k, v, sm, kc, vc)
+    sm = oracle.slot_mapping(pool.block_tables, cu, block_size=block_size)
+    oracle.kv_append(k, v, sm, kc, vc, block_size)
     return pool, kc, vc, k, v, cu, sm
 
 
@@ -80,21 +80,24 @@ def test_cache_bytes_grow_only_vs_constant():
 
 
 # ------------------------------------------------------- append / slots
+@pytest.mark.parametrize("bs", [16, 32])
 @pytest.mark.parametrize("dtype", [W.F32, W.BF16])
-def test_append_one_slot_per_token_and_bytes_exact(dtype):
-    lens = [1, 15, 16, 17, 40]
+def test_append_one_slot_per_token_and_bytes_exact(dtype, bs):
+    lens = [1, 15, 16, 17, 40, 70]
     H, D = 3, 16
-    pool, kc, vc, k, v, cu, sm = _paged_setup(1, lens, H, D, dtype)
-    # exactly one new slot per token, all distinct, all inside the request's own blocks
+    pool, kc, vc, k, v, cu, sm = _paged_setup(1, lens, H, D, dtype, block_size=bs)
+    # exactly one new slot per token, all distinct, all inside the request's own blocks, in
+    # position order within each block
     assert len(sm) == sum(lens) and len(set(sm.tolist())) == len(sm)
     for b in range(len(lens)):
-        owned = set(pool.block_tables[b, :pool.blocks_per_req[b]].tolist())
-        assert all((s // W.BLOCK_SIZE) in owned for s in sm[cu[b]:cu[b + 1]])
+        owned = pool.block_tables[b, :pool.blocks_per_req[b]]
+        for j, s in enumerate(sm[cu[b]:cu[b + 1]]):
+            assert s // bs == owned[j // bs] and s % bs == j % bs
     # the rows appear, byte for byte, at exactly len(sm) slots; every other slot stays poisoned
-    written = ~np.isnan(_f64(kc).reshape(pool.num_blocks, H, W.BLOCK_SIZE, D)[:, 0, :, 0])
+    written = ~np.isnan(_f64(kc).reshape(pool.num_blocks, H, bs, D)[:, 0, :, 0])
     assert int(written.sum()) == sum(lens)
     for t, s in enumerate(sm):
-        assert np.array_equal(kc[s // 16, :, s % 16, :], k[t]) and np.array_equal(vc[s // 16, :, s % 16, :], v[t])
+        assert np.array_equal(kc[s // bs, :, s % bs, :], k[t]) and np.array_equal(vc[s // bs, :, s % bs, :], v[t])
 
 
 def test_append_skips_minus_one():
@@ -108,15 +111,17 @@ def test_append_skips_minus_one():
 
 
 # ------------------------------------------------------------ Full decode
+@pytest.mark.parametrize("bs", [16, 32])
 @pytest.mark.parametrize("dtype", [W.F32, W.BF16])
-def test_decode_matches_sdpa_on_dense_rows(dtype):
-    """Paged decode == dense attention (torch CPU sdpa, fp64) over the rows as generated."""
+def test_decode_matches_sdpa_on_dense_rows(dtype, bs):
+    """Paged decode == dense attention (torch CPU sdpa, fp64) over the rows as generated,
+    with 16- and 32-token blocks."""
     lens = [1, 5, 16, 17, 33, 64]
     H, D = 2, 16
-    pool, kc, vc, k, v, cu, _ = _paged_setup(3, lens, H, D, dtype)
+    pool, kc, vc, k, v, cu, _ = _paged_setup(3, lens, H, D, dtype, block_size=bs)
     q = W.rows(W.rng(33), (len(lens), H, D), D, dtype)
     scale = 1 / math.sqrt(D)
-    out = oracle.full_decode(q, kc, vc, pool.block_tables, lens, scale)
+    out = oracle.full_decode(q, kc, vc, pool.block_tables, lens, scale, block_size=bs)
     for b, n in enumerate(lens):
         K = _f64(k[cu[b]:cu[b + 1]]).transpose(1, 0, 2)      # [H][n][D]
         V = _f64(v[cu[b]:cu[b + 1]]).transpose(1, 0, 2)
@@ -177,19 +182,20 @@ def test_decode_zero_length_gives_zero():
 
 
 # ---------------------------------------------------------- Full prefill
+@pytest.mark.parametrize("bs", [16, 32])
 @pytest.mark.parametrize("ctx", [[0, 0], [16, 5]])
-def test_prefill_matches_causal_sdpa(ctx):
+def test_prefill_matches_causal_sdpa(ctx, bs):
     """Causal prefill (queries at absolute positions ctx + j see keys p <= position)
-    == torch CPU sdpa with an explicit inclusive causal mask, fp64."""
+    == torch CPU sdpa with an explicit inclusive causal mask, fp64; 16- and 32-token blocks."""
     H, D = 2, 16
     qlens = [5, 37]
     tot = [c + n for c, n in zip(ctx, qlens)]
-    pool, kc, vc, k, v, cu_all, _ = _paged_setup(9, tot, H, D, W.BF16)
+    pool, kc, vc, k, v, cu_all, _ = _paged_setup(9, tot, H, D, W.BF16, block_size=bs)
     g = W.rng(10)
     cuq = W.cu_from_lens(qlens)
     q = W.rows(g, (int(cuq[-1]), H, D), D, W.BF16)
     scale = 1 / math.sqrt(D)
-    out = oracle.full_prefill(q, kc, vc, pool.block_tables, cuq, ctx, scale)
+    out = oracle.full_prefill(q, kc, vc, pool.block_tables, cuq, ctx, scale, block_size=bs)
     for b in range(2):
         K = _f64(k[cu_all[b]:cu_all[b + 1]]).transpose(1, 0, 2)
         V = _f64(v[cu_all[b]:cu_all[b + 1]]).transpose(1, 0, 2)
@@ -200,7 +206,8 @@ def test_prefill_matches_causal_sdpa(ctx):
         np.testing.assert_allclose(out[cuq[b]:cuq[b + 1]], ref, rtol=1e-12, atol=1e-14)
     # row subset gives the same rows
     rows = np.array([0, 4, 5, 41], np.int32)
-    np.testing.assert_array_equal(oracle.full_prefill(q, kc, vc, pool.block_tables, cuq, ctx, scale, rows), out[rows])
+    np.testing.assert_array_equal(oracle.full_prefill(q, kc, vc, pool.block_tables, cuq, ctx, scale, rows,
+                                                      block_size=bs), out[rows])
 
 
 # ------------------------------------------------- sliding-window Full attention
