@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--workload", default="decode_single_layer",
                     choices=["decode_single_layer", "hybrid_32layer", "prefill_chunked", "long_context_decode",
-                             "sliding_window", "state_precision", "block32"],
+                             "sliding_window", "state_precision", "block32", "bucketing"],
                     help="decode_single_layer is the headline; the others are timed alone (e.g. for profiling)")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements of the other workloads")
     return ap.parse_args()
@@ -554,9 +554,86 @@ def row_block32(hyb, device, stream, iters, seed=0):
                              peak_source="measured bf16_tflops (burst)")}
 
 
+def row_bucketing(hyb, device, stream, iters, seed=0):
+    """Length-bucketed batching: the 32-layer decode step of the 64-request 80%/20% mix run as
+    one call in arrival order, as one call sorted by length, and as two calls (requests with
+    <= 512 cached tokens, then the rest). The kernels take ragged batches without padding, so
+    bucketing only changes the order and the number of launches."""
+    import torch
+    hbm, _, _ = measured_peaks()
+    db = W.decode_hybrid_32layer(seed)
+    lt = db.extra["layer_types"]
+    B, H, D, NB, MB = db.B, db.H, db.D, db.pool.num_blocks, db.pool.max_blocks
+    d = hyb.dims(H, D, NB, MB, W.BF16)
+    g = W.rng(seed + 19)
+    keep, per_layer = [], []
+    for l, t in enumerate(lt):
+        q = W.device_rows_(torch.empty((B, H, D), dtype=torch.bfloat16, device=device), 400 + l, D)
+        o = torch.empty_like(q)
+        if t == 0:
+            kc = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), 500 + l, D)
+            vc = W.device_rows_(torch.empty_like(kc), 600 + l, D)
+            keep += [q, o, kc, vc]
+            per_layer.append((q, o, kc, vc, None))
+        else:
+            sp = W.device_state_(torch.empty((B, H, D, D), device=device), 700 + l, db.seq_lens, D)
+            keep += [q, o, sp]
+            per_layer.append((q, o, None, None, sp))
+    sh = stream.cuda_stream
+
+    def plan(order):
+        """One dispatch call over the requests in `order` (rows r of q/k/v/out = order[r])."""
+        n = len(order)
+        lens = db.seq_lens[order]
+        bt = torch.from_numpy(np.ascontiguousarray(db.pool.block_tables[order])).to(device)
+        ln = torch.from_numpy(lens).to(device)
+        ctx = torch.from_numpy(lens - 1).to(device)
+        cu = torch.arange(n + 1, dtype=torch.int32, device=device)
+        slots = torch.from_numpy(np.asarray(order, np.int32)).to(device)
+        slot = torch.empty(n, dtype=torch.int64, device=device)
+        msl = int(lens.max())
+        ws_n = hyb.hyb_paged_attn_decode_workspace_size(n, msl, d)
+        ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=device)
+        rows = torch.from_numpy(np.asarray(order, np.int64)).to(device)
+        ios = []
+        bufs = [bt, ln, ctx, cu, slots, slot, ws]
+        for (q, o, kc, vc, sp) in per_layer:
+            qb, ob = q[rows].contiguous(), o[rows].contiguous()
+            bufs += [qb, ob]
+            ios.append(hyb.layer_io(ob, qb, qb, qb, kc, vc) if kc is not None
+                       else hyb.layer_io(ob, qb, qb, qb, state_pool=sp, num_state_slots=B))
+        meta = hyb.batch_meta(n, n, seq_lens=ln, block_tables=bt, slot_mapping=slot, state_slots=slots,
+                              max_seq_len=msl)
+
+        def run():
+            hyb.check(hyb.hyb_slot_mapping(slot, bt, cu, ctx, n, n, d, sh))
+            hyb.check(hyb.hyb_layer_dispatch(lt, len(lt), 0, ios, meta, d, 64, ws, ws_n, sh))
+        return run, bufs
+
+    arrival = np.arange(B)
+    by_len = np.argsort(-db.seq_lens, kind="stable")
+    short = np.nonzero(db.seq_lens <= 512)[0]
+    long_ = np.nonzero(db.seq_lens > 512)[0]
+    res_ms = {}
+    for name, groups in (("one_call_arrival_order", [arrival]), ("one_call_sorted_by_length", [by_len]),
+                         ("two_buckets_short_then_long", [short, long_])):
+        runs = [plan(gr) for gr in groups if len(gr)]
+        res_ms[name] = round(_time(lambda: [r() for r, _ in runs], stream, iters), 4)
+        del runs
+    alg = int((lt == 0).sum()) * (int(db.seq_lens.sum()) * H * D * 4 + 2 * B * H * D * 2) + \
+        int((lt == 1).sum()) * B * H * D * D * 8
+    t0 = res_ms["one_call_arrival_order"]
+    del keep, per_layer
+    torch.cuda.empty_cache()
+    return {"workload": "bucketing: 32-layer decode step, batch 64, 80% ~128 / 20% ~2048 cached tokens",
+            "value": round(B * 32 / (t0 * 1e-3), 1), "unit": UNIT, "ms_per_step": res_ms,
+            "buckets": {"short_le_512": int(len(short)), "long": int(len(long_))},
+            "roofline": _roof("hbm", alg / (t0 * 1e-3) / 1e9, hbm, "GB/s", "whole 32-layer step, one call", alg)}
+
+
 ROWS = {"long_context_decode": row_long_context, "hybrid_32layer": row_hybrid_32layer,
         "prefill_chunked": row_prefill, "sliding_window": row_sliding_window,
-        "state_precision": row_state_precision, "block32": row_block32}
+        "state_precision": row_state_precision, "block32": row_block32, "bucketing": row_bucketing}
 
 
 def bench_ours(args, dist):
