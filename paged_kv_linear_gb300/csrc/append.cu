@@ -17,6 +17,7 @@ __global__ void slot_mapping_kernel(int64_t* __restrict__ slot, const int32_t* _
                                     const int32_t* __restrict__ cu,
                                     const int32_t* __restrict__ ctx, int MB, int NB, int bs,
                                     unsigned* status) {
+  pdl_wait();
   const int b = blockIdx.x;
   const int t0 = cu[b], t1 = cu[b + 1];
   const int64_t p0 = ctx ? ctx[b] : 0;
@@ -34,6 +35,7 @@ __global__ void slot_mapping_kernel(int64_t* __restrict__ slot, const int32_t* _
     }
     slot[t] = s;
   }
+  pdl_trigger();
 }
 
 cudaError_t launch_slot_mapping(int64_t* slot, const int32_t* bt, const int32_t* cu,
@@ -42,9 +44,10 @@ cudaError_t launch_slot_mapping(int64_t* slot, const int32_t* bt, const int32_t*
   if (B == 0 || T == 0) return cudaSuccess;
   const int per_req = (T + B - 1) / B;
   dim3 grid(B, (unsigned)std::min(64, std::max(1, (per_req + 255) / 256)));
-  slot_mapping_kernel<<<grid, 256, 0, s>>>(slot, bt, cu, ctx, MB, NB, bs, status);
+  const cudaError_t e =
+      launch_pdl(slot_mapping_kernel, grid, dim3(256), 0, s, slot, bt, cu, ctx, MB, NB, bs, status);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 // One thread per 16-byte vector of a (token, head) row, for K and V together.
@@ -54,6 +57,7 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k, const uint4* __res
                                  const int64_t* __restrict__ slot, int64_t total, int H, int vpr,
                                  int bs, int64_t n_slots, uint4* __restrict__ kc,
                                  uint4* __restrict__ vc, unsigned* status) {
+  pdl_wait();
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     const int64_t row = i / vpr;           // t*H + h
@@ -71,6 +75,7 @@ __global__ void kv_append_kernel(const uint4* __restrict__ k, const uint4* __res
     kc[dst] = k[i];
     vc[dst] = v[i];
   }
+  pdl_trigger();
 }
 
 cudaError_t launch_kv_append(const void* k, const void* v, const int64_t* slot, int T, int H,
@@ -83,11 +88,12 @@ cudaError_t launch_kv_append(const void* k, const void* v, const int64_t* slot, 
   int64_t blocks = (total + threads - 1) / threads;
   const int64_t cap = (int64_t)num_sms() * 16;
   if (blocks > cap) blocks = cap;
-  kv_append_kernel<<<(unsigned)blocks, threads, 0, s>>>(
-      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot, total, H, vpr, bs,
-      (int64_t)NB * bs, static_cast<uint4*>(kc), static_cast<uint4*>(vc), status);
+  const cudaError_t e = launch_pdl(
+      kv_append_kernel, dim3((unsigned)blocks), dim3(threads), 0, s, static_cast<const uint4*>(k),
+      static_cast<const uint4*>(v), slot, total, H, vpr, bs, (int64_t)NB * bs,
+      static_cast<uint4*>(kc), static_cast<uint4*>(vc), status);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace hyb

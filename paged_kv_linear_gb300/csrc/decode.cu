@@ -110,6 +110,7 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
   using S = DecodeShape<T, D>;
   constexpr int VEC = S::VEC, LPR = S::LPR, TPI = S::TPI, ITER = S::ITER, TILE = S::TILE;
 
+  pdl_wait();                              // inputs may come from the previous kernel
   const int h = blockIdx.y, split = blockIdx.z;
   int b, r, n_raw;                         // request, packed row of q/out, keys to attend
   if (PREFILL) {                           // grid.x = B * max_q: (request, query index)
@@ -259,6 +260,7 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
     for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
   }
 
+  pdl_trigger();                           // the next kernel may launch; it waits for our stores
   // merge the token sub-rows of the warp (lanes with the same c)
 #pragma unroll
   for (int o = LPR; o < 32; o <<= 1)
@@ -302,6 +304,7 @@ __global__ void __launch_bounds__(128)
 decode_combine_kernel(T* __restrict__ out, const int32_t* __restrict__ seq_lens, int H, int MBt,
                       int max_len, int window, int max_splits, const float* __restrict__ ws_acc,
                       const float2* __restrict__ ws_ml) {
+  pdl_wait();
   const int r = blockIdx.x, h = blockIdx.y;
   const int n = clamp_len(seq_lens[r], max_len, MBt);
   const int nsplit = decode_splits(n, window);
@@ -322,6 +325,7 @@ decode_combine_kernel(T* __restrict__ out, const int32_t* __restrict__ seq_lens,
     }
     Elt<T>::store(out + rh * D + t, L > 0.f ? A / L : 0.f);
   }
+  pdl_trigger();
 }
 
 template <typename T, int D>
@@ -348,16 +352,16 @@ cudaError_t launch_typed(void* out, const void* q, const void* kc, const void* v
       static_cast<char*>(ws) + (size_t)R * H * max_splits * D * sizeof(float));
   dim3 grid(prefill ? R * max_q : R, H, max_splits);
   const float scale_log2 = scale * 1.4426950408889634f;
-  kern<<<grid, kNW * 32, Sh::SMEM, s>>>((T*)out, (const T*)q, (const T*)kc, (const T*)vc, bt,
-                                        seq_lens, cu, ctx, max_q, H, NB, MB, rsh, max_len, scale_log2,
-                                        window, max_splits, ws_acc, ws_ml, status);
+  e = launch_pdl(kern, grid, dim3(kNW * 32), Sh::SMEM, s, (T*)out, (const T*)q, (const T*)kc,
+                 (const T*)vc, bt, seq_lens, cu, ctx, max_q, H, NB, MB, rsh, max_len, scale_log2,
+                 window, max_splits, ws_acc, ws_ml, status);
   count_launch();
-  e = cudaGetLastError();
   if (e != cudaSuccess || max_splits == 1) return e;
-  decode_combine_kernel<T, D><<<dim3(R, H), 128, 0, s>>>((T*)out, seq_lens, H, MB << rsh, max_len,
-                                                          window, max_splits, ws_acc, ws_ml);
+  e = launch_pdl(decode_combine_kernel<T, D>, dim3(R, H), dim3(128), 0, s, (T*)out, seq_lens, H,
+                 MB << rsh, max_len, window, max_splits, (const float*)ws_acc,
+                 (const float2*)ws_ml);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 }  // namespace

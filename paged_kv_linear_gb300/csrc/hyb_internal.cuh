@@ -21,6 +21,26 @@ unsigned* status_word();                   // this device's status word (nullptr
 int num_sms();                             // SMs of the current device (cached)
 cudaError_t set_smem(const void* fn, int bytes);   // opt-in dynamic shared memory, once
 
+// Programmatic dependent launch for the short kernels of a decode step: a kernel launched
+// this way may be scheduled while the previous kernel on the stream drains. It calls
+// pdl_wait() before it reads anything (so stream order holds for every input) and
+// pdl_trigger() once its own main work is done, so the next launch overlaps its tail.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // kernel launchers (each returns the launch's cudaError_t)
 cudaError_t launch_slot_mapping(int64_t* slot, const int32_t* bt, const int32_t* cu,
                                 const int32_t* ctx, int B, int T, int MB, int NB, int bs,
@@ -79,6 +99,11 @@ cudaError_t launch_prefill_tc(void* out, const void* q, const void* kc, const vo
 // ------------------------------------------------------------------ device side
 #ifdef __CUDACC__
 namespace hyb {
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ void flag(unsigned* st, unsigned bit) {
   if (st) atomicOr(st, bit);

@@ -62,6 +62,7 @@ linear_step_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __rest
   constexpr int COLS = Sh::COLS, TPR = Sh::TPR, RPP = Sh::RPP, PASSES = Sh::PASSES;
   __shared__ float red[RPP][COLS];
 
+  pdl_wait();
   const int cb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int slot = slots[b];
   if (slot < 0 || slot >= NS) {
@@ -96,6 +97,7 @@ linear_step_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __rest
     o2 = fmaf(qi, s.z, o2);
     o3 = fmaf(qi, s.w, o3);
   }
+  pdl_trigger();
   red[rg][tc * 4 + 0] = o0;
   red[rg][tc * 4 + 1] = o1;
   red[rg][tc * 4 + 2] = o2;
@@ -243,10 +245,11 @@ cudaError_t step_typed(void* out, const void* q, const void* k, const void* v, f
                        cudaStream_t s) {
   using Sh = StepShape<D>;
   dim3 grid(D / Sh::COLS, H, B);
-  linear_step_kernel<T, D><<<grid, Sh::THREADS, 0, s>>>((T*)out, (const T*)q, (const T*)k,
-                                                        (const T*)v, pool, NS, slots, H, status);
+  const cudaError_t e = launch_pdl(linear_step_kernel<T, D>, grid, dim3(Sh::THREADS), 0, s, (T*)out,
+                                   (const T*)q, (const T*)k, (const T*)v, pool, NS, slots, H,
+                                   status);
   count_launch();
-  return cudaGetLastError();
+  return e;
 }
 
 template <typename T, typename S16, int D>
