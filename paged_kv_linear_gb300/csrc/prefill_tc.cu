@@ -50,10 +50,10 @@ constexpr int kNSW = 8;                      // softmax warps: 4 per query tile
 constexpr int kWarpTmaK = kNSW, kWarpTmaV = kNSW + 1, kWarpMma = kNSW + 2;   // + 1 idle warp
 constexpr int kThreads = (kNSW + 4) * 32;    // three full warpgroups
 // Register split (setmaxnreg): the launch gives 384 threads x 168 registers (three warps
-// per SM sub-partition). The producer warpgroup drops to 88 and the two softmax warpgroups
-// rise to 208: 2 x 128 x 208 + 128 x 88 = 64 512 <= 64 512 registers of the launch, and
-// (208 + 208 + 88) x 32 = 16 128 <= 16 384 per sub-partition.
-constexpr uint32_t kRegsSoftmax = 208, kRegsProducer = 88;
+// per SM sub-partition). The producer warpgroup drops to 104 and the two softmax warpgroups
+// rise to 200: 2 x 128 x 200 + 128 x 104 = 64 512 <= 64 512 registers of the launch, and
+// (200 + 200 + 104) x 32 = 16 128 <= 16 384 per sub-partition.
+constexpr uint32_t kRegsSoftmax = 200, kRegsProducer = 104;
 constexpr uint32_t kTmemCols = 512;          // S_0/P_0 | S_1/P_1 | O_0 | O_1
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;
