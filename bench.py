@@ -708,8 +708,10 @@ def bench_ours(args, dist):
     clocks.stop()
     per_op = np.zeros(n_ops)
     total_ms = 0.0
+    step_ms = []
     for e in evs:
-        total_ms += e[0].elapsed_time(e[n_ops])
+        step_ms.append(e[0].elapsed_time(e[n_ops]))
+        total_ms += step_ms[-1]
         for i in range(n_ops):
             per_op[i] += e[i].elapsed_time(e[i + 1])
     per_op /= args.steps
@@ -792,6 +794,8 @@ def bench_ours(args, dist):
     return {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "ms_per_step_p50": round(float(np.percentile(step_ms, 50)), 5),
+        "ms_per_step_p99": round(float(np.percentile(step_ms, 99)), 5),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1)/sqrt(D) q/k/v, shuffled block pool, N(0,seq/D^2) states)",
         "config": {"workload": "decode_single_layer: 32 requests, H=32, D=128, block 16, seq_lens U{128..4096}, "
@@ -835,10 +839,25 @@ def cpu_baseline_decode(wl, budget_s=15.0, requests=None):
             if t_used > budget_s:
                 break
         passes += 1
-    return {"value": round(done * 2 / t_used, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{done} request-steps ({passes} pass(es) over the {wl['B']} requests, all {H} heads; "
-                      f"Full decode + Linear step), fp64 C oracle with OpenMP over (request, head), "
-                      f"{t_used:.1f} s"}
+    res = {"value": round(done * 2 / t_used, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+           "sample": f"{done} request-steps ({passes} pass(es) over the {wl['B']} requests, all {H} heads; "
+                     f"Full decode + Linear step), fp64 C oracle with OpenMP over (request, head), "
+                     f"{t_used:.1f} s"}
+    # the same oracle on one core, over a short sample (first requests of the batch)
+    oracle.set_threads(1)
+    done1, t1 = 0, 0.0
+    for b in order:
+        if t1 > budget_s / 5:
+            break
+        t0 = time.perf_counter()
+        oracle.full_decode(hq["qf"][b:b + 1], kc, vc, db.pool.block_tables[b:b + 1], db.seq_lens[b:b + 1], D ** -0.5)
+        oracle.linear_step(hq["ql"][b:b + 1], hq["kl"][b:b + 1], hq["vl"][b:b + 1], st, wl["slots_h"][b:b + 1])
+        t1 += time.perf_counter() - t0
+        done1 += 1
+    oracle.set_threads(cores)
+    res["single_thread"] = {"value": round(done1 * 2 / t1, 2), "unit": UNIT, "cores": 1,
+                            "sample": f"the first {done1} requests of the batch, {t1:.1f} s"}
+    return res
 
 
 def bench_reference(args, dist):
