@@ -13,14 +13,14 @@
 // conversion warps move TMEM -> registers -> shared/global memory. The state lives in TMEM
 // for the whole call and is accumulated in place. Per chunk (M x N x K), in issue order:
 //   (d) S   += K_c^T V_c          128 x 128 x 64  A = K^T (MN-major), B = V (MN-major)
-//   (b) O^T  = S^T Q_c^T          128 x 64 x 128  A = S^T of the previous chunk end, as two
-//                                                 bf16 parts hi + lo (~16 bits), B = Q
+//   (b) O^T  = S^T Q_c^T          128 x 64 x 128  A = S^T of the previous chunk end, rounded
+//                                                 to bf16 (the fp32 state stays in TMEM), B = Q
 //   (a) P    = Q_c K_c^T          64 x 64 x 128   A = Q (K-major), B = K (K-major)
 //   (c) O^T += V_c^T tril(P)^T    128 x 64 x 64   A = V^T (MN-major), B = tril(P) (K-major)
-// The chain that limits a request is (d) -> read S from TMEM -> hi/lo split -> next (d);
-// (d) is issued first so the conversion warps read the new state while (b) still runs, and
-// write the split only once (b) has consumed the previous one; (c) of a chunk is issued
-// after (a) of the next, so no state update waits for P's conversion. O^T and P are
+// The chain that limits a request is (d) -> read S from TMEM -> next (d): the conversion
+// warps release the state as soon as they hold it in registers ("S read"), and write its
+// bf16 copy for (b) only once (b) has consumed the previous one ("S written"); (c) of a
+// chunk is issued after (a) of the next, so no state update waits for P's conversion. O^T and P are
 // double-buffered (TMEM and shared memory) and every handshake barrier exists once per
 // buffer parity, so none can run two phases ahead of its waiter. Output is computed
 // transposed (M = value dim) so all MMAs but (a) use M = 128, and each conversion thread
@@ -37,9 +37,9 @@ constexpr int kNST = 3;                      // Q/K/V ring stages
 constexpr int kSub = 64 * 128;               // bytes of one [64 rows][64 cols] SW128 sub-tile
 constexpr int kTile = 2 * kSub;              // [64][128] bf16 tile
 constexpr int kStage = 3 * kTile;            // Q, K, V
-constexpr int kOffS = kNST * kStage;         // S^T hi / lo (each [128 k-rows][128], MN-major)
+constexpr int kOffS = kNST * kStage;         // S^T as bf16 ([128 k-rows][128], MN-major)
 constexpr int kSTile = 128 * 128 * 2;
-constexpr int kOffP = kOffS + 2 * kSTile;    // tril(P) [64][64] K-major, two buffers
+constexpr int kOffP = kOffS + kSTile;        // tril(P) [64][64] K-major, two buffers
 constexpr int kOffBar = kOffP + 2 * kSub;
 constexpr int kSmem = kOffBar + 256 + 1024;  // + slack for 1024-byte alignment
 constexpr int kNCW = 8;                      // conversion warps
@@ -55,7 +55,7 @@ constexpr uint32_t kIdescC = idesc_bf16(128, 64, 1, 0);
 
 struct Bars {
   uint64_t full[kNST], empty[kNST];
-  uint64_t s_ready, b_done, s_written, drain;
+  uint64_t s_ready, s_read, b_done, s_written, drain;
   uint64_t p_ready[2], p_written[2], o_ready[2], o_free[2];   // one per buffer parity
 };
 
@@ -102,6 +102,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
       }
       mbar_init(&bars->s_ready, 1);
       mbar_init(&bars->b_done, 1);
+      mbar_init(&bars->s_read, kNCW * 32);
       mbar_init(&bars->s_written, kNCW * 32);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&bars->p_ready[i], 1);
@@ -120,7 +121,6 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   uint8_t* const s_hi = sm + kOffS;
-  uint8_t* const s_lo = s_hi + kSTile;
   uint8_t* const p_tile = sm + kOffP;
 
   if (warp == kWarpTma) {
@@ -165,7 +165,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
     const uint32_t sm0 = smem_u32(sm);
     const uint64_t mn0 = sw128_desc(sm0, kSub, 1024);          // MN-major, 64-row sub-tiles
     const uint64_t km0 = sw128_desc(sm0, 16, 1024);            // K-major
-    const uint64_t st0 = sw128_desc(sm0 + kOffS, 16384, 1024); // S^T hi (lo at +kSTile)
+    const uint64_t st0 = sw128_desc(sm0 + kOffS, 16384, 1024); // S^T (bf16)
     auto issue_c = [&](int c) {                  // (c) O^T += V^T tril(P)^T of chunk c
       const int st = c % kNST, pb = c & 1;
       const uint32_t vo = st * kStage + 2 * kTile, po = kOffP + pb * kSub;
@@ -199,7 +199,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
         fence_async_smem();
       }
       __syncwarp();
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_written, c & 1));
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_read, c & 1));   // S of chunk c-1 read
       if (!ok) break;
       if (lane == 0) {
         tc_fence_after();
@@ -213,17 +213,15 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_free[ob], ((c - 2) >> 1) & 1));
         if (!ok) break;
       }
+      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_written, c & 1));   // bf16 S^T ready
+      if (!ok) break;
       if (lane == 0) {
         tc_fence_after();
         const uint32_t od = tmem + kColO + ob * 64;
 #pragma unroll
-        for (int part = 0; part < 2; ++part) {   // (b) O^T = S^T Q^T, hi then lo
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t boff = (k >> 2) * kSub + (k & 3) * 32;
-            tc_mma(od, desc_add(st0, part * kSTile + k * 2048), desc_add(km0, qo + boff), kIdescB,
-                   (part | k) != 0);
-          }
+        for (int k = 0; k < 8; ++k) {            // (b) O^T = S^T Q^T
+          const uint32_t boff = (k >> 2) * kSub + (k & 3) * 32;
+          tc_mma(od, desc_add(st0, k * 2048), desc_add(km0, qo + boff), kIdescB, k != 0);
         }
         tc_commit(&bars->b_done);
 #pragma unroll
@@ -257,23 +255,14 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
     const uint32_t soff0 = (row >> 3) * 1024;            // k-row group of the S^T operand
     bool ok = true;
-    // hi/lo bf16 parts of 8 consecutive state values
-    auto split8 = [](const float* v, uint4& hi, uint4& lo) {
-      uint32_t hw[4], lw[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const __nv_bfloat16 h0 = __float2bfloat16_rn(v[2 * e]), h1 = __float2bfloat16_rn(v[2 * e + 1]);
-        hw[e] = (uint32_t)__bfloat16_as_ushort(h0) | ((uint32_t)__bfloat16_as_ushort(h1) << 16);
-        lw[e] = pack_bf16(v[2 * e] - __bfloat162float(h0), v[2 * e + 1] - __bfloat162float(h1));
-      }
-      hi = make_uint4(hw[0], hw[1], hw[2], hw[3]);
-      lo = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+    // bf16 copy of 8 consecutive state values
+    auto pack8 = [](const float* v) {
+      return make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                        pack_bf16(v[6], v[7]));
     };
-    // this thread's part of the S^T operands: k-row `row`, value columns hf*64 .. +63
-    auto put8 = [&](int ch, const uint4& hi, const uint4& lo) {   // ch = chunk 0..7 of MN block hf
-      const uint32_t off = hf * 16384 + soff0 + sw128_off(row & 7, ch);
-      *reinterpret_cast<uint4*>(s_hi + off) = hi;
-      *reinterpret_cast<uint4*>(s_lo + off) = lo;
+    // this thread's part of the S^T operand: k-row `row`, value columns hf*64 .. +63
+    auto put8 = [&](int ch, const uint4& w) {            // ch = chunk 0..7 of MN block hf
+      *reinterpret_cast<uint4*>(s_hi + hf * 16384 + soff0 + sw128_off(row & 7, ch)) = w;
     };
     // O^T of chunk cc -> global: this thread owns value dim j = row, tokens hf*32 .. +31
     auto store_out = [&](int cc) -> bool {
@@ -307,15 +296,12 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
         }
         tmem_st32(tl + kColS + j0, v);
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint4 hi, lo;
-          split8(v + ch * 8, hi, lo);
-          put8(part * 4 + ch, hi, lo);
-        }
+        for (int ch = 0; ch < 4; ++ch) put8(part * 4 + ch, pack8(v + ch * 8));
       }
       tmem_st_wait();
       fence_async_smem();
       tc_fence_before();
+      mbar_arrive(&bars->s_read);
       mbar_arrive(&bars->s_written);
     }
     for (int c = 0; c < nch; ++c) {
@@ -335,30 +321,29 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
           for (int e = 0; e < 32; e += 4)
             *reinterpret_cast<float4*>(Sg + (int64_t)row * kD + j0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
         }
+        tc_fence_before();
+        mbar_arrive(&bars->s_read);
       } else {
-        // first 32 columns split before (b) releases the old operand, the rest after:
-        // keeps the live registers within the 10-warp budget
-        uint4 hi[4], lo[4];
+        // hold the new state in registers and release TMEM at once: the next (d) may run
+        uint4 w[8];
         {
-          float v[32];
+          float v[32], v2[32];
           tmem_ld32(tl + kColS + hf * 64, v);
+          tmem_ld32(tl + kColS + hf * 64 + 32, v2);
           tmem_ld_wait();
+          tc_fence_before();
+          mbar_arrive(&bars->s_read);
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) split8(v + ch * 8, hi[ch], lo[ch]);
+          for (int ch = 0; ch < 4; ++ch) {
+            w[ch] = pack8(v + ch * 8);
+            w[4 + ch] = pack8(v2 + ch * 8);
+          }
         }
-        float v2[32];
-        tmem_ld32(tl + kColS + hf * 64 + 32, v2);
-        tmem_ld_wait();
+        // ... and overwrite the bf16 copy only after (b) has read the previous one
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->b_done, c & 1));
         if (!ok) break;
 #pragma unroll
-        for (int ch = 0; ch < 4; ++ch) put8(ch, hi[ch], lo[ch]);
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          uint4 h2, l2;
-          split8(v2 + ch * 8, h2, l2);
-          put8(4 + ch, h2, l2);
-        }
+        for (int ch = 0; ch < 8; ++ch) put8(ch, w[ch]);
         fence_async_smem();
       }
       tc_fence_before();
