@@ -23,8 +23,10 @@
 // chunk is issued after (a) of the next, so no state update waits for P's conversion. O^T and P are
 // double-buffered (TMEM and shared memory) and every handshake barrier exists once per
 // buffer parity, so none can run two phases ahead of its waiter. Output is computed
-// transposed (M = value dim) so all MMAs but (a) use M = 128, and each conversion thread
-// stores one column of O: a warp's stores are 64 contiguous bytes.
+// transposed (M = value dim) so all MMAs but (a) use M = 128; the conversion threads write
+// each output chunk into a shared staging tile (two buffers) that one thread stores with
+// TMA, so the conversion warps do not wait on global stores (a request's last, partial
+// chunk is stored directly, so no row of the next request is touched).
 #include <cuda_bf16.h>
 
 #include "tc.cuh"
@@ -40,7 +42,8 @@ constexpr int kStage = 3 * kTile;            // Q, K, V
 constexpr int kOffS = kNST * kStage;         // S^T as bf16 ([128 k-rows][128], MN-major)
 constexpr int kSTile = 128 * 128 * 2;
 constexpr int kOffP = kOffS + kSTile;        // tril(P) [64][64] K-major, two buffers
-constexpr int kOffBar = kOffP + 2 * kSub;
+constexpr int kOffO = kOffP + 2 * kSub;      // output staging [64 tokens][128] bf16, two buffers
+constexpr int kOffBar = kOffO + 2 * kTile;
 constexpr int kSmem = kOffBar + 256 + 1024;  // + slack for 1024-byte alignment
 constexpr int kNCW = 8;                      // conversion warps
 constexpr int kWarpTma = kNCW, kWarpMma = kNCW + 1;
@@ -57,12 +60,14 @@ struct Bars {
   uint64_t full[kNST], empty[kNST];
   uint64_t s_ready, s_read, b_done, s_written, drain;
   uint64_t p_ready[2], p_written[2], o_ready[2], o_free[2];   // one per buffer parity
+  uint64_t o_staged[2], o_stage_free[2];
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
 linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
                          const __grid_constant__ CUtensorMap tk,
-                         const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ out,
+                         const __grid_constant__ CUtensorMap tv,
+                         const __grid_constant__ CUtensorMap to, __nv_bfloat16* __restrict__ out,
                          const int32_t* __restrict__ cu, const int32_t* __restrict__ ctx,
                          float* __restrict__ pool, int NS, const int32_t* __restrict__ slots,
                          const uint8_t* __restrict__ reset, int H, unsigned* status) {
@@ -109,6 +114,8 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
         mbar_init(&bars->p_written[i], kNCW * 32);
         mbar_init(&bars->o_ready[i], 1);
         mbar_init(&bars->o_free[i], kNCW * 32);
+        mbar_init(&bars->o_staged[i], kNCW * 32);
+        mbar_init(&bars->o_stage_free[i], 1);
       }
       mbar_init(&bars->drain, 1);
       fence_mbar_init();
@@ -122,6 +129,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
   const uint32_t tmem = tmem_base;
   uint8_t* const s_hi = sm + kOffS;
   uint8_t* const p_tile = sm + kOffP;
+  uint8_t* const o_stage = sm + kOffO;
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA warp
@@ -264,23 +272,53 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
     auto put8 = [&](int ch, const uint4& w) {            // ch = chunk 0..7 of MN block hf
       *reinterpret_cast<uint4*>(s_hi + hf * 16384 + soff0 + sw128_off(row & 7, ch)) = w;
     };
-    // O^T of chunk cc -> global: this thread owns value dim j = row, tokens hf*32 .. +31
+    // O^T of chunk cc -> global: this thread owns value dim j = row, tokens hf*32 .. +31.
+    // Full chunks go through staging buffer cc & 1 and a TMA store issued by one thread;
+    // before it writes a buffer again, that thread has seen the previous store read it.
+    const bool issuer = warp == 0 && lane == 0;
     auto store_out = [&](int cc) -> bool {
       if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_ready[cc & 1], (cc >> 1) & 1))) return false;
       tc_fence_after();
       float v[32];
       tmem_ld32(tl + kColO + (cc & 1) * 64 + hf * 32, v);
       tmem_ld_wait();
-      const int nv = min(kC, n - cc * kC) - hf * 32;     // valid tokens of this half
-      __nv_bfloat16* o = out + ((int64_t)(t0 + cc * kC + hf * 32) * H + h) * kD + row;
-      const int64_t step = (int64_t)H * kD;               // one token further
+      tc_fence_before();
+      mbar_arrive(&bars->o_free[cc & 1]);                 // TMEM buffer free for (b) of cc + 2
+      const int nvalid = min(kC, n - cc * kC);
+      if (nvalid < kC) {                                   // partial chunk: direct stores
+        const int nv = nvalid - hf * 32;                   // valid tokens of this half
+        __nv_bfloat16* o = out + ((int64_t)(t0 + cc * kC + hf * 32) * H + h) * kD + row;
+        const int64_t step = (int64_t)H * kD;              // one token further
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          if (e < nv) *o = __float2bfloat16_rn(v[e]);
+          o += step;
+        }
+        return true;
+      }
+      const int sb = cc & 1;
+      if (cc >= 2 &&
+          !__all_sync(0xffffffffu, mbar_wait(&bars->o_stage_free[sb], ((cc - 2) >> 1) & 1)))
+        return false;
+      // staging tile: two [64 tokens][64 j] SW128 sub-tiles (j halves), row = token; this
+      // thread's j sits in 16-byte chunk (j & 63) / 8 at byte (j & 7) * 2
+      uint8_t* const ob = o_stage + sb * kTile + (row >> 6) * kSub + (row & 7) * 2;
+      const uint32_t jc = (row & 63) >> 3;
 #pragma unroll
       for (int e = 0; e < 32; ++e) {
-        if (e < nv) *o = __float2bfloat16_rn(v[e]);
-        o += step;
+        const int t = hf * 32 + e;
+        *reinterpret_cast<__nv_bfloat16*>(ob + sw128_off(t, jc)) = __float2bfloat16_rn(v[e]);
       }
-      tc_fence_before();
-      mbar_arrive(&bars->o_free[cc & 1]);
+      fence_async_smem();
+      mbar_arrive(&bars->o_staged[sb]);
+      if (issuer) {
+        if (!mbar_wait(&bars->o_staged[sb], (cc >> 1) & 1)) return false;
+        tma_store_3d(&to, o_stage + sb * kTile, 0, h, t0 + cc * kC);
+        tma_store_3d(&to, o_stage + sb * kTile + kSub, 64, h, t0 + cc * kC);
+        bulk_commit();
+        bulk_wait_read<1>();                               // the previous chunk's store has read
+        if (cc >= 1) mbar_arrive(&bars->o_stage_free[sb ^ 1]);
+      }
       return true;
     };
     {                                                    // initial state, 32 columns at a time
@@ -381,6 +419,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
       }
     }
     if (ok) ok = store_out(nch - 1);
+    if (issuer) bulk_wait<0>();                            // every store complete before exit
     if (!ok && lane == 0) flag(status, HYB_DEVERR_TIMEOUT);
   }
   tc_fence_before();
@@ -403,18 +442,19 @@ cudaError_t launch_linear_prefill_tc(void* out, const void* q, const void* k, co
   (void)max_len;
   (void)C;
   if (B == 0) return cudaSuccess;
-  CUtensorMap mq, mk, mv;
+  CUtensorMap mq, mk, mv, mo;
   const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)H, (uint64_t)(T > 0 ? T : 1)};
   const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)H * kD * 2};
   const uint32_t box[3] = {64, 1, (uint32_t)kC};
   if (!encode_tmap_bf16(&mq, q, 3, dims, strides, box) ||
       !encode_tmap_bf16(&mk, k, 3, dims, strides, box) ||
-      !encode_tmap_bf16(&mv, v, 3, dims, strides, box))
+      !encode_tmap_bf16(&mv, v, 3, dims, strides, box) ||
+      !encode_tmap_bf16(&mo, out, 3, dims, strides, box))
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem((const void*)linear_prefill_tc_kernel, kSmem);
   if (e != cudaSuccess) return e;
   linear_prefill_tc_kernel<<<dim3(H, B), kThreads, kSmem, s>>>(
-      mq, mk, mv, static_cast<__nv_bfloat16*>(out), cu, ctx, pool, NS, slots, reset, H, status);
+      mq, mk, mv, mo, static_cast<__nv_bfloat16*>(out), cu, ctx, pool, NS, slots, reset, H, status);
   count_launch();
   return cudaGetLastError();
 }
