@@ -23,10 +23,10 @@
 // chunk is issued after (a) of the next, so no state update waits for P's conversion. O^T and P are
 // double-buffered (TMEM and shared memory) and every handshake barrier exists once per
 // buffer parity, so none can run two phases ahead of its waiter. Output is computed
-// transposed (M = value dim) so all MMAs but (a) use M = 128; the conversion threads write
-// each output chunk into a shared staging tile (two buffers) that one thread stores with
-// TMA, so the conversion warps do not wait on global stores (a request's last, partial
-// chunk is stored directly, so no row of the next request is touched).
+// transposed (M = value dim) so all MMAs but (a) use M = 128. Four conversion warps carry
+// the state and P; the other four only move outputs: they write each output chunk into a
+// shared staging tile (two buffers) that one thread stores with TMA (a request's last,
+// partial chunk is stored directly, so no row of the next request is touched).
 #include <cuda_bf16.h>
 
 #include "tc.cuh"
@@ -107,14 +107,14 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
       }
       mbar_init(&bars->s_ready, 1);
       mbar_init(&bars->b_done, 1);
-      mbar_init(&bars->s_read, kNCW * 32);
-      mbar_init(&bars->s_written, kNCW * 32);
+      mbar_init(&bars->s_read, 128);               // state warps (0-3)
+      mbar_init(&bars->s_written, 128);
       for (int i = 0; i < 2; ++i) {
         mbar_init(&bars->p_ready[i], 1);
-        mbar_init(&bars->p_written[i], kNCW * 32);
+        mbar_init(&bars->p_written[i], 128);           // state warps
         mbar_init(&bars->o_ready[i], 1);
-        mbar_init(&bars->o_free[i], kNCW * 32);
-        mbar_init(&bars->o_staged[i], kNCW * 32);
+        mbar_init(&bars->o_free[i], 128);              // output warps (4-7)
+        mbar_init(&bars->o_staged[i], 128);
         mbar_init(&bars->o_stage_free[i], 1);
       }
       mbar_init(&bars->drain, 1);
@@ -258,168 +258,166 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
     }
   } else {
     // ------------------------------------------------------------ conversion warps
-    const int quarter = warp & 3, hf = warp >> 2;
+    // Warps 0-3 carry the state chain and P; warps 4-7 only write outputs, so a late output
+    // never holds up the next state update. Warp w reaches TMEM lanes 32 * (w % 4) ...
+    const int quarter = warp & 3;
     const int row = quarter * 32 + lane;                 // TMEM lane of this thread
     const uint32_t tl = tmem + ((uint32_t)(quarter * 32) << 16);
-    const uint32_t soff0 = (row >> 3) * 1024;            // k-row group of the S^T operand
     bool ok = true;
-    // bf16 copy of 8 consecutive state values
-    auto pack8 = [](const float* v) {
-      return make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
-                        pack_bf16(v[6], v[7]));
-    };
-    // this thread's part of the S^T operand: k-row `row`, value columns hf*64 .. +63
-    auto put8 = [&](int ch, const uint4& w) {            // ch = chunk 0..7 of MN block hf
-      *reinterpret_cast<uint4*>(s_hi + hf * 16384 + soff0 + sw128_off(row & 7, ch)) = w;
-    };
-    // O^T of chunk cc -> global: this thread owns value dim j = row, tokens hf*32 .. +31.
-    // Full chunks go through staging buffer cc & 1 and a TMA store issued by one thread;
-    // before it writes a buffer again, that thread has seen the previous store read it.
-    const bool issuer = warp == 0 && lane == 0;
-    auto store_out = [&](int cc) -> bool {
-      if (!__all_sync(0xffffffffu, mbar_wait(&bars->o_ready[cc & 1], (cc >> 1) & 1))) return false;
-      tc_fence_after();
-      float v[32];
-      tmem_ld32(tl + kColO + (cc & 1) * 64 + hf * 32, v);
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(&bars->o_free[cc & 1]);                 // TMEM buffer free for (b) of cc + 2
-      const int nvalid = min(kC, n - cc * kC);
-      if (nvalid < kC) {                                   // partial chunk: direct stores
-        const int nv = nvalid - hf * 32;                   // valid tokens of this half
-        __nv_bfloat16* o = out + ((int64_t)(t0 + cc * kC + hf * 32) * H + h) * kD + row;
-        const int64_t step = (int64_t)H * kD;              // one token further
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          if (e < nv) *o = __float2bfloat16_rn(v[e]);
-          o += step;
-        }
-        return true;
-      }
-      const int sb = cc & 1;
-      if (cc >= 2 &&
-          !__all_sync(0xffffffffu, mbar_wait(&bars->o_stage_free[sb], ((cc - 2) >> 1) & 1)))
-        return false;
-      // staging tile: two [64 tokens][64 j] SW128 sub-tiles (j halves), row = token; this
-      // thread's j sits in 16-byte chunk (j & 63) / 8 at byte (j & 7) * 2
-      uint8_t* const ob = o_stage + sb * kTile + (row >> 6) * kSub + (row & 7) * 2;
-      const uint32_t jc = (row & 63) >> 3;
-#pragma unroll
-      for (int e = 0; e < 32; ++e) {
-        const int t = hf * 32 + e;
-        *reinterpret_cast<__nv_bfloat16*>(ob + sw128_off(t, jc)) = __float2bfloat16_rn(v[e]);
-      }
-      fence_async_smem();
-      mbar_arrive(&bars->o_staged[sb]);
-      if (issuer) {
-        if (!mbar_wait(&bars->o_staged[sb], (cc >> 1) & 1)) return false;
-        tma_store_3d(&to, o_stage + sb * kTile, 0, h, t0 + cc * kC);
-        tma_store_3d(&to, o_stage + sb * kTile + kSub, 64, h, t0 + cc * kC);
-        bulk_commit();
-        bulk_wait_read<1>();                               // the previous chunk's store has read
-        if (cc >= 1) mbar_arrive(&bars->o_stage_free[sb ^ 1]);
-      }
-      return true;
-    };
-    {                                                    // initial state, 32 columns at a time
+    if (warp < 4) {
+      const uint32_t soff0 = (row >> 3) * 1024;          // k-row group of the S^T operand
+      // bf16 copy of 8 consecutive state values
+      auto pack8 = [](const float* v) {
+        return make_uint4(pack_bf16(v[0], v[1]), pack_bf16(v[2], v[3]), pack_bf16(v[4], v[5]),
+                          pack_bf16(v[6], v[7]));
+      };
+      // this thread's part of the S^T operand: k-row `row`, value columns 8 * ch ..; MN
+      // block ch / 8
+      auto put8 = [&](int ch, const uint4& w) {
+        *reinterpret_cast<uint4*>(s_hi + (ch >> 3) * 16384 + soff0 + sw128_off(row & 7, ch & 7)) = w;
+      };
+      {                                                  // initial state, 32 columns at a time
 #pragma unroll 1
-      for (int part = 0; part < 2; ++part) {
-        const int j0 = hf * 64 + part * 32;
-        float v[32];
-#pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const float4 x = zero_start ? make_float4(0.f, 0.f, 0.f, 0.f)
-                                      : *reinterpret_cast<const float4*>(Sg + (int64_t)row * kD + j0 + e);
-          v[e] = x.x; v[e + 1] = x.y; v[e + 2] = x.z; v[e + 3] = x.w;
-        }
-        tmem_st32(tl + kColS + j0, v);
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) put8(part * 4 + ch, pack8(v + ch * 8));
-      }
-      tmem_st_wait();
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars->s_read);
-      mbar_arrive(&bars->s_written);
-    }
-    for (int c = 0; c < nch; ++c) {
-      const bool last = c == nch - 1;
-      // ---- new state: read it from TMEM; write the hi/lo operand once (b) has used the old one
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_ready, c & 1));
-      if (!ok) break;
-      tc_fence_after();
-      if (last) {
-#pragma unroll 1
-        for (int part = 0; part < 2; ++part) {
-          const int j0 = hf * 64 + part * 32;
+        for (int part = 0; part < 4; ++part) {
+          const int j0 = part * 32;
           float v[32];
-          tmem_ld32(tl + kColS + j0, v);
-          tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            *reinterpret_cast<float4*>(Sg + (int64_t)row * kD + j0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+          for (int e = 0; e < 32; e += 4) {
+            const float4 x = zero_start ? make_float4(0.f, 0.f, 0.f, 0.f)
+                                        : *reinterpret_cast<const float4*>(Sg + (int64_t)row * kD + j0 + e);
+            v[e] = x.x; v[e + 1] = x.y; v[e + 2] = x.z; v[e + 3] = x.w;
+          }
+          tmem_st32(tl + kColS + j0, v);
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) put8(part * 4 + ch, pack8(v + ch * 8));
         }
+        tmem_st_wait();
+        fence_async_smem();
         tc_fence_before();
         mbar_arrive(&bars->s_read);
-      } else {
-        // hold the new state in registers and release TMEM at once: the next (d) may run
-        uint4 w[8];
-        {
-          float v[32], v2[32];
-          tmem_ld32(tl + kColS + hf * 64, v);
-          tmem_ld32(tl + kColS + hf * 64 + 32, v2);
-          tmem_ld_wait();
+        mbar_arrive(&bars->s_written);
+      }
+      for (int c = 0; c < nch; ++c) {
+        const bool last = c == nch - 1;
+        // ---- new state: read it from TMEM; write the bf16 copy once (b) has used the old one
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_ready, c & 1));
+        if (!ok) break;
+        tc_fence_after();
+        if (last) {
+#pragma unroll 1
+          for (int part = 0; part < 4; ++part) {
+            const int j0 = part * 32;
+            float v[32];
+            tmem_ld32(tl + kColS + j0, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; e += 4)
+              *reinterpret_cast<float4*>(Sg + (int64_t)row * kD + j0 + e) = make_float4(v[e], v[e + 1], v[e + 2], v[e + 3]);
+          }
           tc_fence_before();
           mbar_arrive(&bars->s_read);
+        } else {
+          // hold the new state (as bf16) in registers and release TMEM: the next (d) may run
+          uint4 w[16];
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            w[ch] = pack8(v + ch * 8);
-            w[4 + ch] = pack8(v2 + ch * 8);
+          for (int part = 0; part < 4; ++part) {
+            float v[32];
+            tmem_ld32(tl + kColS + part * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int ch = 0; ch < 4; ++ch) w[part * 4 + ch] = pack8(v + ch * 8);
           }
+          tc_fence_before();
+          mbar_arrive(&bars->s_read);
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->b_done, c & 1));
+          if (!ok) break;
+#pragma unroll
+          for (int ch = 0; ch < 16; ++ch) put8(ch, w[ch]);
+          fence_async_smem();
         }
-        // ... and overwrite the bf16 copy only after (b) has read the previous one
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->b_done, c & 1));
+        tc_fence_before();
+        mbar_arrive(&bars->s_written);
+        // ---- tril(P) -> shared (K-major [t][t']), buffer c & 1
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_ready[c & 1], (c >> 1) & 1));
         if (!ok) break;
+        tc_fence_after();
+        {
+          uint8_t* const pt = p_tile + (c & 1) * kSub;
+#pragma unroll 1
+          for (int hf = 0; hf < 2; ++hf) {
+            float v[32];
+            tmem_ld32(tl + kColP + (c & 1) * 64 + hf * 32, v);
+            tmem_ld_wait();
+            if (lane < 16) {
+              const int t = quarter * 16 + lane;         // M = 64 layout: lanes 0..15 of each quarter
 #pragma unroll
-        for (int ch = 0; ch < 8; ++ch) put8(ch, w[ch]);
-        fence_async_smem();
-      }
-      tc_fence_before();
-      mbar_arrive(&bars->s_written);
-      // ---- tril(P) -> shared (K-major [t][t']), buffer c & 1
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_ready[c & 1], (c >> 1) & 1));
-      if (!ok) break;
-      tc_fence_after();
-      {
-        float v[32];
-        tmem_ld32(tl + kColP + (c & 1) * 64 + hf * 32, v);
-        tmem_ld_wait();
-        uint8_t* const pt = p_tile + (c & 1) * kSub;
-        if (lane < 16) {
-          const int t = quarter * 16 + lane;             // M = 64 layout: lanes 0..15 of each quarter
+              for (int ch = 0; ch < 4; ++ch) {
+                uint32_t wp[4];
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const int tp = hf * 32 + ch * 8 + 2 * e;
-              w[e] = pack_bf16(tp <= t ? v[ch * 8 + 2 * e] : 0.f, tp + 1 <= t ? v[ch * 8 + 2 * e + 1] : 0.f);
+                for (int e = 0; e < 4; ++e) {
+                  const int tp = hf * 32 + ch * 8 + 2 * e;
+                  wp[e] = pack_bf16(tp <= t ? v[ch * 8 + 2 * e] : 0.f, tp + 1 <= t ? v[ch * 8 + 2 * e + 1] : 0.f);
+                }
+                *reinterpret_cast<uint4*>(pt + sw128_off(t, hf * 4 + ch)) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
+              }
             }
-            *reinterpret_cast<uint4*>(pt + sw128_off(t, hf * 4 + ch)) = make_uint4(w[0], w[1], w[2], w[3]);
           }
         }
+        fence_async_smem();
+        tc_fence_before();
+        mbar_arrive(&bars->p_written[c & 1]);
       }
-      fence_async_smem();
-      tc_fence_before();
-      mbar_arrive(&bars->p_written[c & 1]);
-      // ---- output of the previous chunk (its (c) is issued after this chunk's (a))
-      if (c >= 1) {
-        ok = store_out(c - 1);
+    } else {
+      // O^T of chunk cc -> global: this thread owns value dim j = row, all 64 tokens. Full
+      // chunks go through staging buffer cc & 1 and a TMA store issued by one thread; before
+      // a buffer is written again, that thread has seen the store that used it read it.
+      const bool issuer = warp == 4 && lane == 0;
+      for (int cc = 0; cc < nch && ok; ++cc) {
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[cc & 1], (cc >> 1) & 1));
         if (!ok) break;
+        tc_fence_after();
+        float v[64];
+        tmem_ld32(tl + kColO + (cc & 1) * 64, v);
+        tmem_ld32(tl + kColO + (cc & 1) * 64 + 32, v + 32);
+        tmem_ld_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->o_free[cc & 1]);              // TMEM buffer free for (b) of cc + 2
+        const int nvalid = min(kC, n - cc * kC);
+        if (nvalid < kC) {                               // partial chunk: direct stores
+          __nv_bfloat16* o = out + ((int64_t)(t0 + cc * kC) * H + h) * kD + row;
+          const int64_t step = (int64_t)H * kD;          // one token further
+#pragma unroll
+          for (int e = 0; e < 64; ++e) {
+            if (e < nvalid) *o = __float2bfloat16_rn(v[e]);
+            o += step;
+          }
+          continue;
+        }
+        const int sb = cc & 1;
+        if (cc >= 2) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_stage_free[sb], ((cc - 2) >> 1) & 1));
+          if (!ok) break;
+        }
+        // staging tile: two [64 tokens][64 j] SW128 sub-tiles (j halves), row = token; this
+        // thread's j sits in 16-byte chunk (j & 63) / 8 at byte (j & 7) * 2
+        uint8_t* const ob = o_stage + sb * kTile + (row >> 6) * kSub + (row & 7) * 2;
+        const uint32_t jc = (row & 63) >> 3;
+#pragma unroll
+        for (int t = 0; t < 64; ++t)
+          *reinterpret_cast<__nv_bfloat16*>(ob + sw128_off(t, jc)) = __float2bfloat16_rn(v[t]);
+        fence_async_smem();
+        mbar_arrive(&bars->o_staged[sb]);
+        if (issuer) {
+          if (!mbar_wait(&bars->o_staged[sb], (cc >> 1) & 1)) { ok = false; break; }
+          tma_store_3d(&to, o_stage + sb * kTile, 0, h, t0 + cc * kC);
+          tma_store_3d(&to, o_stage + sb * kTile + kSub, 64, h, t0 + cc * kC);
+          bulk_commit();
+          bulk_wait_read<1>();                           // the previous chunk's store has read
+          if (cc >= 1) mbar_arrive(&bars->o_stage_free[sb ^ 1]);
+        }
       }
+      if (issuer) bulk_wait<0>();                        // every store complete before exit
     }
-    if (ok) ok = store_out(nch - 1);
-    if (issuer) bulk_wait<0>();                            // every store complete before exit
     if (!ok && lane == 0) flag(status, HYB_DEVERR_TIMEOUT);
   }
   tc_fence_before();
