@@ -229,6 +229,15 @@ hyb_status_t hyb_linear_attn_step_lowp(void* out, const void* q, const void* k, 
  * row count. chunk_size 64 with D = 128 and bf16
  * runs the tensor-core kernel; other (D, dtype, chunk) combinations run the CUDA-core
  * kernel (same contract).
+ * The tensor-core kernel is a cooperative launch of at most one CTA per SM that shares all
+ * (request, head) chains' chunks out evenly; a chain cut between two CTAs is handed over
+ * through its own state slot, with a flag in a small library-owned array (128 KiB of device
+ * memory per GPU) that names the call (a per-call epoch, bumped by a one-thread kernel
+ * launched just before, and the launch's grid id). Calls on one stream, eager or captured
+ * in graphs, need nothing more. Calls whose kernels overlap on the GPU (two streams) can
+ * overwrite each other's flags: a waiting CTA then gives up after ~2 s and sets
+ * HYB_DEVERR_TIMEOUT. A flag is only ever accepted from its own call, so overlap never
+ * yields a silently wrong state.
  * ------------------------------------------------------------------------- */
 hyb_status_t hyb_linear_attn_chunked_prefill(void* out, const void* q, const void* k,
                                              const void* v, const int32_t* cu_seqlens,

@@ -179,6 +179,66 @@ def test_chunked_linear_misaligned_start_is_flagged(hyb, devstatus):
     assert_out_close(out[:100], o_ref)
 
 
+def test_chunked_linear_many_chains_ragged(hyb, devstatus):
+    """More (request, head) chains than SMs with ragged lengths: empty requests (reset or
+    not), one row, exactly one chunk, partial last chunks, one long request. Every output
+    row and every state against the recurrence. The kernel shares all chunks out evenly
+    over its CTAs, so here chains are cut between CTAs at many points and several short
+    chains follow one another inside one CTA."""
+    g = W.rng(95)
+    lens = g.integers(0, 700, 48)
+    lens[[3, 17, 30]] = 0
+    lens[[5, 6, 7]] = [1, 64, 129]
+    lens[40] = 2500
+    c = _linear_case(96, lens, H=8)
+    c["reset"][[3, 17]] = 1                              # an empty request with a reset: zero state
+    c["reset"][30] = 0                                   # and one without: state left alone
+    o_ref, s_ref = oracle.linear_recurrence(c["q"], c["k"], c["v"], c["cu"], c["pool"], c["slots"], c["reset"])
+    out, pool_d = _linear_gpu(hyb, c)
+    assert_out_close(out, o_ref, "linear prefill out")
+    got = to_host(pool_d)
+    assert_states_close(got[c["slots"]], s_ref, "linear prefill state")
+    assert not got[c["slots"][[3, 17]]].any()
+    assert np.array_equal(got[c["slots"][30]], c["pool"][c["slots"][30]])
+    untouched = np.setdiff1d(np.arange(c["NS"]), c["slots"])
+    assert np.array_equal(got[untouched], c["pool"][untouched])
+    assert devstatus() == (0, 0)
+
+
+def test_chunked_linear_graph_replays_with_new_inputs(hyb, devstatus):
+    """The prefill captured once in a CUDA graph and replayed with new q/k/v and a fresh
+    state each time: every replay equals the recurrence on its own inputs (so no replay
+    takes a state handed over by an earlier one)."""
+    c = _linear_case(97, np.full(40, 300), H=8)
+    qd, kd, vd = (to_dev(c[x]) for x in ("q", "k", "v"))
+    cu_d, slots_d, reset_d = to_dev(c["cu"]), to_dev(c["slots"]), to_dev(c["reset"])
+    pool_d = to_dev(c["pool"])
+    out = empty_rows((c["T"], c["H"], c["D"]), W.BF16)
+
+    def call():
+        hyb.check(hyb.hyb_linear_attn_chunked_prefill(out, qd, kd, vd, cu_d, None, pool_d, c["NS"], slots_d,
+                                                      reset_d, c["B"], c["T"], 300, c["H"], c["D"], 64, W.BF16))
+
+    call()                                               # first call outside the capture
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        call()
+    for rep in range(3):
+        g = W.rng(300 + rep)
+        new = {x: W.rows(g, (c["T"], c["H"], c["D"]), c["D"], W.BF16) for x in ("q", "k", "v")}
+        for x, d in (("q", qd), ("k", kd), ("v", vd)):
+            d.copy_(to_dev(new[x]))
+        pool_d.copy_(to_dev(c["pool"]))
+        graph.replay()
+        torch.cuda.synchronize()
+        o_ref, s_ref = oracle.linear_recurrence(new["q"], new["k"], new["v"], c["cu"], c["pool"], c["slots"],
+                                                c["reset"])
+        assert_out_close(out, o_ref, f"replay {rep}")
+        assert_states_close(to_host(pool_d)[c["slots"]], s_ref, f"replay {rep} state")
+    assert devstatus() == (0, 0)
+
+
 def test_chunked_linear_full_workload_sampled(hyb, devstatus):
     """8 requests x 8192 tokens, H=32, D=128, chunk 64, zero initial state: whole output
     shape computed on the GPU; sampled (request, head) chains against the recurrence."""
@@ -196,7 +256,7 @@ def test_chunked_linear_full_workload_sampled(hyb, devstatus):
                                                   W.BF16))
     torch.cuda.synchronize()
     outh, st = to_host(out), to_host(pool)
-    for b, h in [(0, 0), (3, 17), (7, 31)]:
+    for b, h in [(0, 0), (0, 1), (3, 17), (5, 9), (7, 31)]:
         sl = slice(int(cu[b]), int(cu[b + 1]))
         o_ref, s_ref = oracle.linear_recurrence(q[sl, h:h + 1], k[sl, h:h + 1], v[sl, h:h + 1], [0, 8192])
         assert_out_close(outh[sl, h:h + 1], o_ref, f"chain ({b},{h})")
