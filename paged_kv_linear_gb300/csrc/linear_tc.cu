@@ -1,36 +1,39 @@
 // Chunked linear-attention prefill on the tensor cores (tcgen05 + TMEM + TMA), bf16 q/k/v,
-// D = 128, chunk C = 64, fp32 state.
+// D = 128, fp32 state.
 //
 // Page: "推理框架适配Hybrid Model：KV Cache管理与算子调度实战", §2.1 (state update
 // S <- S + k (outer) v, output q.S), §2.3 (state zeroed at request start, accumulated in
 // prefill, kept in fp32) and §2.4 (chunks carry the state; chunk boundaries aligned).
 // Per chunk c of a (request, head), with S the fp32 state at the chunk start:
 //     O_c = Q_c S + tril(Q_c K_c^T) V_c        S <- S + K_c^T V_c
+// The result does not depend on where the chunks are cut, so the kernel cuts each call's
+// rows into chunks of 128 (the call's start must still sit on a 64-token boundary, the
+// chunk size of the interface): every product is then a 128 x 128 tile, the shape the
+// tensor core runs best (a smaller N costs almost as many cycles per instruction).
 //
 // GB300 design. Each (request, head) chain is sequential, and there are often not many more
 // chains than SMs (8 x 32 = 256 chains on 152 SMs would leave a second wave two-thirds
 // full). So one CTA per SM, all resident at once (cooperative launch), takes an equal share
 // of all chunks laid end to end; a chain cut between two CTAs hands its state over through
 // the state pool (see "work split" below). Within a CTA the runs follow one another without
-// draining the pipeline. Warp roles: one TMA warp streams Q/K/V chunks through a 3-stage ring (SW128
-// tiles, one mbarrier per stage); one MMA warp issues the tensor-core work; eight
-// conversion warps move TMEM -> registers -> shared/global memory. The state lives in TMEM
-// for the whole call and is accumulated in place. Per chunk (M x N x K), in issue order:
-//   (d) S   += K_c^T V_c          128 x 128 x 64  A = K^T (MN-major), B = V (MN-major)
-//   (b) O^T  = S^T Q_c^T          128 x 64 x 128  A = S^T of the previous chunk end, rounded
-//                                                 to bf16 (the fp32 state stays in TMEM), B = Q
-//   (a) P    = Q_c K_c^T          64 x 64 x 128   A = Q (K-major), B = K (K-major)
-//   (c) O^T += V_c^T tril(P)^T    128 x 64 x 64   A = V^T (MN-major), B = tril(P) (K-major)
-// The chain that limits a request is (d) -> read S from TMEM -> next (d): the conversion
-// warps release the state as soon as they hold it in registers ("S read"), and write its
-// bf16 copy for (b) only once (b) has consumed the previous one ("S written"); (c) of a
-// chunk is issued after (a) of the next, so no state update waits for P's conversion. O^T and P are
-// double-buffered (TMEM and shared memory) and every handshake barrier exists once per
-// buffer parity, so none can run two phases ahead of its waiter. Output is computed
-// transposed (M = value dim) so all MMAs but (a) use M = 128. Four conversion warps carry
-// the state and P; the other four only move outputs: they write each output chunk into a
-// shared staging tile (two buffers) that one thread stores with TMA (a request's last,
-// partial chunk is stored directly, so no row of the next request is touched).
+// draining the pipeline. Warp roles: one TMA warp streams Q/K/V chunks through a 2-stage
+// ring (SW128 tiles, one mbarrier per stage); one MMA warp issues the tensor-core work;
+// four state warps carry the state and P; four output warps write O. The state lives in
+// TMEM for the whole call and is accumulated in place. Per chunk (M x N x K, all 128):
+//   (d) S  += K_c^T V_c      A = K^T (MN-major), B = V (MN-major)
+//   (b) O   = Q_c S          A = Q (K-major), B = the state at the chunk start rounded to
+//                            bf16 (MN-major, shared memory; the fp32 state stays in TMEM)
+//   (a) P   = Q_c K_c^T      A = Q, B = K (both K-major), fp32 into TMEM
+//   (c) O  += tril(P) V_c    A = tril(P) as bf16 in TMEM (written over P by the state
+//                            warps), B = V (MN-major)
+// Issue order per chunk: (d)_c, (b)_c, (c)_{c-1}, (a)_c. The tensor core runs them in
+// order, so (a)_c overwrites P only after (c)_{c-1} has read it, and the state warps
+// convert P_c while (d)_{c+1} and (b)_{c+1} run. The state chain is (d) -> read S from
+// TMEM -> next (d): the state warps release the state as soon as it is in their registers
+// ("S read") and write its bf16 copy for (b) once (b) has consumed the previous one ("S
+// written"). O is double-buffered in TMEM; every handshake barrier has one phase in flight
+// at most. Output rows go straight from registers to global memory (one thread per token
+// row of 256 bytes).
 #include <cuda_bf16.h>
 
 #include "tc.cuh"
@@ -38,34 +41,32 @@
 namespace hyb {
 namespace {
 
-constexpr int kC = 64, kD = 128;
-constexpr int kNST = 3;                      // Q/K/V ring stages
-constexpr int kSub = 64 * 128;               // bytes of one [64 rows][64 cols] SW128 sub-tile
-constexpr int kTile = 2 * kSub;              // [64][128] bf16 tile
+constexpr int kC = 128, kD = 128;            // chunk rows, head dim
+constexpr int kAlign = 64;                   // chunk size of the interface: call starts align to it
+constexpr int kNST = 2;                      // Q/K/V ring stages
+constexpr int kSub = 128 * 128;              // bytes of one [128 rows][64 cols] SW128 sub-tile
+constexpr int kTile = 2 * kSub;              // [128][128] bf16 tile
 constexpr int kStage = 3 * kTile;            // Q, K, V
-constexpr int kOffS = kNST * kStage;         // S^T as bf16 ([128 k-rows][128], MN-major)
+constexpr int kOffS = kNST * kStage;         // state as bf16 ([128 i][128 j], MN-major B)
 constexpr int kSTile = 128 * 128 * 2;
-constexpr int kOffP = kOffS + kSTile;        // tril(P) [64][64] K-major, two buffers
-constexpr int kOffO = kOffP + 2 * kSub;      // output staging [64 tokens][128] bf16, two buffers
-constexpr int kOffBar = kOffO + 2 * kTile;
+constexpr int kOffBar = kOffS + kSTile;
 constexpr int kSmem = kOffBar + 256 + 1024;  // + slack for 1024-byte alignment
-constexpr int kNCW = 8;                      // conversion warps
-constexpr int kWarpTma = kNCW, kWarpMma = kNCW + 1;
-constexpr int kThreads = (kNCW + 2) * 32;
-constexpr uint32_t kTmemCols = 512;          // S [0,128) | O^T x2 [128,256) | P x2 [256,384)
-constexpr uint32_t kColS = 0, kColO = 128, kColP = 256;
+constexpr int kWarpTma = 8, kWarpMma = 9;
+constexpr int kThreads = 10 * 32;
+constexpr uint32_t kTmemCols = 512;          // S [0,128) | O x2 [128,384) | P [384,512)
+constexpr uint32_t kColS = 0, kColO = 128, kColP = 384;
 
-constexpr uint32_t kIdescA = idesc_bf16(64, 64, 0, 0);
-constexpr uint32_t kIdescB = idesc_bf16(128, 64, 1, 0);
-constexpr uint32_t kIdescD = idesc_bf16(128, 128, 1, 1);
-constexpr uint32_t kIdescC = idesc_bf16(128, 64, 1, 0);
+constexpr uint32_t kIdescD = idesc_bf16(128, 128, 1, 1);   // K^T, V: both MN-major
+constexpr uint32_t kIdescB = idesc_bf16(128, 128, 0, 1);   // Q K-major, S MN-major
+constexpr uint32_t kIdescA = idesc_bf16(128, 128, 0, 0);   // Q, K: K-major
+constexpr uint32_t kIdescC = idesc_bf16(128, 128, 0, 1);   // tril(P) from TMEM, V MN-major
 
 struct Bars {
   uint64_t full[kNST], empty[kNST];
   uint64_t s_ready, s_read, b_done, s_written, drain;
-  uint64_t p_ready[2], p_written[2], o_ready[2], o_free[2];   // one per buffer parity
-  uint64_t o_staged[2], o_stage_free[2];
-  uint64_t published;        // state warps' pool writes of a run that hands its state over
+  uint64_t p_ready, p_written;
+  uint64_t o_ready[2], o_free[2];   // one per buffer parity
+  uint64_t published;               // state warps' pool writes of a run that hands its state over
 };
 
 // ------------------------------------------------------------------ work split
@@ -187,7 +188,7 @@ __device__ __forceinline__ bool make_run(int unit, int c0, int c1, const int32_t
   const int b = unit / H;
   const int nc = chunks_of(cu, b);
   const int slot = slots[b];
-  if (nc == 0 || slot < 0 || slot >= NS || (ctx && ctx[b] % kC != 0)) return false;
+  if (nc == 0 || slot < 0 || slot >= NS || (ctx && ctx[b] % kAlign != 0)) return false;
   s.h = unit - b * H;
   s.t0 = cu[b];
   s.n = cu[b + 1] - s.t0;
@@ -250,17 +251,16 @@ __device__ __forceinline__ uint4 pack8(const float* v) {     // bf16 copy of 8 v
                     pack_bf16(v[6], v[7]));
 }
 
-// This thread's 16-byte piece ch (value columns 8 ch ..) of the S^T operand: k-row `row`,
-// MN block ch / 8, SW128 layout.
+// This thread's 16-byte piece ch (value columns 8 ch ..) of the bf16 state operand: row
+// i = `row`, MN block ch / 8, SW128 layout ([j / 64][i / 8][i % 8][j % 64]).
 __device__ __forceinline__ void put8(uint8_t* s_t, int row, int ch, const uint4& w) {
   *reinterpret_cast<uint4*>(s_t + (ch >> 3) * 16384 + (row >> 3) * 1024 + sw128_off(row & 7, ch & 7)) = w;
 }
 
 // Starting state of run `sg`, row `row` (one state warp thread) -> TMEM lane `tl`, and its
-// bf16 copy -> the S^T operand s_t (which (b) must no longer be reading). A run that
-// continues a chain first waits until the CTA that ran the chain's start has published it
-// with this call's tag `want` (on expiry: reported, and the pool's contents are used as
-// they are).
+// bf16 copy -> the operand s_t (which (b) must no longer be reading). A run that continues
+// a chain first waits until the CTA that ran the chain's start has published it with this
+// call's tag `want` (on expiry: reported, and the pool's contents are used as they are).
 __device__ __forceinline__ void load_start(const Seg& sg, uint8_t* s_t, uint32_t tl, int row,
                                            const unsigned long long* handoff_flag,
                                            unsigned long long want, unsigned* status) {
@@ -295,8 +295,7 @@ __device__ __forceinline__ void load_start(const Seg& sg, uint8_t* s_t, uint32_t
 __global__ void __launch_bounds__(kThreads, 1)
 linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
                          const __grid_constant__ CUtensorMap tk,
-                         const __grid_constant__ CUtensorMap tv,
-                         const __grid_constant__ CUtensorMap to, __nv_bfloat16* __restrict__ out,
+                         const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ out,
                          const int32_t* __restrict__ cu, const int32_t* __restrict__ ctx,
                          float* __restrict__ pool, int NS, const int32_t* __restrict__ slots,
                          const uint8_t* __restrict__ reset, int B, int H, unsigned* status) {
@@ -312,7 +311,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
       if (tid == 0) flag(status, HYB_DEVERR_BAD_STATE);
       continue;
     }
-    if (ctx && ctx[b] % kC != 0) {
+    if (ctx && ctx[b] % kAlign != 0) {
       if (tid == 0) flag(status, HYB_DEVERR_MISALIGNED);
       continue;
     }
@@ -349,13 +348,11 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
       mbar_init(&bars->b_done, 1);
       mbar_init(&bars->s_read, 128);               // state warps (0-3)
       mbar_init(&bars->s_written, 128);
+      mbar_init(&bars->p_ready, 1);
+      mbar_init(&bars->p_written, 128);            // state warps
       for (int i = 0; i < 2; ++i) {
-        mbar_init(&bars->p_ready[i], 1);
-        mbar_init(&bars->p_written[i], 128);           // state warps
         mbar_init(&bars->o_ready[i], 1);
-        mbar_init(&bars->o_free[i], 128);              // output warps (4-7)
-        mbar_init(&bars->o_staged[i], 128);
-        mbar_init(&bars->o_stage_free[i], 1);
+        mbar_init(&bars->o_free[i], 128);          // output warps (4-7)
       }
       mbar_init(&bars->drain, 1);
       mbar_init(&bars->published, 128);
@@ -369,8 +366,6 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
   tc_fence_after();
   const uint32_t tmem = tmem_base;
   uint8_t* const s_hi = sm + kOffS;
-  uint8_t* const p_tile = sm + kOffP;
-  uint8_t* const o_stage = sm + kOffO;
 
   if (warp == kWarpTma) {
     // ------------------------------------------------------------ TMA warp
@@ -409,28 +404,12 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA warp
-    // Issue order per chunk c: (d)_c, (b)_c, (a)_c, then (c)_{c-1} -- the output update of
-    // the previous chunk goes last so the next state update never waits for P's conversion.
     bool ok = true;
     // descriptors built once; every MMA below adds an offset (see desc_add)
     const uint32_t sm0 = smem_u32(sm);
-    const uint64_t mn0 = sw128_desc(sm0, kSub, 1024);          // MN-major, 64-row sub-tiles
+    const uint64_t mn0 = sw128_desc(sm0, kSub, 1024);          // MN-major: two 64-wide blocks
     const uint64_t km0 = sw128_desc(sm0, 16, 1024);            // K-major
-    const uint64_t st0 = sw128_desc(sm0 + kOffS, 16384, 1024); // S^T (bf16)
-    auto issue_c = [&](int c) {                  // (c) O^T += V^T tril(P)^T of chunk c
-      const int st = c % kNST, pb = c & 1;
-      const uint32_t vo = st * kStage + 2 * kTile, po = kOffP + pb * kSub;
-      if (lane == 0) {
-        tc_fence_after();
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-          tc_mma(tmem + kColO + pb * 64, desc_add(mn0, vo + k * 2048), desc_add(km0, po + k * 32),
-                 kIdescC, 1);
-        tc_commit(&bars->o_ready[pb]);
-        tc_commit(&bars->empty[st]);
-      }
-      __syncwarp();
-    };
+    const uint64_t st0 = sw128_desc(sm0 + kOffS, 16384, 1024); // bf16 state (MN-major)
     int c = 0;
     Seg sg;
     while (ok && NEXT_RUN(sg)) {
@@ -453,50 +432,53 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
           fence_async_smem();
         }
         __syncwarp();
+        if (lane == 0) {
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; ++k) {            // (a) P = Q K^T (after (c) of c-1 read P)
+            const uint32_t off = (k >> 2) * kSub + (k & 3) * 32;
+            tc_mma(tmem + kColP, desc_add(km0, qo + off), desc_add(km0, ko + off), kIdescA, k > 0);
+          }
+          tc_commit(&bars->p_ready);
+        }
+        __syncwarp();
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_read, c & 1));   // state of chunk c-1 read
         if (!ok) break;
         if (lane == 0) {
           tc_fence_after();
 #pragma unroll
-          for (int k = 0; k < 4; ++k)              // (d) S += K^T V
-            tc_mma(tmem + kColS, desc_add(mn0, ko + k * 2048), desc_add(mn0, vo + k * 2048),
-                   kIdescD, 1);
+          for (int k = 0; k < 8; ++k)              // (d) S += K^T V
+            tc_mma(tmem + kColS, desc_add(mn0, ko + k * 2048), desc_add(mn0, vo + k * 2048), kIdescD, 1);
           tc_commit(&bars->s_ready);
         }
         if (c >= 2) {
           ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_free[ob], ((c - 2) >> 1) & 1));
           if (!ok) break;
         }
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_written, c & 1));   // bf16 S^T ready
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_written, c & 1));   // bf16 state ready
         if (!ok) break;
         if (lane == 0) {
           tc_fence_after();
-          const uint32_t od = tmem + kColO + ob * 64;
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {            // (b) O^T = S^T Q^T
-            const uint32_t boff = (k >> 2) * kSub + (k & 3) * 32;
-            tc_mma(od, desc_add(st0, k * 2048), desc_add(km0, qo + boff), kIdescB, k != 0);
+          for (int k = 0; k < 8; ++k) {            // (b) O = Q S
+            const uint32_t aoff = (k >> 2) * kSub + (k & 3) * 32;
+            tc_mma(tmem + kColO + ob * 128, desc_add(km0, qo + aoff), desc_add(st0, k * 2048), kIdescB, k != 0);
           }
           tc_commit(&bars->b_done);
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {            // (a) P = Q K^T
-            const uint32_t off = (k >> 2) * kSub + (k & 3) * 32;
-            tc_mma(tmem + kColP + ob * 64, desc_add(km0, qo + off), desc_add(km0, ko + off), kIdescA,
-                   k > 0);
-          }
-          tc_commit(&bars->p_ready[ob]);
         }
         __syncwarp();
-        if (c >= 1) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_written[(c - 1) & 1], ((c - 1) >> 1) & 1));
-          if (!ok) break;
-          issue_c(c - 1);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_written, c & 1));
+        if (!ok) break;
+        if (lane == 0) {
+          tc_fence_after();
+#pragma unroll
+          for (int k = 0; k < 8; ++k)              // (c) O += tril(P) V
+            tc_mma_ta(tmem + kColO + ob * 128, tmem + kColP + k * 8, desc_add(mn0, vo + k * 2048), kIdescC, 1);
+          tc_commit(&bars->o_ready[ob]);
+          tc_commit(&bars->empty[st]);
         }
+        __syncwarp();
       }
-    }
-    if (ok && c > 0) {
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_written[(c - 1) & 1], ((c - 1) >> 1) & 1));
-      if (ok) issue_c(c - 1);
     }
     if (!ok && lane == 0) {                  // let every issued MMA finish before exiting
       flag(status, HYB_DEVERR_TIMEOUT);
@@ -522,6 +504,30 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
       }
       int ci = sg.c0;
       for (int c = 0; have; ++c) {
+        // ---- tril(P) as bf16 pairs over the first 64 columns of P (row t = this lane); (c)
+        // waits for it right after (b), so P goes first
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_ready, c & 1));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll 1
+        for (int half = 0; half < 2; ++half) {           // keys 64 half .. 64 half + 63
+          uint32_t w[32];
+#pragma unroll
+          for (int q2 = 0; q2 < 2; ++q2) {
+            float v[32];
+            tmem_ld32(tl + kColP + half * 64 + q2 * 32, v);
+            tmem_ld_wait();
+            const int tp0 = half * 64 + q2 * 32;
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              w[q2 * 16 + e] = pack_bf16(tp0 + 2 * e <= row ? v[2 * e] : 0.f,
+                                         tp0 + 2 * e + 1 <= row ? v[2 * e + 1] : 0.f);
+          }
+          tmem_st32u(tl + kColP + half * 32, w);         // reads of these columns are done
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(&bars->p_written);
         // ---- new state: read it from TMEM; write the bf16 copy once (b) has used the old one
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->s_ready, c & 1));
         if (!ok) break;
@@ -580,93 +586,34 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
         }
         tc_fence_before();
         mbar_arrive(&bars->s_written);
-        // ---- tril(P) -> shared (K-major [t][t']), buffer c & 1
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_ready[c & 1], (c >> 1) & 1));
-        if (!ok) break;
-        tc_fence_after();
-        {
-          uint8_t* const pt = p_tile + (c & 1) * kSub;
-#pragma unroll 1
-          for (int hf = 0; hf < 2; ++hf) {
-            float v[32];
-            tmem_ld32(tl + kColP + (c & 1) * 64 + hf * 32, v);
-            tmem_ld_wait();
-            if (lane < 16) {
-              const int t = quarter * 16 + lane;         // M = 64 layout: lanes 0..15 of each quarter
-#pragma unroll
-              for (int ch = 0; ch < 4; ++ch) {
-                uint32_t wp[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int tp = hf * 32 + ch * 8 + 2 * e;
-                  wp[e] = pack_bf16(tp <= t ? v[ch * 8 + 2 * e] : 0.f, tp + 1 <= t ? v[ch * 8 + 2 * e + 1] : 0.f);
-                }
-                *reinterpret_cast<uint4*>(pt + sw128_off(t, hf * 4 + ch)) = make_uint4(wp[0], wp[1], wp[2], wp[3]);
-              }
-            }
-          }
-        }
-        fence_async_smem();
-        tc_fence_before();
-        mbar_arrive(&bars->p_written[c & 1]);
       }
     } else {
-      // O^T of chunk c -> global: this thread owns value dim j = row, all 64 tokens. Full
-      // chunks go through staging buffer f & 1 (f counts full chunks) and a TMA store issued
-      // by one thread; before a buffer is written again, that thread has seen the store that
-      // used it read it.
-      const bool issuer = warp == 4 && lane == 0;
-      int c = 0, f = 0;
+      // O of chunk c -> global: this thread owns token row t = row, all 128 value columns
+      int c = 0;
       Seg sg;
       while (ok && NEXT_RUN(sg)) {
         for (int ci = sg.c0; ci < sg.c1; ++ci, ++c) {
           ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_ready[c & 1], (c >> 1) & 1));
           if (!ok) break;
           tc_fence_after();
-          float v[64];
-          tmem_ld32(tl + kColO + (c & 1) * 64, v);
-          tmem_ld32(tl + kColO + (c & 1) * 64 + 32, v + 32);
-          tmem_ld_wait();
+          uint32_t w[64];
+#pragma unroll
+          for (int part = 0; part < 4; ++part) {
+            float v[32];
+            tmem_ld32(tl + kColO + (c & 1) * 128 + part * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) w[part * 16 + e] = pack_bf16(v[2 * e], v[2 * e + 1]);
+          }
           tc_fence_before();
-          mbar_arrive(&bars->o_free[c & 1]);               // TMEM buffer free for (b) of c + 2
-          const int z = sg.t0 + ci * kC;
-          const int nvalid = min(kC, sg.n - ci * kC);
-          if (nvalid < kC) {                               // partial chunk: direct stores
-            __nv_bfloat16* o = out + ((int64_t)z * H + sg.h) * kD + row;
-            const int64_t step = (int64_t)H * kD;          // one token further
+          mbar_arrive(&bars->o_free[c & 1]);             // TMEM buffer free for (b) of c + 2
+          if (row < min(kC, sg.n - ci * kC)) {
+            uint4* o = reinterpret_cast<uint4*>(out + ((int64_t)(sg.t0 + ci * kC + row) * H + sg.h) * kD);
 #pragma unroll
-            for (int e = 0; e < 64; ++e) {
-              if (e < nvalid) *o = __float2bfloat16_rn(v[e]);
-              o += step;
-            }
-            continue;
+            for (int e = 0; e < 16; ++e) o[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
           }
-          const int sb = f & 1;
-          if (f >= 2) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_stage_free[sb], ((f - 2) >> 1) & 1));
-            if (!ok) break;
-          }
-          // staging tile: two [64 tokens][64 j] SW128 sub-tiles (j halves), row = token; this
-          // thread's j sits in 16-byte chunk (j & 63) / 8 at byte (j & 7) * 2
-          uint8_t* const ob = o_stage + sb * kTile + (row >> 6) * kSub + (row & 7) * 2;
-          const uint32_t jc = (row & 63) >> 3;
-#pragma unroll
-          for (int t = 0; t < 64; ++t)
-            *reinterpret_cast<__nv_bfloat16*>(ob + sw128_off(t, jc)) = __float2bfloat16_rn(v[t]);
-          fence_async_smem();
-          mbar_arrive(&bars->o_staged[sb]);
-          if (issuer) {
-            if (!mbar_wait(&bars->o_staged[sb], (f >> 1) & 1)) { ok = false; break; }
-            tma_store_3d(&to, o_stage + sb * kTile, 0, sg.h, z);
-            tma_store_3d(&to, o_stage + sb * kTile + kSub, 64, sg.h, z);
-            bulk_commit();
-            bulk_wait_read<1>();                           // the previous chunk's store has read
-            if (f >= 1) mbar_arrive(&bars->o_stage_free[sb ^ 1]);
-          }
-          ++f;
         }
       }
-      if (issuer) bulk_wait<0>();                        // every store complete before exit
     }
     if (!ok && lane == 0) flag(status, HYB_DEVERR_TIMEOUT);
   }
@@ -680,7 +627,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
 }  // namespace
 
 bool linear_prefill_tc_supported(int dtype, int D, int C) {
-  return dtype == HYB_BF16 && D == kD && C == kC;
+  return dtype == HYB_BF16 && D == kD && C == kAlign;
 }
 
 cudaError_t launch_linear_prefill_tc(void* out, const void* q, const void* k, const void* v,
@@ -691,14 +638,13 @@ cudaError_t launch_linear_prefill_tc(void* out, const void* q, const void* k, co
   (void)max_len;
   (void)C;
   if (B == 0) return cudaSuccess;
-  CUtensorMap mq, mk, mv, mo;
+  CUtensorMap mq, mk, mv;
   const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)H, (uint64_t)(T > 0 ? T : 1)};
   const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)H * kD * 2};
   const uint32_t box[3] = {64, 1, (uint32_t)kC};
   if (!encode_tmap_bf16(&mq, q, 3, dims, strides, box) ||
       !encode_tmap_bf16(&mk, k, 3, dims, strides, box) ||
-      !encode_tmap_bf16(&mv, v, 3, dims, strides, box) ||
-      !encode_tmap_bf16(&mo, out, 3, dims, strides, box))
+      !encode_tmap_bf16(&mv, v, 3, dims, strides, box))
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem((const void*)linear_prefill_tc_kernel, kSmem);
   if (e != cudaSuccess) return e;
@@ -719,7 +665,7 @@ cudaError_t launch_linear_prefill_tc(void* out, const void* q, const void* k, co
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, linear_prefill_tc_kernel, mq, mk, mv, mo,
+  e = cudaLaunchKernelEx(&cfg, linear_prefill_tc_kernel, mq, mk, mv,
                          static_cast<__nv_bfloat16*>(out), cu, ctx, pool, NS, slots, reset, B, H,
                          status);
   count_launch();
