@@ -44,6 +44,8 @@ namespace {
 constexpr int kC = 128, kD = 128;            // chunk rows, head dim
 constexpr int kAlign = 64;                   // chunk size of the interface: call starts align to it
 constexpr int kNST = 2;                      // Q/K/V ring stages
+constexpr int kBoxRows = 16;                 // rows per TMA box; both column halves of a row
+                                             // group are requested back to back
 constexpr int kSub = 128 * 128;              // bytes of one [128 rows][64 cols] SW128 sub-tile
 constexpr int kTile = 2 * kSub;              // [128][128] bf16 tile
 constexpr int kStage = 3 * kTile;            // Q, K, V
@@ -389,11 +391,13 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
           uint64_t* bar = &bars->full[st];
           mbar_expect_tx(bar, kStage);
           const int z = sg.t0 + ci * kC;
-          for (int sb = 0; sb < 2; ++sb) {
-            tma_load_3d(q + sb * kSub, &tq, sb * 64, sg.h, z, bar);
-            tma_load_3d(q + kTile + sb * kSub, &tk, sb * 64, sg.h, z, bar);
-            tma_load_3d(q + 2 * kTile + sb * kSub, &tv, sb * 64, sg.h, z, bar);
-          }
+          for (int r0 = 0; r0 < kC; r0 += kBoxRows)
+            for (int sb = 0; sb < 2; ++sb) {
+              const int o = sb * kSub + r0 * 128;
+              tma_load_3d(q + o, &tq, sb * 64, sg.h, z + r0, bar);
+              tma_load_3d(q + kTile + o, &tk, sb * 64, sg.h, z + r0, bar);
+              tma_load_3d(q + 2 * kTile + o, &tv, sb * 64, sg.h, z + r0, bar);
+            }
         }
       }
     }
@@ -641,7 +645,7 @@ cudaError_t launch_linear_prefill_tc(void* out, const void* q, const void* k, co
   CUtensorMap mq, mk, mv;
   const uint64_t dims[3] = {(uint64_t)kD, (uint64_t)H, (uint64_t)(T > 0 ? T : 1)};
   const uint64_t strides[2] = {(uint64_t)kD * 2, (uint64_t)H * kD * 2};
-  const uint32_t box[3] = {64, 1, (uint32_t)kC};
+  const uint32_t box[3] = {64, 1, (uint32_t)kBoxRows};
   if (!encode_tmap_bf16(&mq, q, 3, dims, strides, box) ||
       !encode_tmap_bf16(&mk, k, 3, dims, strides, box) ||
       !encode_tmap_bf16(&mv, v, 3, dims, strides, box))
