@@ -760,44 +760,67 @@ def bench_ours(args, dist):
     h_all_np = h_all.numpy()
     for n, a in host_arrays.items():
         h_all_np[offs[n]:offs[n] + a.nbytes] = np.ascontiguousarray(a).view(np.uint8).reshape(-1)
-    d_all = torch.empty(total, dtype=torch.uint8, device=device)
-
-    def dview(n):
-        a = host_arrays[n]
-        t = d_all[offs[n]:offs[n] + a.nbytes]
-        t = t.view(torch.bfloat16) if a.dtype == np.uint16 else t.view(getattr(torch, a.dtype.name))
-        return t.view(a.shape)
-
-    d_in = {n: dview(n) for n in wl["host"]}
-    d_meta = {n: dview(n) for n in ("lens", "bt", "ctx", "slots", "cu")}
-    out_all = torch.empty(2 * B * H * D, dtype=torch.bfloat16, device=device)
-    e_out_f, e_out_l = out_all[:B * H * D].view(B, H, D), out_all[B * H * D:].view(B, H, D)
-    h_out = torch.empty(2 * B * H * D, dtype=torch.int16).pin_memory()
     h2d = sum(a.nbytes for a in host_arrays.values())
-    d2h = h_out.numel() * h_out.element_size()
-    meta = hyb.batch_meta(B, B, seq_lens=d_meta["lens"], block_tables=d_meta["bt"], slot_mapping=slot,
-                          state_slots=d_meta["slots"], max_seq_len=msl)
-    ios = [hyb.layer_io(e_out_f, d_in["qf"], d_in["kf"], d_in["vf"], wl["kc"], wl["vc"]),
-           hyb.layer_io(e_out_l, d_in["ql"], d_in["kl"], d_in["vl"], state_pool=wl["state"], num_state_slots=B)]
+    # Two sets of device buffers: step s copies its inputs into set s % 2 on a copy stream
+    # while the compute stream still runs step s - 1, and reads its outputs back while step
+    # s + 1 computes (the pipelining a serving loop does).
+    sets = []
+    for _ in range(2):
+        d_all = torch.empty(total, dtype=torch.uint8, device=device)
 
-    def e2e_step():
-        d_all.copy_(h_all, non_blocking=True)
-        hyb.check(hyb.hyb_slot_mapping(slot, d_meta["bt"], d_meta["cu"], d_meta["ctx"], B, B, d, sh))
-        hyb.check(hyb.hyb_layer_dispatch([0, 1], 2, 0, ios, meta, d, 64, ws, ws_n, sh))
-        h_out.copy_(out_all.view(torch.int16), non_blocking=True)
+        def dview(n, d_all=d_all):
+            a = host_arrays[n]
+            t = d_all[offs[n]:offs[n] + a.nbytes]
+            t = t.view(torch.bfloat16) if a.dtype == np.uint16 else t.view(getattr(torch, a.dtype.name))
+            return t.view(a.shape)
+
+        d_in = {n: dview(n) for n in wl["host"]}
+        d_meta = {n: dview(n) for n in ("lens", "bt", "ctx", "slots", "cu")}
+        out_all = torch.empty(2 * B * H * D, dtype=torch.bfloat16, device=device)
+        e_out_f, e_out_l = out_all[:B * H * D].view(B, H, D), out_all[B * H * D:].view(B, H, D)
+        meta = hyb.batch_meta(B, B, seq_lens=d_meta["lens"], block_tables=d_meta["bt"], slot_mapping=slot,
+                              state_slots=d_meta["slots"], max_seq_len=msl)
+        ios = [hyb.layer_io(e_out_f, d_in["qf"], d_in["kf"], d_in["vf"], wl["kc"], wl["vc"]),
+               hyb.layer_io(e_out_l, d_in["ql"], d_in["kl"], d_in["vl"], state_pool=wl["state"],
+                            num_state_slots=B)]
+        sets.append(dict(d_all=d_all, d_meta=d_meta, out_all=out_all, meta=meta, ios=ios,
+                         h_out=torch.empty(2 * B * H * D, dtype=torch.int16).pin_memory(),
+                         loaded=torch.cuda.Event(), computed=torch.cuda.Event(), read=torch.cuda.Event()))
+    d2h = sets[0]["h_out"].numel() * sets[0]["h_out"].element_size()
+    h2d_stream = torch.cuda.Stream(device=device)   # one stream per direction: a read-back
+    d2h_stream = torch.cuda.Stream(device=device)   # must not hold up the next step's inputs
+
+    def e2e_step(i):
+        st = sets[i % 2]
+        if i >= 2:
+            h2d_stream.wait_event(st["read"])        # step i - 2's outputs are back (so it is done)
+        with torch.cuda.stream(h2d_stream):
+            st["d_all"].copy_(h_all, non_blocking=True)
+            st["loaded"].record(h2d_stream)
+        stream.wait_event(st["loaded"])
+        hyb.check(hyb.hyb_slot_mapping(slot, st["d_meta"]["bt"], st["d_meta"]["cu"], st["d_meta"]["ctx"], B, B, d, sh))
+        hyb.check(hyb.hyb_layer_dispatch([0, 1], 2, 0, st["ios"], st["meta"], d, 64, ws, ws_n, sh))
+        st["computed"].record(stream)
+        d2h_stream.wait_event(st["computed"])
+        with torch.cuda.stream(d2h_stream):
+            st["h_out"].copy_(st["out_all"].view(torch.int16), non_blocking=True)
+            st["read"].record(d2h_stream)
 
     e2e_steps = max(10, min(args.steps, 500))
     with torch.cuda.stream(stream):
-        for _ in range(3):
-            e2e_step()
-        stream.synchronize()
+        for i in range(3):
+            e2e_step(i)
+        torch.cuda.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         dist.barrier()
         e0.record(stream)
-        for _ in range(e2e_steps):
-            e2e_step()
+        h2d_stream.wait_event(e0)                # no copy of the timed steps starts before e0
+        for i in range(e2e_steps):
+            e2e_step(i)
+        for st in sets:                          # the last steps' outputs are on the host
+            stream.wait_event(st["read"])
         e1.record(stream)
-        stream.synchronize()
+        torch.cuda.synchronize()
     e2e_ms = dist.max(e0.elapsed_time(e1) / e2e_steps)
     e2e_val = units / (e2e_ms * 1e-3)
 
@@ -830,7 +853,8 @@ def bench_ours(args, dist):
         "roofline": roofline, "ops": ops,
         "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
-                "path": "hyb_slot_mapping + hyb_layer_dispatch; inputs in one pinned buffer, one copy each way"},
+                "path": "hyb_slot_mapping + hyb_layer_dispatch; inputs in one pinned buffer, one copy each way, "
+                        "on copy streams double-buffered against the compute stream"},
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
