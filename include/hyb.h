@@ -140,6 +140,29 @@ hyb_status_t hyb_paged_attn_decode(void* out, const void* q, const void* k_cache
                                    void* stream);
 
 /* -------------------------------------------------------------------------
+ * Decode step with the KV append fused in: one launch does what hyb_paged_kv_append(k, v,
+ * slot_mapping, T = B, ...) followed by hyb_paged_attn_decode(...) do, for a decode batch
+ * (one new token per request, row b of k/v/q). The pages pair the two: the new token's K
+ * and V are written into the paged cache [KV §2.1] and the decode attends over the cache
+ * including them [KV §2.3]; fusing them removes one launch per Full layer and step.
+ * - k, v: [B][H][D] this step's rows; slot_mapping: int64 [B], the cache slot of request b's
+ *   new row (-1: none), as hyb_slot_mapping gives it for position seq_lens[b] - 1.
+ * - Caches are written (only at those slots); everything else is as hyb_paged_attn_decode,
+ *   with the same workspace. A slot >= num_blocks * block_size sets HYB_DEVERR_BAD_SLOT and
+ *   that row is not written.
+ * - The result is bit-identical to the two calls when slot_mapping[b] is -1 or the slot of
+ *   position seq_lens[b] - 1. Any other slot still receives the row, but the attention of
+ *   that step does not see it there.
+ * ------------------------------------------------------------------------- */
+hyb_status_t hyb_paged_attn_decode_append(void* out, const void* q, const void* k,
+                                          const void* v, const int64_t* slot_mapping,
+                                          void* k_cache, void* v_cache,
+                                          const int32_t* block_tables, const int32_t* seq_lens,
+                                          int32_t B, int32_t max_seq_len,
+                                          const hyb_attn_dims_t* d, void* workspace,
+                                          size_t ws_bytes, void* stream);
+
+/* -------------------------------------------------------------------------
  * Paged decode without a workspace. The pages have no counterpart to this entry point:
  * it exists for callers that cannot allocate device memory -- a runtime whose device
  * memory is all assigned by its own planner and that gives an op only its input and
@@ -256,8 +279,8 @@ hyb_status_t hyb_linear_attn_chunked_prefill(void* out, const void* q, const voi
  * layer_types (host, [L]) holds HYB_FULL / HYB_LINEAR / HYB_SLIDING. layers (host, [L]) gives
  * each layer's own buffers; meta (host struct of device pointers) is shared by all
  * layers of the batch. Layers run in order on `stream`:
- *   decode  (mode 0): FULL   -> hyb_paged_kv_append(k, v @ slot_mapping) +
- *                               hyb_paged_attn_decode(seq_lens)
+ *   decode  (mode 0): FULL   -> hyb_paged_attn_decode_append(k, v @ slot_mapping,
+ *                               seq_lens): the append and the decode in one launch
  *                     LINEAR -> hyb_linear_attn_step(state_slots)
  *   prefill (mode 1): FULL   -> hyb_paged_kv_append + hyb_paged_attn_prefill_causal
  *                     LINEAR -> hyb_linear_attn_chunked_prefill(reset, chunk_size)

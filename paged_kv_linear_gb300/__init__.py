@@ -64,6 +64,7 @@ def _load():
         "hyb_paged_attn_decode_workspace_size": ([i32, i32, p], sz),
         "hyb_paged_attn_decode": [p, p, p, p, p, p, i32, i32, p, p, sz, p],
         "hyb_paged_attn_decode_noalloc": [p, p, p, p, p, p, i32, i32, p, p],
+        "hyb_paged_attn_decode_append": [p, p, p, p, p, p, p, p, p, i32, i32, p, p, sz, p],
         "hyb_paged_attn_prefill_causal": [p, p, p, p, p, p, p, i32, i32, i32, p, p],
         "hyb_linear_attn_step": [p, p, p, p, p, i32, p, i32, i32, i32, i32, p],
         "hyb_linear_attn_step_lowp": [p, p, p, p, p, i32, i32, p, i32, i32, i32, i32, p],
@@ -168,6 +169,14 @@ def hyb_paged_attn_decode(out, q, k_cache, v_cache, block_tables, seq_lens, B, m
     return _lib.hyb_paged_attn_decode(_p(out), _p(q), _p(k_cache), _p(v_cache), _p(block_tables),
                                       _p(seq_lens), B, max_seq_len, C.byref(d), _p(workspace),
                                       ws_bytes, _s(stream))
+
+
+def hyb_paged_attn_decode_append(out, q, k, v, slot_mapping, k_cache, v_cache, block_tables,
+                                 seq_lens, B, max_seq_len, d, workspace, ws_bytes, stream=None):
+    return _lib.hyb_paged_attn_decode_append(_p(out), _p(q), _p(k), _p(v), _p(slot_mapping),
+                                             _p(k_cache), _p(v_cache), _p(block_tables),
+                                             _p(seq_lens), B, max_seq_len, C.byref(d),
+                                             _p(workspace), ws_bytes, _s(stream))
 
 
 def hyb_paged_attn_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_lens, B,

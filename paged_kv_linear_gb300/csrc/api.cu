@@ -181,13 +181,14 @@ hyb_status_t check_linear_prefill(const void* out, const void* q, const void* k,
 // ---- launches (arguments already checked) -----------------------------------------
 hyb_status_t run_decode(void* out, const void* q, const void* kc, const void* vc,
                         const int32_t* bt, const int32_t* seq_lens, int B, int max_seq_len,
-                        const hyb_attn_dims_t* d, void* ws, unsigned* status, cudaStream_t s) {
+                        const hyb_attn_dims_t* d, void* ws, unsigned* status, cudaStream_t s,
+                        const DecodeAppend* app = nullptr) {
   if (B == 0) return HYB_OK;
   const DecodePlan p = plan_decode(B, d->num_heads, d->head_dim, max_seq_len, d->window);
   return cuda_status(launch_paged_decode(out, q, kc, vc, bt, seq_lens, nullptr, nullptr, B, 0,
                                          d->num_heads, d->head_dim, d->dtype, d->num_blocks,
                                          d->max_blocks_per_seq, d->block_size, max_seq_len,
-                                         d->scale, d->window, p, ws, status, s));
+                                         d->scale, d->window, p, ws, status, s, app));
 }
 
 hyb_status_t run_prefill(void* out, const void* q, const void* kc, const void* vc,
@@ -273,6 +274,25 @@ hyb_status_t hyb_paged_attn_decode(void* out, const void* q, const void* k_cache
   if (!sw) return HYB_ERR_CUDA;
   return run_decode(out, q, k_cache, v_cache, block_tables, seq_lens, B, max_seq_len, d,
                     workspace, sw, (cudaStream_t)stream);
+}
+
+hyb_status_t hyb_paged_attn_decode_append(void* out, const void* q, const void* k,
+                                          const void* v, const int64_t* slot_mapping,
+                                          void* k_cache, void* v_cache,
+                                          const int32_t* block_tables, const int32_t* seq_lens,
+                                          int32_t B, int32_t max_seq_len,
+                                          const hyb_attn_dims_t* d, void* workspace,
+                                          size_t ws_bytes, void* stream) {
+  hyb_status_t st = check_append(k, v, slot_mapping, B, k_cache, v_cache, d);
+  if (st != HYB_OK) return st;
+  st = check_decode(out, q, k_cache, v_cache, block_tables, seq_lens, B, max_seq_len, d,
+                    workspace, ws_bytes);
+  if (st != HYB_OK || B == 0) return st;
+  unsigned* sw = status_word();
+  if (!sw) return HYB_ERR_CUDA;
+  const DecodeAppend app{k, v, slot_mapping};
+  return run_decode(out, q, k_cache, v_cache, block_tables, seq_lens, B, max_seq_len, d,
+                    workspace, sw, (cudaStream_t)stream, &app);
 }
 
 hyb_status_t hyb_paged_attn_prefill_causal(void* out, const void* q, const void* k_cache,
@@ -391,15 +411,18 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
     if (layer_types[l] == HYB_FULL || layer_types[l] == HYB_SLIDING) {
       hyb_attn_dims_t dl = *d;
       dl.window = io.window;
-      st = cuda_status(launch_kv_append(io.k, io.v, meta->slot_mapping, T, H, D, esize_of(dt),
-                                        d->num_blocks, d->block_size, io.k_cache, io.v_cache, sw,
-                                        s));
-      if (st != HYB_OK) return st;
-      st = mode == HYB_MODE_DECODE
-               ? run_decode(io.out, io.q, io.k_cache, io.v_cache, meta->block_tables,
-                            meta->seq_lens, B, meta->max_seq_len, &dl, workspace, sw, s)
-               : run_prefill(io.out, io.q, io.k_cache, io.v_cache, meta->block_tables,
-                             meta->cu_q_lens, meta->ctx_lens, B, T, meta->max_q_len, &dl, sw, s);
+      if (mode == HYB_MODE_DECODE) {         // append fused into the decode launch
+        const DecodeAppend app{io.k, io.v, meta->slot_mapping};
+        st = run_decode(io.out, io.q, io.k_cache, io.v_cache, meta->block_tables, meta->seq_lens,
+                        B, meta->max_seq_len, &dl, workspace, sw, s, &app);
+      } else {
+        st = cuda_status(launch_kv_append(io.k, io.v, meta->slot_mapping, T, H, D, esize_of(dt),
+                                          d->num_blocks, d->block_size, io.k_cache, io.v_cache,
+                                          sw, s));
+        if (st != HYB_OK) return st;
+        st = run_prefill(io.out, io.q, io.k_cache, io.v_cache, meta->block_tables,
+                         meta->cu_q_lens, meta->ctx_lens, B, T, meta->max_q_len, &dl, sw, s);
+      }
     } else {
       st = mode == HYB_MODE_DECODE
                ? cuda_status(launch_linear_step(io.out, io.q, io.k, io.v, io.state_pool,

@@ -100,12 +100,14 @@ struct DecodeShape {
 // WINDOW = false compiles the lower key bound away (window must then be 0).
 template <typename T, int D, bool PREFILL, bool WINDOW>
 __global__ void __launch_bounds__(kNW * 32)
-paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __restrict__ kc,
-                    const T* __restrict__ vc, const int32_t* __restrict__ bt,
+paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict__ kc,
+                    T* __restrict__ vc, const int32_t* __restrict__ bt,
                     const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ cu,
                     const int32_t* __restrict__ ctx, int max_q, int H, int NB, int MB,
                     int rsh, int max_len, float scale_log2, int window, int max_splits,
-                    float* __restrict__ ws_acc, float2* __restrict__ ws_ml, unsigned* status) {
+                    float* __restrict__ ws_acc, float2* __restrict__ ws_ml,
+                    const T* __restrict__ k_new, const T* __restrict__ v_new,
+                    const int64_t* __restrict__ slot_map, unsigned* status) {
   using E = Elt<T>;
   using S = DecodeShape<T, D>;
   constexpr int VEC = S::VEC, LPR = S::LPR, TPI = S::TPI, ITER = S::ITER, TILE = S::TILE;
@@ -135,6 +137,42 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
 
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int32_t* btrow = bt + (int64_t)b * MB;
+  const int sub_mask = (1 << rsh) - 1;
+  const int64_t head_off = (int64_t)h * (kBlockSize << rsh) * D;
+  const int64_t blk_stride = (int64_t)H * (kBlockSize << rsh) * D;
+  constexpr int kRowChunks = D * (int)sizeof(T) / 16;   // 16-byte pieces of one K or V row
+
+  // Append fused into the decode: the last split of (r, h) stores this step's k/v row at
+  // slot_map[r]; when that slot is the one of position n - 1 (the normal decode step), the
+  // warp that loads that position's tile also patches the row into shared memory, so the
+  // attention sees exactly what an append followed by the decode would.
+  int patch_sub = -1;                      // 16-token sub-tile holding position n - 1, if patched
+  if (!PREFILL && k_new && split == nsplit - 1) {
+    int64_t slot = slot_map[r];
+    const int bsz = kBlockSize << rsh;
+    if (slot >= (int64_t)NB * bsz) {
+      if (threadIdx.x == 0) flag(status, HYB_DEVERR_BAD_SLOT);
+      slot = -1;
+    }
+    if (slot >= 0) {
+      if (warp == kNW - 1) {
+        const int64_t blk = slot / bsz, off = slot - blk * bsz;
+        const int64_t dst = ((blk * H + h) * bsz + off) * D;
+        const int64_t src = ((int64_t)r * H + h) * D;
+        for (int e = lane; e < kRowChunks; e += 32) {
+          reinterpret_cast<uint4*>(kc + dst)[e] = reinterpret_cast<const uint4*>(k_new + src)[e];
+          reinterpret_cast<uint4*>(vc + dst)[e] = reinterpret_cast<const uint4*>(v_new + src)[e];
+        }
+      }
+      if (n >= 1) {
+        const int s_last = (n - 1) / kBlockSize;
+        const int pb = btrow[s_last >> rsh];
+        if (pb >= 0 && pb < NB && slot == (int64_t)pb * bsz + (n - 1) % bsz) patch_sub = s_last;
+      }
+    }
+  }
+
   uint8_t* ring = smem + (size_t)warp * kNST * 2 * TILE;
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + (size_t)kNW * kNST * 2 * TILE) + warp * kNST;
   float* red_acc = reinterpret_cast<float*>(smem + (size_t)kNW * kNST * 2 * TILE + kNW * kNST * 8);
@@ -152,10 +190,6 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
   const int first = blk_begin + warp;   // this warp's logical blocks: first + i*kNW
   const int ntiles = first < blk_end ? (blk_end - first + kNW - 1) / kNW : 0;
   // 16-token sub-tile s lives in block btrow[s >> rsh], rows (s & sub_mask) * 16 onwards
-  const int32_t* btrow = bt + (int64_t)b * MB;
-  const int sub_mask = (1 << rsh) - 1;
-  const int64_t head_off = (int64_t)h * (kBlockSize << rsh) * D;
-  const int64_t blk_stride = (int64_t)H * (kBlockSize << rsh) * D;
 
   if (lane == 0) {
 #pragma unroll
@@ -198,6 +232,17 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __res
       const T* Ks = reinterpret_cast<const T*>(ring + st * 2 * TILE);
       const T* Vs = reinterpret_cast<const T*>(ring + st * 2 * TILE + TILE);
       const int tok0 = (first + i * kNW) * kBlockSize;
+      if (first + i * kNW == patch_sub) {  // this step's row, straight from the inputs
+        const int row = (n - 1) % kBlockSize;
+        const int64_t src = ((int64_t)r * H + h) * D;
+        uint4* kd = reinterpret_cast<uint4*>(ring + st * 2 * TILE) + row * kRowChunks;
+        uint4* vd = reinterpret_cast<uint4*>(ring + st * 2 * TILE + TILE) + row * kRowChunks;
+        for (int e = lane; e < kRowChunks; e += 32) {
+          kd[e] = reinterpret_cast<const uint4*>(k_new + src)[e];
+          vd[e] = reinterpret_cast<const uint4*>(v_new + src)[e];
+        }
+        __syncwarp();
+      }
       float s[ITER];
       float mt = -INFINITY;
 #pragma unroll
@@ -358,12 +403,12 @@ cudaError_t launch_typed(void* out, const void* q, const void* kc, const void* v
                          const int32_t* bt, const int32_t* seq_lens, const int32_t* cu,
                          const int32_t* ctx, int R, int max_q, int H, int NB, int MB,
                          int bs, int max_len, float scale, int window, const DecodePlan& plan,
-                         void* ws, unsigned* status, cudaStream_t s) {
+                         void* ws, unsigned* status, cudaStream_t s, const DecodeAppend* app) {
   using Sh = DecodeShape<T, D>;
   const bool prefill = cu != nullptr, win = window > 0;
-  using K = void (*)(T*, const T*, const T*, const T*, const int32_t*, const int32_t*,
-                     const int32_t*, const int32_t*, int, int, int, int, int, int, float, int,
-                     int, float*, float2*, unsigned*);
+  using K = void (*)(T*, const T*, T*, T*, const int32_t*, const int32_t*, const int32_t*,
+                     const int32_t*, int, int, int, int, int, int, float, int, int, float*,
+                     float2*, const T*, const T*, const int64_t*, unsigned*);
   const int rsh = log2_int(bs / kBlockSize);
   const K kern = prefill ? (win ? paged_decode_kernel<T, D, true, true>
                                 : paged_decode_kernel<T, D, true, false>)
@@ -377,9 +422,12 @@ cudaError_t launch_typed(void* out, const void* q, const void* kc, const void* v
       static_cast<char*>(ws) + (size_t)R * H * max_splits * D * sizeof(float));
   dim3 grid(prefill ? R * max_q : R, H, max_splits);
   const float scale_log2 = scale * 1.4426950408889634f;
-  e = launch_pdl(kern, grid, dim3(kNW * 32), Sh::SMEM, s, (T*)out, (const T*)q, (const T*)kc,
-                 (const T*)vc, bt, seq_lens, cu, ctx, max_q, H, NB, MB, rsh, max_len, scale_log2,
-                 window, max_splits, ws_acc, ws_ml, status);
+  const bool fused = app != nullptr && !prefill;
+  e = launch_pdl(kern, grid, dim3(kNW * 32), Sh::SMEM, s, (T*)out, (const T*)q, (T*)kc, (T*)vc,
+                 bt, seq_lens, cu, ctx, max_q, H, NB, MB, rsh, max_len, scale_log2, window,
+                 max_splits, ws_acc, ws_ml, fused ? (const T*)app->k : (const T*)nullptr,
+                 fused ? (const T*)app->v : (const T*)nullptr,
+                 fused ? app->slot : (const int64_t*)nullptr, status);
   count_launch();
   if (e != cudaSuccess || max_splits == 1) return e;
   e = launch_pdl(decode_combine_kernel<T, D>, dim3(R, H), dim3(128), 0, s, (T*)out, seq_lens, H,
@@ -413,12 +461,12 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* kc, const 
                                 const int32_t* ctx, int R, int max_q, int H, int D, int dtype,
                                 int NB, int MB, int bs, int max_len, float scale, int window,
                                 const DecodePlan& plan, void* ws, unsigned* status,
-                                cudaStream_t s) {
+                                cudaStream_t s, const DecodeAppend* app) {
   if (R == 0 || (cu && max_q == 0)) return cudaSuccess;
 #define HYB_DEC(T, DD)                                                                       \
   if (D == DD)                                                                               \
     return launch_typed<T, DD>(out, q, kc, vc, bt, seq_lens, cu, ctx, R, max_q, H, NB, MB, bs, \
-                               max_len, scale, window, plan, ws, status, s);
+                               max_len, scale, window, plan, ws, status, s, app);
   if (dtype == HYB_BF16) {
     HYB_DEC(__nv_bfloat16, 16)
     HYB_DEC(__nv_bfloat16, 32)

@@ -61,12 +61,21 @@ bool decode_supported(int dtype, int D);
 // prefill mode (cu != nullptr): R = B requests; query j < max_q of request b is packed row
 // cu[b] + j and attends to ctx[b] + j + 1 keys (no split-K; no workspace).
 // window > 0 keeps the last `window` of those keys.
+// append (decode mode only, may be null): this step's k/v rows [R][H][D] go to the cache
+// at slot[r] (-1: none) inside the decode launch, and the attention sees them; equal to a
+// KV append with the same slots followed by the decode, for slot[r] = -1 or the slot of
+// position seq_lens[r] - 1.
+struct DecodeAppend {
+  const void* k;
+  const void* v;
+  const int64_t* slot;
+};
 cudaError_t launch_paged_decode(void* out, const void* q, const void* kc, const void* vc,
                                 const int32_t* bt, const int32_t* seq_lens, const int32_t* cu,
                                 const int32_t* ctx, int R, int max_q, int H, int D, int dtype,
                                 int NB, int MB, int bs, int max_len, float scale, int window,
                                 const DecodePlan& plan, void* ws, unsigned* status,
-                                cudaStream_t s);
+                                cudaStream_t s, const DecodeAppend* app = nullptr);
 
 bool linear_supported(int dtype, int D);
 // 16-bit state pool (state_dtype HYB_BF16 or HYB_F16), same shapes as launch_linear_step
