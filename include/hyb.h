@@ -348,6 +348,16 @@ const char* hyb_last_cuda_error(void);
  * call with reset != 0 (host-side counter; benchmarks report it). */
 uint64_t hyb_launch_count(int32_t reset);
 
+/* Dispatch trace. With HYB_TRACE set in the environment (to anything but "" or "0"),
+ * hyb_layer_dispatch writes one line per layer to stderr naming the kernels it launches
+ * for that layer, and records a CUDA event before the first layer and after each layer on
+ * the dispatch's stream (not while the stream is being captured into a graph). Events are
+ * created once per host thread and device and reused; no device memory is allocated.
+ * hyb_trace_layer_ms fills ms[0..L0) with each layer's device time in milliseconds for the
+ * last traced dispatch of this thread (L0 layers), waiting for its last event; it returns
+ * HYB_ERR_INVALID_ARG when there is none, when L < L0, or when the current device differs. */
+hyb_status_t hyb_trace_layer_ms(float* ms, int32_t L);
+
 #if defined(__GNUC__)
 #pragma GCC visibility pop
 #endif

@@ -76,6 +76,7 @@ def _load():
         "hyb_status_string": ([i32], C.c_char_p),
         "hyb_last_cuda_error": ([], C.c_char_p),
         "hyb_launch_count": ([i32], u64),
+        "hyb_trace_layer_ms": [p, i32],
     }
     for name, s in sig.items():
         fn = getattr(L, name)
@@ -256,6 +257,14 @@ def hyb_device_status(clear: bool = True):
     flags = C.c_uint32()
     st = _lib.hyb_device_status(C.byref(flags), 1 if clear else 0)
     return int(st), int(flags.value)
+
+
+def hyb_trace_layer_ms(L: int):
+    """Per-layer device times (ms) of this thread's last dispatch traced with HYB_TRACE set;
+    returns (status, list of L floats)."""
+    buf = (C.c_float * max(L, 1))()
+    st = _lib.hyb_trace_layer_ms(buf, L)
+    return int(st), [float(x) for x in buf[:L]]
 
 
 def hyb_launch_count(reset: bool = False) -> int:

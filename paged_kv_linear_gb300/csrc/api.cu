@@ -4,9 +4,12 @@
 
 #include <cmath>
 #include <cstdint>
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 #include <set>
 #include <utility>
+#include <vector>
 
 #include "hyb_internal.cuh"
 
@@ -357,6 +360,63 @@ hyb_status_t hyb_linear_attn_chunked_prefill(void* out, const void* q, const voi
                             (cudaStream_t)stream);
 }
 
+// ---- dispatch trace (HYB_TRACE set in the environment): a line per layer on stderr naming
+// its kernels, and a CUDA event before the first layer and after each layer, kept per host
+// thread so hyb_trace_layer_ms can report the last traced dispatch.
+namespace {
+struct Trace {
+  std::vector<cudaEvent_t> ev;
+  int layers = 0;                          // layers of the last traced dispatch (0: none)
+  int dev = -1;
+};
+thread_local Trace g_trace;
+
+bool trace_on(cudaStream_t s) {
+  const char* e = std::getenv("HYB_TRACE");
+  if (!e || !*e || (e[0] == '0' && !e[1])) return false;
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cs) != cudaSuccess || cs != cudaStreamCaptureStatusNone)
+    return false;                          // not inside a graph capture
+  return true;
+}
+
+// Event i of the current trace (created on first use, on the current device).
+cudaEvent_t trace_event(int i) {
+  const int d = cur_dev();
+  if (d != g_trace.dev) {                  // events belong to a device: start over
+    for (cudaEvent_t e : g_trace.ev) cudaEventDestroy(e);
+    g_trace.ev.clear();
+    g_trace.dev = d;
+  }
+  while ((int)g_trace.ev.size() <= i) {
+    cudaEvent_t e = nullptr;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    g_trace.ev.push_back(e);
+  }
+  return g_trace.ev[i];
+}
+
+const char* layer_kernels(int lt, int mode, const hyb_attn_dims_t* d, int chunk) {
+  if (lt == HYB_LINEAR)
+    return mode == HYB_MODE_DECODE ? "linear_step_kernel"
+           : linear_prefill_tc_supported(d->dtype, d->head_dim, chunk)
+               ? "linear_handoff_epoch_kernel + linear_prefill_tc_kernel"
+               : "linear_prefill_simt_kernel";
+  if (mode == HYB_MODE_DECODE) return "paged_decode_kernel (KV append fused) [+ decode_combine_kernel]";
+  return prefill_tc_supported(d->dtype, d->head_dim) ? "kv_append_kernel + prefill_tc_kernel"
+                                                     : "kv_append_kernel + paged_decode_kernel<prefill>";
+}
+}  // namespace
+
+hyb_status_t hyb_trace_layer_ms(float* ms, int32_t L) {
+  if (!ms || g_trace.layers == 0 || L < g_trace.layers) return HYB_ERR_INVALID_ARG;
+  if (cur_dev() != g_trace.dev) return HYB_ERR_INVALID_ARG;
+  cudaError_t e = cudaEventSynchronize(g_trace.ev[g_trace.layers]);
+  for (int l = 0; e == cudaSuccess && l < g_trace.layers; ++l)
+    e = cudaEventElapsedTime(&ms[l], g_trace.ev[l], g_trace.ev[l + 1]);
+  return cuda_status(e);
+}
+
 hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t mode,
                                 const hyb_layer_io_t* layers, const hyb_batch_meta_t* meta,
                                 const hyb_attn_dims_t* d, int32_t chunk_size, void* workspace,
@@ -405,9 +465,21 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
   unsigned* sw = status_word();
   if (!sw) return HYB_ERR_CUDA;
   cudaStream_t s = (cudaStream_t)stream;
+  const bool trace = trace_on(s);
+  if (trace) {
+    g_trace.layers = 0;
+    cudaEvent_t e0 = trace_event(0);
+    if (!e0 || cudaEventRecord(e0, s) != cudaSuccess) return HYB_ERR_CUDA;
+    std::fprintf(stderr, "hyb: dispatch %s, %d layers, batch %d, %d rows\n",
+                 mode == HYB_MODE_DECODE ? "decode" : "prefill", L, B, T);
+  }
   // 2) run the plan in layer order
   for (int l = 0; l < L; ++l) {
     const hyb_layer_io_t& io = layers[l];
+    if (trace)
+      std::fprintf(stderr, "hyb:   layer %d %s -> %s\n", l,
+                   layer_types[l] == HYB_LINEAR ? "linear" : layer_types[l] == HYB_SLIDING ? "sliding" : "full",
+                   layer_kernels(layer_types[l], mode, d, chunk_size));
     if (layer_types[l] == HYB_FULL || layer_types[l] == HYB_SLIDING) {
       hyb_attn_dims_t dl = *d;
       dl.window = io.window;
@@ -434,7 +506,12 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
                                     s);
     }
     if (st != HYB_OK) return st;
+    if (trace) {
+      cudaEvent_t e = trace_event(l + 1);
+      if (!e || cudaEventRecord(e, s) != cudaSuccess) return HYB_ERR_CUDA;
+    }
   }
+  if (trace) g_trace.layers = L;
   return HYB_OK;
 }
 

@@ -164,3 +164,9 @@ def test_lowp_state_step_arguments(hyb):
     assert hyb.hyb_linear_attn_step_lowp(f, f, f, f, f, hyb.HYB_BF16, 4, f, 2, 4, 48, hyb.HYB_BF16, 0) == hyb.HYB_ERR_UNSUPPORTED
     # B = 0 is a no-op
     assert hyb.hyb_linear_attn_step_lowp(None, None, None, None, None, hyb.HYB_BF16, 4, None, 0, 4, 128, hyb.HYB_BF16, 0) == hyb.HYB_OK
+
+
+def test_trace_without_a_traced_dispatch(hyb):
+    """No dispatch has been traced on this thread: nothing to report (no CUDA call made)."""
+    st, _ = hyb.hyb_trace_layer_ms(4)
+    assert st == hyb.HYB_ERR_INVALID_ARG
