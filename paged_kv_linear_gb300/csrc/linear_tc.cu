@@ -26,14 +26,15 @@
 //   (a) P   = Q_c K_c^T      A = Q, B = K (both K-major), fp32 into TMEM
 //   (c) O  += tril(P) V_c    A = tril(P) as bf16 in TMEM (written over P by the state
 //                            warps), B = V (MN-major)
-// Issue order per chunk: (d)_c, (b)_c, (c)_{c-1}, (a)_c. The tensor core runs them in
-// order, so (a)_c overwrites P only after (c)_{c-1} has read it, and the state warps
-// convert P_c while (d)_{c+1} and (b)_{c+1} run. The state chain is (d) -> read S from
-// TMEM -> next (d): the state warps release the state as soon as it is in their registers
-// ("S read") and write its bf16 copy for (b) once (b) has consumed the previous one ("S
-// written"). O is double-buffered in TMEM; every handshake barrier has one phase in flight
-// at most. Output rows go straight from registers to global memory (one thread per token
-// row of 256 bytes).
+// Issue order per chunk: (a)_c, (d)_c, (b)_c, (c)_c. The state warps convert P_c while
+// (d)_c and (b)_c run, and the chunk's ring stage is released at the end of its own chunk,
+// which gives the next load a whole chunk of lead. The tensor core runs the MMAs in order,
+// so (a)_{c+1} overwrites P only after (c)_c has read it. The state chain is (d) -> read S
+// from TMEM -> next (d): the state warps release the state as soon as it is in their
+// registers ("S read") and write its bf16 copy for (b) once (b) has consumed the previous
+// one ("S written"). O is double-buffered in TMEM; every handshake barrier has one phase in
+// flight at most. Output rows go straight from registers to global memory (one thread per
+// token row of 256 bytes).
 #include <cuda_bf16.h>
 
 #include "tc.cuh"
