@@ -3,8 +3,9 @@
 
 Workload (default, `decode_single_layer`): 32 requests, H=32, D=128, bf16 KV, fp32 linear
 state, seq_lens ~ U{128..4096} with blocks shuffled across a pool; one step = one decode
-token for every request through one Full layer (slot mapping, KV append, split-K paged
-decode) and one Linear layer (in-place state step). Metric: req-tokens/s per layer
+token for every request through one Full layer (KV append at position seq_len - 1 fused
+into the split-K paged decode, plus the split combine) and one Linear layer (in-place state
+step). Metric: req-tokens/s per layer
 = B * layers / step time. Inputs live in HBM before timing; the per-step working set
 (~1.2 GB of KV and 128 MiB of state) is far larger than L2, so no flush is needed.
 
@@ -661,10 +662,7 @@ def bench_ours(args, dist):
     x = {n: bf(a) for n, a in wl["host"].items()}
     bt = dev(db.pool.block_tables)
     lens = dev(db.seq_lens)
-    ctx = dev(db.seq_lens - 1)
-    cu = dev(np.arange(B + 1, dtype=np.int32))
     slots = dev(wl["slots_h"])
-    slot = torch.empty(B, dtype=torch.int64, device=device)
     msl = int(db.seq_lens.max())
     ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, msl, d)
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=device)
@@ -673,19 +671,18 @@ def bench_ours(args, dist):
     stream = torch.cuda.Stream(device=device)
     sh = stream.cuda_stream
     L = 2
-    n_ops = 3
-    names = ["slot_mapping", "paged_decode", "linear_step"]
+    n_ops = 2
+    names = ["paged_decode", "linear_step"]
 
     def step(ev=None):
         if ev: ev[0].record(stream)
-        hyb.check(hyb.hyb_slot_mapping(slot, bt, cu, ctx, B, B, d, sh))
-        if ev: ev[1].record(stream)
-        # Full layer: KV append and paged decode in one launch (plus the split combine)
-        hyb.check(hyb.hyb_paged_attn_decode_append(out_f, x["qf"], x["kf"], x["vf"], slot, wl["kc"], wl["vc"],
+        # Full layer: KV append (at position seq_len - 1 through the block table) and paged
+        # decode in one launch, plus the split combine
+        hyb.check(hyb.hyb_paged_attn_decode_append(out_f, x["qf"], x["kf"], x["vf"], None, wl["kc"], wl["vc"],
                                                    bt, lens, B, msl, d, ws, ws_n, sh))
-        if ev: ev[2].record(stream)
+        if ev: ev[1].record(stream)
         hyb.check(hyb.hyb_linear_attn_step(out_l, x["ql"], x["kl"], x["vl"], wl["state"], B, slots, B, H, D, W.BF16, sh))
-        if ev: ev[3].record(stream)
+        if ev: ev[2].record(stream)
 
     for _ in range(args.warmup):
         step()
@@ -735,7 +732,7 @@ def bench_ours(args, dist):
     tokens = int(db.seq_lens.sum())
     # K+V read, q read, out write, and the new K/V rows read and written into the cache
     alg_bytes = tokens * H * D * 2 * 2 + 2 * B * H * D * 2 + 4 * B * H * D * 2
-    achieved = alg_bytes / (per_op[1] * 1e-3) / 1e9
+    achieved = alg_bytes / (per_op[0] * 1e-3) / 1e9
     trec = traffic_record("paged_decode", "decode.cu")
     roofline = {"kernel": "paged_decode with the KV append fused (split-K + combine)", "bound": "hbm",
                 "achieved": round(achieved, 1),
@@ -745,15 +742,14 @@ def bench_ours(args, dist):
     lin_bytes = B * H * D * D * 4 * 2
     ops = {n: {"ms": round(float(t), 5)} for n, t in zip(names, per_op)}
     ops["paged_decode"]["GB/s"] = round(achieved, 1)
-    ops["linear_step"]["GB/s"] = round(lin_bytes / (per_op[2] * 1e-3) / 1e9, 1)
+    ops["linear_step"]["GB/s"] = round(lin_bytes / (per_op[1] * 1e-3) / 1e9, 1)
     ops["linear_step"]["frac"] = round(ops["linear_step"]["GB/s"] / hbm_peak, 4)
 
     # ---- end to end through the public dispatcher, host buffers, copies timed. All of a
     # step's inputs sit in one pinned host buffer and go over in one copy; both layers'
     # outputs come back in one copy.
     host_arrays = dict(wl["host"])
-    host_arrays.update({"lens": db.seq_lens, "bt": db.pool.block_tables, "ctx": db.seq_lens - 1,
-                        "slots": wl["slots_h"], "cu": np.arange(B + 1, dtype=np.int32)})
+    host_arrays.update({"lens": db.seq_lens, "bt": db.pool.block_tables, "slots": wl["slots_h"]})
     offs, total = {}, 0
     for n, a in host_arrays.items():
         offs[n] = total
@@ -777,11 +773,11 @@ def bench_ours(args, dist):
             return t.view(a.shape)
 
         d_in = {n: dview(n) for n in wl["host"]}
-        d_meta = {n: dview(n) for n in ("lens", "bt", "ctx", "slots", "cu")}
+        d_meta = {n: dview(n) for n in ("lens", "bt", "slots")}
         out_all = torch.empty(2 * B * H * D, dtype=torch.bfloat16, device=device)
         e_out_f, e_out_l = out_all[:B * H * D].view(B, H, D), out_all[B * H * D:].view(B, H, D)
-        meta = hyb.batch_meta(B, B, seq_lens=d_meta["lens"], block_tables=d_meta["bt"], slot_mapping=slot,
-                              state_slots=d_meta["slots"], max_seq_len=msl)
+        meta = hyb.batch_meta(B, B, seq_lens=d_meta["lens"], block_tables=d_meta["bt"],
+                              state_slots=d_meta["slots"], max_seq_len=msl)   # new rows at seq_len - 1 via the table
         ios = [hyb.layer_io(e_out_f, d_in["qf"], d_in["kf"], d_in["vf"], wl["kc"], wl["vc"]),
                hyb.layer_io(e_out_l, d_in["ql"], d_in["kl"], d_in["vl"], state_pool=wl["state"],
                             num_state_slots=B)]
@@ -800,7 +796,6 @@ def bench_ours(args, dist):
             st["d_all"].copy_(h_all, non_blocking=True)
             st["loaded"].record(h2d_stream)
         stream.wait_event(st["loaded"])
-        hyb.check(hyb.hyb_slot_mapping(slot, st["d_meta"]["bt"], st["d_meta"]["cu"], st["d_meta"]["ctx"], B, B, d, sh))
         hyb.check(hyb.hyb_layer_dispatch([0, 1], 2, 0, st["ios"], st["meta"], d, 64, ws, ws_n, sh))
         st["computed"].record(stream)
         d2h_stream.wait_event(st["computed"])
@@ -855,7 +850,7 @@ def bench_ours(args, dist):
         "roofline": roofline, "ops": ops,
         "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
-                "path": "hyb_slot_mapping + hyb_layer_dispatch; inputs in one pinned buffer, one copy each way, "
+                "path": "hyb_layer_dispatch; inputs in one pinned buffer, one copy each way, "
                         "on copy streams double-buffered against the compute stream"},
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),

@@ -146,7 +146,10 @@ hyb_status_t hyb_paged_attn_decode(void* out, const void* q, const void* k_cache
  * and V are written into the paged cache [KV §2.1] and the decode attends over the cache
  * including them [KV §2.3]; fusing them removes one launch per Full layer and step.
  * - k, v: [B][H][D] this step's rows; slot_mapping: int64 [B], the cache slot of request b's
- *   new row (-1: none), as hyb_slot_mapping gives it for position seq_lens[b] - 1.
+ *   new row (-1: none), as hyb_slot_mapping gives it for position seq_lens[b] - 1. NULL
+ *   means exactly that: each row goes to position seq_lens[b] - 1 through the block table
+ *   (nothing when seq_lens[b] = 0 or that block id is invalid), so the step needs no
+ *   separate slot-mapping launch.
  * - Caches are written (only at those slots); everything else is as hyb_paged_attn_decode,
  *   with the same workspace. A slot >= num_blocks * block_size sets HYB_DEVERR_BAD_SLOT and
  *   that row is not written.
@@ -280,7 +283,8 @@ hyb_status_t hyb_linear_attn_chunked_prefill(void* out, const void* q, const voi
  * each layer's own buffers; meta (host struct of device pointers) is shared by all
  * layers of the batch. Layers run in order on `stream`:
  *   decode  (mode 0): FULL   -> hyb_paged_attn_decode_append(k, v @ slot_mapping,
- *                               seq_lens): the append and the decode in one launch
+ *                               seq_lens): the append and the decode in one launch;
+ *                               meta->slot_mapping may be NULL (position seq_lens[b] - 1)
  *                     LINEAR -> hyb_linear_attn_step(state_slots)
  *   prefill (mode 1): FULL   -> hyb_paged_kv_append + hyb_paged_attn_prefill_causal
  *                     LINEAR -> hyb_linear_attn_chunked_prefill(reset, chunk_size)

@@ -286,7 +286,10 @@ hyb_status_t hyb_paged_attn_decode_append(void* out, const void* q, const void* 
                                           int32_t B, int32_t max_seq_len,
                                           const hyb_attn_dims_t* d, void* workspace,
                                           size_t ws_bytes, void* stream) {
-  hyb_status_t st = check_append(k, v, slot_mapping, B, k_cache, v_cache, d);
+  // a null slot_mapping means: position seq_lens[b] - 1 through the block table
+  static const int64_t dummy_slot = 0;
+  hyb_status_t st = check_append(k, v, slot_mapping ? slot_mapping : &dummy_slot, B, k_cache,
+                                 v_cache, d);
   if (st != HYB_OK) return st;
   st = check_decode(out, q, k_cache, v_cache, block_tables, seq_lens, B, max_seq_len, d,
                     workspace, ws_bytes);
@@ -441,7 +444,11 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
         return HYB_ERR_INVALID_ARG;
       hyb_attn_dims_t dl = *d;
       dl.window = io.window;
-      st = check_append(io.k, io.v, meta->slot_mapping, T, io.k_cache, io.v_cache, &dl);
+      static const int64_t dummy_slot = 0;   // decode: a null slot mapping is allowed (see A7)
+      st = check_append(io.k, io.v,
+                        mode == HYB_MODE_DECODE && !meta->slot_mapping ? &dummy_slot
+                                                                       : meta->slot_mapping,
+                        T, io.k_cache, io.v_cache, &dl);
       if (st != HYB_OK) return st;
       st = mode == HYB_MODE_DECODE
                ? check_decode(io.out, io.q, io.k_cache, io.v_cache, meta->block_tables,

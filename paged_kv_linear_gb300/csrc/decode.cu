@@ -149,8 +149,14 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict_
   // attention sees exactly what an append followed by the decode would.
   int patch_sub = -1;                      // 16-token sub-tile holding position n - 1, if patched
   if (!PREFILL && k_new && split == nsplit - 1) {
-    int64_t slot = slot_map[r];
     const int bsz = kBlockSize << rsh;
+    int64_t slot = -1;
+    if (slot_map) {
+      slot = slot_map[r];
+    } else if (n >= 1) {                   // no slot mapping: position n - 1 through the table
+      const int pb = btrow[((n - 1) / kBlockSize) >> rsh];
+      if (pb >= 0 && pb < NB) slot = (int64_t)pb * bsz + (n - 1) % bsz;
+    }
     if (slot >= (int64_t)NB * bsz) {
       if (threadIdx.x == 0) flag(status, HYB_DEVERR_BAD_SLOT);
       slot = -1;

@@ -76,11 +76,14 @@ def test_bad_arguments_rejected_before_launch(hyb):
     need = hyb.hyb_paged_attn_decode_workspace_size(2, 1024, d64)
     assert need > 0
     assert hyb.hyb_paged_attn_decode(fake, fake, fake, fake, fake, fake, 2, 1024, d64, fake, need - 16, 0) == hyb.HYB_ERR_INVALID_ARG
-    # fused append + decode: no slot mapping / misaligned k / K and V the same pool / small workspace
+    # fused append + decode: no k / misaligned k / misaligned slot mapping / K and V the same
+    # pool / small workspace (a null slot mapping is valid: positions from the block table)
     da = lambda k, slot, kc, vc, ws_b: hyb.hyb_paged_attn_decode_append(
         fake, fake, k, fake, slot, kc, vc, fake, fake, 2, 1024, d64, fake, ws_b, 0)
-    assert da(fake, None, fake, fake + 256, need) == hyb.HYB_ERR_INVALID_ARG
+    assert da(None, fake, fake, fake + 256, need) == hyb.HYB_ERR_INVALID_ARG
+    assert da(None, None, fake, fake + 256, need) == hyb.HYB_ERR_INVALID_ARG
     assert da(fake + 2, fake, fake, fake + 256, need) == hyb.HYB_ERR_INVALID_ARG
+    assert da(fake, fake + 4, fake, fake + 256, need) == hyb.HYB_ERR_INVALID_ARG
     assert da(fake, fake, fake, fake, need) == hyb.HYB_ERR_INVALID_ARG
     assert da(fake, fake, fake, fake + 256, need - 16) == hyb.HYB_ERR_INVALID_ARG
     assert hyb.hyb_paged_attn_decode_append(fake, fake, fake, fake, fake, fake, fake + 256, fake, fake, 0, 1,

@@ -97,3 +97,29 @@ def test_dispatch_decode_uses_fused_append_bit_identically(hyb, devstatus):
     assert same_bytes(to_host(out), out_s)
     assert same_bytes(to_host(kcd), kc_s) and same_bytes(to_host(vcd), vc_s)
     assert devstatus() == (0, 0)
+
+
+def test_decode_append_without_slot_mapping(hyb, devstatus):
+    """slot_mapping NULL: each new row goes to position seq_len - 1 through the block table,
+    bit-identical to passing the slots hyb_slot_mapping computes; also through the dispatch."""
+    c = decode_case(740, [1, 16, 17, 500, 2049], 4, 128, W.BF16, block_size=32)
+    out_s, kc_s, vc_s = _run(hyb, c, _slots(c), True)
+    d = c.dims(hyb)
+    lens = c.ctx + 1
+    msl = int(lens.max())
+    ws_n = hyb.hyb_paged_attn_decode_workspace_size(c.B, msl, d)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+    q, k, v = to_dev(c.q), to_dev(c.k), to_dev(c.v)
+    bt, ln = to_dev(c.pool.block_tables), to_dev(lens)
+    for via_dispatch in (False, True):
+        kcd, vcd = to_dev(c.kc), to_dev(c.vc)
+        out = empty_rows((c.B, c.H, c.D), c.dtype)
+        if via_dispatch:
+            meta = hyb.batch_meta(c.B, c.B, seq_lens=ln, block_tables=bt, max_seq_len=msl)
+            hyb.check(hyb.hyb_layer_dispatch([0], 1, 0, [hyb.layer_io(out, q, k, v, kcd, vcd)], meta, d, 64, ws, ws_n))
+        else:
+            hyb.check(hyb.hyb_paged_attn_decode_append(out, q, k, v, None, kcd, vcd, bt, ln, c.B, msl, d, ws, ws_n))
+        torch.cuda.synchronize()
+        assert same_bytes(to_host(out), out_s)
+        assert same_bytes(to_host(kcd), kc_s) and same_bytes(to_host(vcd), vc_s)
+    assert devstatus() == (0, 0)
