@@ -744,6 +744,7 @@ def bench_ours(args, dist):
     ops["paged_decode"]["GB/s"] = round(achieved, 1)
     ops["linear_step"]["GB/s"] = round(lin_bytes / (per_op[1] * 1e-3) / 1e9, 1)
     ops["linear_step"]["frac"] = round(ops["linear_step"]["GB/s"] / hbm_peak, 4)
+    ops["linear_step"]["traffic"] = _traffic("linear_step", "linear.cu")
 
     # ---- end to end through the public dispatcher, host buffers, copies timed. All of a
     # step's inputs sit in one pinned host buffer and go over in one copy; both layers'
