@@ -278,18 +278,15 @@ def row_hybrid_32layer(hyb, device, stream, iters, seed=0):
             ios.append(hyb.layer_io(o, q, k, v, state_pool=sp, num_state_slots=B))
     bt = torch.from_numpy(db.pool.block_tables).to(device)
     lens = torch.from_numpy(db.seq_lens).to(device)
-    ctx = torch.from_numpy(db.seq_lens - 1).to(device)
-    cu = torch.arange(B + 1, dtype=torch.int32, device=device)
     slots = torch.from_numpy(g.permutation(B).astype(np.int32)).to(device)
-    slot = torch.empty(B, dtype=torch.int64, device=device)
     msl = int(db.seq_lens.max())
     ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, msl, d)
     ws = torch.empty(ws_n, dtype=torch.uint8, device=device)
-    meta = hyb.batch_meta(B, B, seq_lens=lens, block_tables=bt, slot_mapping=slot, state_slots=slots, max_seq_len=msl)
+    # no slot mapping: each Full layer appends its new rows at seq_len - 1 via the block table
+    meta = hyb.batch_meta(B, B, seq_lens=lens, block_tables=bt, state_slots=slots, max_seq_len=msl)
     sh = stream.cuda_stream
 
     def step():
-        hyb.check(hyb.hyb_slot_mapping(slot, bt, cu, ctx, B, B, d, sh))
         hyb.check(hyb.hyb_layer_dispatch(lt, 32, 0, ios, meta, d, 64, ws, ws_n, sh))
     hyb.hyb_launch_count(reset=True)
     step()
@@ -588,26 +585,21 @@ def row_bucketing(hyb, device, stream, iters, seed=0):
         lens = db.seq_lens[order]
         bt = torch.from_numpy(np.ascontiguousarray(db.pool.block_tables[order])).to(device)
         ln = torch.from_numpy(lens).to(device)
-        ctx = torch.from_numpy(lens - 1).to(device)
-        cu = torch.arange(n + 1, dtype=torch.int32, device=device)
         slots = torch.from_numpy(np.asarray(order, np.int32)).to(device)
-        slot = torch.empty(n, dtype=torch.int64, device=device)
         msl = int(lens.max())
         ws_n = hyb.hyb_paged_attn_decode_workspace_size(n, msl, d)
         ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=device)
         rows = torch.from_numpy(np.asarray(order, np.int64)).to(device)
         ios = []
-        bufs = [bt, ln, ctx, cu, slots, slot, ws]
+        bufs = [bt, ln, slots, ws]
         for (q, o, kc, vc, sp) in per_layer:
             qb, ob = q[rows].contiguous(), o[rows].contiguous()
             bufs += [qb, ob]
             ios.append(hyb.layer_io(ob, qb, qb, qb, kc, vc) if kc is not None
                        else hyb.layer_io(ob, qb, qb, qb, state_pool=sp, num_state_slots=B))
-        meta = hyb.batch_meta(n, n, seq_lens=ln, block_tables=bt, slot_mapping=slot, state_slots=slots,
-                              max_seq_len=msl)
+        meta = hyb.batch_meta(n, n, seq_lens=ln, block_tables=bt, state_slots=slots, max_seq_len=msl)
 
-        def run():
-            hyb.check(hyb.hyb_slot_mapping(slot, bt, cu, ctx, n, n, d, sh))
+        def run():                         # new rows at seq_len - 1 via the block table
             hyb.check(hyb.hyb_layer_dispatch(lt, len(lt), 0, ios, meta, d, 64, ws, ws_n, sh))
         return run, bufs
 
