@@ -17,7 +17,8 @@
 // of all chunks laid end to end; a chain cut between two CTAs hands its state over through
 // the state pool (see "work split" below). Within a CTA the runs follow one another without
 // draining the pipeline. Warp roles: one TMA warp streams Q/K/V chunks through a 2-stage
-// ring (SW128 tiles, one mbarrier per stage); one MMA warp issues the tensor-core work;
+// ring (SW128 tiles, one "full" mbarrier per stage, one "empty" mbarrier per tile of a
+// stage); one MMA warp issues the tensor-core work;
 // four state warps carry the state and P; four output warps write O. The state lives in
 // TMEM for the whole call and is accumulated in place. Per chunk (M x N x K, all 128):
 //   (d) S  += K_c^T V_c      A = K^T (MN-major), B = V (MN-major)
@@ -27,8 +28,9 @@
 //   (c) O  += tril(P) V_c    A = tril(P) as bf16 in TMEM (written over P by the state
 //                            warps), B = V (MN-major)
 // Issue order per chunk: (a)_c, (d)_c, (b)_c, (c)_c. The state warps convert P_c while
-// (d)_c and (b)_c run, and the chunk's ring stage is released at the end of its own chunk,
-// which gives the next load a whole chunk of lead. The tensor core runs the MMAs in order,
+// (d)_c and (b)_c run. Each tile of the chunk's ring stage is released after its own last
+// MMA (K after (d), Q after (b), V after (c)) and reloaded in that order, so the loads of
+// chunk c+2 start while chunk c is still computing. The tensor core runs the MMAs in order,
 // so (a)_{c+1} overwrites P only after (c)_c has read it. The state chain is (d) -> read S
 // from TMEM -> next (d): the state warps release the state as soon as it is in their
 // registers ("S read") and write its bf16 copy for (b) once (b) has consumed the previous
@@ -65,12 +67,14 @@ constexpr uint32_t kIdescA = idesc_bf16(128, 128, 0, 0);   // Q, K: K-major
 constexpr uint32_t kIdescC = idesc_bf16(128, 128, 0, 1);   // tril(P) from TMEM, V MN-major
 
 struct Bars {
-  uint64_t full[kNST], empty[kNST];
+  uint64_t full[kNST];
+  uint64_t empty[3][kNST];          // per tile of a stage (Q, K, V): each frees after its last MMA
   uint64_t s_ready, s_read, b_done, s_written, drain;
   uint64_t p_ready, p_written;
   uint64_t o_ready[2], o_free[2];   // one per buffer parity
   uint64_t published;               // state warps' pool writes of a run that hands its state over
 };
+static_assert(sizeof(Bars) <= 256, "barriers overflow their shared-memory slot");
 
 // ------------------------------------------------------------------ work split
 // Units are the (request, head) chains, in order u = b * H + h; unit u has nch(b) chunks.
@@ -344,8 +348,8 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
   if (warp == kWarpMma) {
     if (lane == 0) {
       for (int s = 0; s < kNST; ++s) {
-        mbar_init(&bars->full[s], 1);
-        mbar_init(&bars->empty[s], 1);
+        mbar_init(&bars->full[s], 3);                // one arrival per tile, with its bytes
+        for (int t = 0; t < 3; ++t) mbar_init(&bars->empty[t][s], 1);
       }
       mbar_init(&bars->s_ready, 1);
       mbar_init(&bars->b_done, 1);
@@ -383,22 +387,33 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
     while (ok && NEXT_RUN(sg)) {
       for (int ci = sg.c0; ci < sg.c1; ++ci, ++c) {
         const int st = c % kNST;
-        if (c >= kNST) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars->empty[st], ((c - kNST) / kNST) & 1));
-          if (!ok) break;
+        uint8_t* q = sm + st * kStage;
+        uint64_t* bar = &bars->full[st];
+        const int z = sg.t0 + ci * kC;
+        // Tiles in the order the MMAs release them: K after (d), Q after (b), V after (c).
+        int t = 0;
+#pragma unroll
+        for (; t < 3; ++t) {
+          const int tt = t == 0 ? 1 : (t == 1 ? 0 : 2);
+          if (c >= kNST) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bars->empty[tt][st], ((c - kNST) / kNST) & 1));
+            if (!ok) break;
+          }
+          if (lane == 0) {
+            const CUtensorMap* m = tt == 0 ? &tq : (tt == 1 ? &tk : &tv);
+            mbar_expect_tx(bar, kTile);
+            for (int r0 = 0; r0 < kC; r0 += kBoxRows)
+              for (int sb = 0; sb < 2; ++sb)
+                tma_load_3d(q + tt * kTile + sb * kSub + r0 * 128, m, sb * 64, sg.h, z + r0, bar);
+          }
         }
-        if (lane == 0) {
-          uint8_t* q = sm + st * kStage;
-          uint64_t* bar = &bars->full[st];
-          mbar_expect_tx(bar, kStage);
-          const int z = sg.t0 + ci * kC;
-          for (int r0 = 0; r0 < kC; r0 += kBoxRows)
-            for (int sb = 0; sb < 2; ++sb) {
-              const int o = sb * kSub + r0 * 128;
-              tma_load_3d(q + o, &tq, sb * 64, sg.h, z + r0, bar);
-              tma_load_3d(q + kTile + o, &tk, sb * 64, sg.h, z + r0, bar);
-              tma_load_3d(q + 2 * kTile + o, &tv, sb * 64, sg.h, z + r0, bar);
-            }
+        if (!ok) {                           // the tiles not issued arrive without bytes, so
+          if (t > 0) {                       // the chunk's phase completes when its loads land
+            if (lane == 0)
+              for (int r = t; r < 3; ++r) mbar_arrive(bar);
+            ++c;
+          }
+          break;
         }
       }
     }
@@ -455,6 +470,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
           for (int k = 0; k < 8; ++k)              // (d) S += K^T V
             tc_mma(tmem + kColS, desc_add(mn0, ko + k * 2048), desc_add(mn0, vo + k * 2048), kIdescD, 1);
           tc_commit(&bars->s_ready);
+          tc_commit(&bars->empty[1][st]);        // K's last use
         }
         if (c >= 2) {
           ok = __all_sync(0xffffffffu, mbar_wait(&bars->o_free[ob], ((c - 2) >> 1) & 1));
@@ -470,6 +486,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
             tc_mma(tmem + kColO + ob * 128, desc_add(km0, qo + aoff), desc_add(st0, k * 2048), kIdescB, k != 0);
           }
           tc_commit(&bars->b_done);
+          tc_commit(&bars->empty[0][st]);        // Q's last use
         }
         __syncwarp();
         ok = __all_sync(0xffffffffu, mbar_wait(&bars->p_written, c & 1));
@@ -480,7 +497,7 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
           for (int k = 0; k < 8; ++k)              // (c) O += tril(P) V
             tc_mma_ta(tmem + kColO + ob * 128, tmem + kColP + k * 8, desc_add(mn0, vo + k * 2048), kIdescC, 1);
           tc_commit(&bars->o_ready[ob]);
-          tc_commit(&bars->empty[st]);
+          tc_commit(&bars->empty[2][st]);        // V's last use
         }
         __syncwarp();
       }
