@@ -350,8 +350,10 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict_
 }
 
 // Merges the splits of one (request, head): out = sum_s 2^(m_s-M) acc_s / sum_s 2^(m_s-M) l_s.
-// The max is a block reduction; the sums keep split order (so results do not depend on the
-// CTA shape) with eight splits' loads in flight at a time.
+// Every thread takes the max M itself from the (m, l) pairs (the same addresses for all
+// threads, so one broadcast load each): no block reduction, and with at most 8 splits the
+// pairs and the partial sums are all loaded in one round trip. The sums keep split order,
+// so results do not depend on the CTA shape.
 template <typename T, int D>
 __global__ void __launch_bounds__(128)
 decode_combine_kernel(T* __restrict__ out, const int32_t* __restrict__ seq_lens, int H, int MBt,
@@ -365,38 +367,55 @@ decode_combine_kernel(T* __restrict__ out, const int32_t* __restrict__ seq_lens,
   const int64_t rh = (int64_t)r * H + h;
   const float2* ml = ws_ml + rh * max_splits;
   const float* acc = ws_acc + rh * max_splits * D;
-  __shared__ float red[4];
-  float M = -INFINITY;
-  for (int s = threadIdx.x; s < nsplit; s += blockDim.x) M = fmaxf(M, ml[s].x);
-#pragma unroll
-  for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = M;
-  __syncthreads();
-  M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
   for (int t = threadIdx.x; t < D; t += blockDim.x) {
     float L = 0.f, A = 0.f;
-    if (M != -INFINITY) {
-      int s = 0;
-      for (; s + 8 <= nsplit; s += 8) {
-        float2 v[8];
-        float a[8];
+    if (nsplit <= 8) {
+      float2 v[8];
+      float a[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        v[u] = u < nsplit ? ml[u] : make_float2(-INFINITY, 0.f);
+        a[u] = u < nsplit ? acc[(int64_t)u * D + t] : 0.f;
+      }
+      float M = v[0].x;
+#pragma unroll
+      for (int u = 1; u < 8; ++u) M = fmaxf(M, v[u].x);
+      if (M != -INFINITY) {
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          v[u] = ml[s + u];
-          a[u] = acc[(int64_t)(s + u) * D + t];
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const float sc = fast_exp2(v[u].x - M);
-          L = fmaf(v[u].y, sc, L);
-          A = fmaf(a[u], sc, A);
+          if (u < nsplit) {
+            const float sc = fast_exp2(v[u].x - M);
+            L = fmaf(v[u].y, sc, L);
+            A = fmaf(a[u], sc, A);
+          }
         }
       }
-      for (; s < nsplit; ++s) {
-        const float2 v = ml[s];
-        const float sc = fast_exp2(v.x - M);
-        L = fmaf(v.y, sc, L);
-        A = fmaf(acc[(int64_t)s * D + t], sc, A);
+    } else {
+      float M = -INFINITY;
+      for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[s].x);
+      if (M != -INFINITY) {
+        int s = 0;
+        for (; s + 8 <= nsplit; s += 8) {
+          float2 v[8];
+          float a[8];
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            v[u] = ml[s + u];
+            a[u] = acc[(int64_t)(s + u) * D + t];
+          }
+#pragma unroll
+          for (int u = 0; u < 8; ++u) {
+            const float sc = fast_exp2(v[u].x - M);
+            L = fmaf(v[u].y, sc, L);
+            A = fmaf(a[u], sc, A);
+          }
+        }
+        for (; s < nsplit; ++s) {
+          const float2 v = ml[s];
+          const float sc = fast_exp2(v.x - M);
+          L = fmaf(v.y, sc, L);
+          A = fmaf(acc[(int64_t)s * D + t], sc, A);
+        }
       }
     }
     Elt<T>::store(out + rh * D + t, L > 0.f ? A / L : 0.f);
