@@ -57,6 +57,7 @@ constexpr uint32_t kRegsSoftmax = 200, kRegsProducer = 104;
 constexpr uint32_t kTmemCols = 512;          // S_0/P_0 | S_1/P_1 | O_0 | O_1
 constexpr uint32_t kColO = 256;
 constexpr float kRescaleLog2 = 8.f;
+constexpr int kTailGroups = 16;              // (request, head) groups scheduled heavy first together
 
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 0, 1);   // A = P from TMEM
@@ -103,8 +104,23 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
                   const int32_t* __restrict__ bt, const int32_t* __restrict__ cu,
                   const int32_t* __restrict__ ctx, int H, int NB, int MB, int rsh,
                   float scale_log2, int window, unsigned* status) {
-  const int pt = gridDim.x - 1 - blockIdx.x;           // heavy pairs first
-  const int h = blockIdx.y, b = blockIdx.z;
+  // CTAs start in linear block order. Each (request, head) group's pairs run heavy first,
+  // group after group, so a group's K/V tiles are re-read from L2. The last kTailGroups
+  // groups (64 MiB of K/V at 8192 tokens) are interleaved heavy first across all of them,
+  // so the final wave holds light pairs instead of a late group's heavy ones.
+  const int np = gridDim.x, G = gridDim.y * gridDim.z;
+  const int lin = blockIdx.x + np * (blockIdx.y + gridDim.y * blockIdx.z);
+  const int gt = min(kTailGroups, G), head_ctas = (G - gt) * np;
+  int pt, grp;
+  if (lin < head_ctas) {
+    grp = lin / np;
+    pt = np - 1 - lin % np;
+  } else {
+    const int l = lin - head_ctas;
+    grp = G - gt + l % gt;
+    pt = np - 1 - l / gt;
+  }
+  const int h = grp % gridDim.y, b = grp / gridDim.y;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = cu[b], n = cu[b + 1] - t0;
   const int q0 = pt * 2 * kBM;                         // first query of the pair
