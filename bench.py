@@ -48,7 +48,7 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--workload", default="decode_single_layer",
                     choices=["decode_single_layer", "hybrid_32layer", "prefill_chunked", "long_context_decode",
-                             "sliding_window", "state_precision", "block32", "bucketing"],
+                             "sliding_window", "state_precision", "block32", "bucketing", "prefill_lengths"],
                     help="decode_single_layer is the headline; the others are timed alone (e.g. for profiling)")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements of the other workloads")
     return ap.parse_args()
@@ -624,9 +624,45 @@ def row_bucketing(hyb, device, stream, iters, seed=0):
             "roofline": _roof("hbm", alg / (t0 * 1e-3) / 1e9, hbm, "GB/s", "whole 32-layer step, one call", alg)}
 
 
+def row_prefill_lengths(hyb, device, stream, iters, seed=0):
+    """Tensor-core causal prefill at one CTA count (8 192 pairs of query tiles) and five
+    prompt lengths, 32 x 2048 ... 2 x 32768 tokens, H=32, D=128: how the per-CTA fill and
+    drain weigh against the per-key-step cost."""
+    import torch
+    _, tf, _ = measured_peaks()
+    res = {"workload": "prefill_lengths: causal prefill, 8192 CTAs, B x L = 32x2048 .. 2x32768, H=32, D=128",
+           "unit": "TFLOP/s", "cases": {}}
+    for B, L in ((32, 2048), (16, 4096), (8, 8192), (4, 16384), (2, 32768)):
+        pb = W.prefill_chunked(seed, B=B, L=L)
+        H, D, NB = pb.H, pb.D, pb.pool.num_blocks
+        cu_h = W.cu_from_lens(pb.q_lens)
+        T = int(cu_h[-1])
+        d = hyb.dims(H, D, NB, pb.pool.max_blocks, W.BF16)
+        q = W.device_rows_(torch.empty((T, H, D), dtype=torch.bfloat16, device=device), 61, D)
+        kc = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), 5, D)
+        vc = W.device_rows_(torch.empty_like(kc), 6, D)
+        bt = torch.from_numpy(pb.pool.block_tables).to(device)
+        cu = torch.from_numpy(cu_h).to(device)
+        out = torch.empty_like(q)
+        sh = stream.cuda_stream
+        t = _time(lambda: hyb.check(hyb.hyb_paged_attn_prefill_causal(out, q, kc, vc, bt, cu, None, B, T, L, d, sh)),
+                  stream, min(iters, 10))
+        n = pb.q_lens.astype(np.float64)
+        fl = 4.0 * H * D * float((n * (n + 1) / 2).sum())
+        res["cases"][f"{B}x{L}"] = {"ms": round(t, 4), "TFLOP/s": round(fl / (t * 1e-3) / 1e12, 1),
+                                    "frac": round(fl / (t * 1e-3) / 1e12 / tf, 4)}
+        del q, kc, vc, out
+        torch.cuda.empty_cache()
+    st_, fl = hyb.hyb_device_status(clear=True)
+    if st_ != 0:
+        raise RuntimeError(f"device-side check flags {fl:#x}")
+    return res
+
+
 ROWS = {"long_context_decode": row_long_context, "hybrid_32layer": row_hybrid_32layer,
         "prefill_chunked": row_prefill, "sliding_window": row_sliding_window,
         "state_precision": row_state_precision, "block32": row_block32, "bucketing": row_bucketing}
+EXTRA_ROWS = {"prefill_lengths": row_prefill_lengths}   # --workload only, not in the default rows
 
 
 def bench_ours(args, dist):
@@ -642,7 +678,7 @@ def bench_ours(args, dist):
     device = torch.device("cuda", dist.local)
     if args.workload != "decode_single_layer":          # one other workload, timed alone
         stream = torch.cuda.Stream(device=device)
-        r = ROWS[args.workload](hyb, device, stream, max(args.steps, 1), args.seed + dist.rank)
+        r = {**ROWS, **EXTRA_ROWS}[args.workload](hyb, device, stream, max(args.steps, 1), args.seed + dist.rank)
         r.update({"metric": METRIC, "n_gpus": dist.world, "steps": args.steps, "warmup": 3,
                   "higher_is_better": True, "dtype": "bf16", "data": "synthetic"})
         return r
