@@ -71,10 +71,12 @@ def test_prefill_rows_equal_decode_of_same_prefix(hyb, devstatus):
     assert devstatus() == (0, 0)
 
 
-def test_causal_prefill_full_workload_sampled(hyb, devstatus):
-    """8 requests x 8192 tokens, H=32, D=128: KV appended to a shuffled pool, tensor-core
-    causal prefill; sampled rows (incl. first/last of every request) against the oracle."""
-    pb = W.prefill_chunked(0)
+@pytest.mark.parametrize("B,L", [(8, 8192), (2, 32768)])
+def test_causal_prefill_full_workload_sampled(hyb, devstatus, B, L):
+    """8 requests x 8192 tokens (and 2 x 32768, the longest prompts the prefill-length bench
+    row runs), H=32, D=128: KV appended to a shuffled pool, tensor-core causal prefill;
+    sampled rows (incl. first/last of every request) against the oracle."""
+    pb = W.prefill_chunked(0, B=B, L=L)
     B, H, D, NB = len(pb.q_lens), pb.H, pb.D, pb.pool.num_blocks
     cu = W.cu_from_lens(pb.q_lens)
     T = int(cu[-1])
@@ -89,13 +91,13 @@ def test_causal_prefill_full_workload_sampled(hyb, devstatus):
     hyb.check(hyb.hyb_slot_mapping(slot, bt, cu_d, None, B, T, d))
     hyb.check(hyb.hyb_paged_kv_append(to_dev(k), to_dev(v), slot, T, kc, vc, d))
     out = empty_rows((T, H, D), W.BF16)
-    hyb.check(hyb.hyb_paged_attn_prefill_causal(out, to_dev(q), kc, vc, bt, cu_d, None, B, T, 8192, d))
+    hyb.check(hyb.hyb_paged_attn_prefill_causal(out, to_dev(q), kc, vc, bt, cu_d, None, B, T, L, d))
     torch.cuda.synchronize()
     sm = oracle.slot_mapping(pb.pool.block_tables, cu)
     assert np.array_equal(to_host(slot), sm)
     rng = np.random.default_rng(3)
     rows = sorted(set([int(cu[b]) for b in range(B)] + [int(cu[b + 1]) - 1 for b in range(B)] +
-                      [int(cu[b]) + j for b in range(B) for j in (127, 128, 4095)] +
+                      [int(cu[b]) + j for b in range(B) for j in (127, 128, 4095, L - 129)] +
                       rng.integers(0, T, 24).tolist()))
     # oracle cache image built by the oracle itself (same bytes as the inputs)
     okc = np.zeros((NB, H, 16, D), np.uint16)
