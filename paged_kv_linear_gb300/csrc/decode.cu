@@ -349,11 +349,38 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict_
   }
 }
 
+// Split sums of one output element for a row with at most NS splits: every (m, l) pair and
+// partial sum is loaded before the maximum is taken, so they take one round trip.
+template <int NS, int D>
+__device__ __forceinline__ void combine_few(const float2* __restrict__ ml,
+                                            const float* __restrict__ acc, int nsplit, int t,
+                                            float& L, float& A) {
+  float2 v[NS];
+  float a[NS];
+#pragma unroll
+  for (int u = 0; u < NS; ++u) {
+    v[u] = u < nsplit ? ml[u] : make_float2(-INFINITY, 0.f);
+    a[u] = u < nsplit ? acc[(int64_t)u * D + t] : 0.f;
+  }
+  float M = v[0].x;
+#pragma unroll
+  for (int u = 1; u < NS; ++u) M = fmaxf(M, v[u].x);
+  if (M == -INFINITY) return;
+#pragma unroll
+  for (int u = 0; u < NS; ++u) {
+    if (u < nsplit) {
+      const float sc = fast_exp2(v[u].x - M);
+      L = fmaf(v[u].y, sc, L);
+      A = fmaf(a[u], sc, A);
+    }
+  }
+}
+
 // Merges the splits of one (request, head): out = sum_s 2^(m_s-M) acc_s / sum_s 2^(m_s-M) l_s.
 // Every thread takes the max M itself from the (m, l) pairs (the same addresses for all
-// threads, so one broadcast load each): no block reduction, and with at most 8 splits the
+// threads, so one broadcast load each): no block reduction, and with at most 16 splits the
 // pairs and the partial sums are all loaded in one round trip. The sums keep split order,
-// so results do not depend on the CTA shape.
+// so results do not depend on the CTA shape or on which branch a row takes.
 template <typename T, int D>
 __global__ void __launch_bounds__(128)
 decode_combine_kernel(T* __restrict__ out, const int32_t* __restrict__ seq_lens, int H, int MBt,
@@ -370,26 +397,9 @@ decode_combine_kernel(T* __restrict__ out, const int32_t* __restrict__ seq_lens,
   for (int t = threadIdx.x; t < D; t += blockDim.x) {
     float L = 0.f, A = 0.f;
     if (nsplit <= 8) {
-      float2 v[8];
-      float a[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        v[u] = u < nsplit ? ml[u] : make_float2(-INFINITY, 0.f);
-        a[u] = u < nsplit ? acc[(int64_t)u * D + t] : 0.f;
-      }
-      float M = v[0].x;
-#pragma unroll
-      for (int u = 1; u < 8; ++u) M = fmaxf(M, v[u].x);
-      if (M != -INFINITY) {
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          if (u < nsplit) {
-            const float sc = fast_exp2(v[u].x - M);
-            L = fmaf(v[u].y, sc, L);
-            A = fmaf(a[u], sc, A);
-          }
-        }
-      }
+      combine_few<8, D>(ml, acc, nsplit, t, L, A);
+    } else if (nsplit <= 16) {
+      combine_few<16, D>(ml, acc, nsplit, t, L, A);
     } else {
       float M = -INFINITY;
       for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[s].x);
