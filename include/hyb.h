@@ -336,6 +336,16 @@ uint64_t hyb_cache_bytes(int32_t L_full, int32_t L_linear, int32_t H, int32_t D,
                          int32_t batch, int32_t kv_elem_bytes, int32_t state_elem_bytes,
                          uint64_t* full_out, uint64_t* linear_out);
 
+/* Bounded-wait self-test (failure detection without a fault). Launches one small kernel
+ * on `stream` (NULL: the default stream) whose two device-side waits can never be met: an
+ * mbarrier phase that nothing completes (the helper behind every TMA and tensor-core wait
+ * in the library) and a global flag that nothing sets (the acquire-load wait of the
+ * chunked linear prefill's state handoff). Each gives up after limit_us microseconds and
+ * sets HYB_DEVERR_TIMEOUT in the device status word, which hyb_device_status() then
+ * reports; the kernel returns normally and the context stays usable.
+ * limit_us outside [1, 1000000] returns HYB_ERR_INVALID_ARG before any launch. */
+hyb_status_t hyb_selftest_bounded_waits(uint32_t limit_us, void* stream);
+
 /* Reads (and, if clear != 0, zeroes) the device status word of the current device
  * into *flags (host). Synchronises the device. Returns HYB_ERR_DEVICE_CHECK when any
  * bit was set, HYB_OK otherwise. */

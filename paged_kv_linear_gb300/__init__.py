@@ -77,6 +77,7 @@ def _load():
         "hyb_last_cuda_error": ([], C.c_char_p),
         "hyb_launch_count": ([i32], u64),
         "hyb_trace_layer_ms": [p, i32],
+        "hyb_selftest_bounded_waits": [C.c_uint32, p],
     }
     for name, s in sig.items():
         fn = getattr(L, name)
@@ -265,6 +266,12 @@ def hyb_trace_layer_ms(L: int):
     buf = (C.c_float * max(L, 1))()
     st = _lib.hyb_trace_layer_ms(buf, L)
     return int(st), [float(x) for x in buf[:L]]
+
+
+def hyb_selftest_bounded_waits(limit_us: int, stream=None):
+    """Runs the bounded-wait self-test kernel: two waits nothing satisfies, each giving up
+    after limit_us and setting HYB_DEVERR_TIMEOUT in the device status word."""
+    return _lib.hyb_selftest_bounded_waits(limit_us, _s(stream))
 
 
 def hyb_launch_count(reset: bool = False) -> int:

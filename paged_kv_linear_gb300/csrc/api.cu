@@ -15,6 +15,41 @@
 
 // Device-side check word (one per device that loads the library); kernels OR bits in.
 static __device__ unsigned g_hyb_status;
+// A flag that nothing ever sets: the bounded-wait self-test waits on it.
+static __device__ unsigned long long g_hyb_never_set;
+
+namespace hyb {
+namespace {
+// Two device-side waits that nothing satisfies, each with the library's bounded-wait
+// mechanism: warp 0 on an mbarrier phase that no thread or copy completes (the helper every
+// TMA and tensor-core wait uses), warp 1 on a global flag that no thread sets (an acquire
+// load, %globaltimer and a back-off, as in the chunked linear prefill's state handoff). Each
+// gives up after limit_ns, reports HYB_DEVERR_TIMEOUT and returns.
+__global__ void selftest_bounded_waits_kernel(uint64_t limit_ns, unsigned* status) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (!mbar_wait(&bar, 0, limit_ns)) flag(status, HYB_DEVERR_TIMEOUT);
+  } else if (threadIdx.x == 32) {
+    const uint64_t t0 = global_ns();
+    while (true) {
+      unsigned long long v;
+      asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(&g_hyb_never_set) : "memory");
+      if (v == ~0ull) break;                   // never true: nothing writes the flag
+      if (global_ns() - t0 > limit_ns) {
+        flag(status, HYB_DEVERR_TIMEOUT);
+        break;
+      }
+      __nanosleep(1000);
+    }
+  }
+}
+}  // namespace
+}  // namespace hyb
 
 namespace hyb {
 namespace {
@@ -558,6 +593,16 @@ const char* hyb_status_string(hyb_status_t s) {
     case HYB_ERR_DEVICE_CHECK: return "a device-side check failed (see hyb_device_status flags)";
   }
   return "unknown status";
+}
+
+hyb_status_t hyb_selftest_bounded_waits(uint32_t limit_us, void* stream) {
+  if (limit_us < 1 || limit_us > 1000000) return HYB_ERR_INVALID_ARG;
+  unsigned* sw = hyb::status_word();
+  if (!sw) return HYB_ERR_CUDA;
+  hyb::selftest_bounded_waits_kernel<<<1, 64, 0, (cudaStream_t)stream>>>(
+      (uint64_t)limit_us * 1000ull, sw);
+  hyb::count_launch();
+  return cuda_status(cudaGetLastError());
 }
 
 uint64_t hyb_launch_count(int32_t reset) {

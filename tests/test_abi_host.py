@@ -173,3 +173,9 @@ def test_trace_without_a_traced_dispatch(hyb):
     """No dispatch has been traced on this thread: nothing to report (no CUDA call made)."""
     st, _ = hyb.hyb_trace_layer_ms(4)
     assert st == hyb.HYB_ERR_INVALID_ARG
+
+
+def test_selftest_limit_checked_before_launch(hyb):
+    """The bounded-wait self-test rejects a limit outside [1 us, 1 s] before any CUDA call."""
+    assert hyb.hyb_selftest_bounded_waits(0, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_selftest_bounded_waits(1000001, 0) == hyb.HYB_ERR_INVALID_ARG
