@@ -367,7 +367,8 @@ def row_prefill(hyb, device, stream, iters, seed=0):
                                            tflops=round(lin_tf, 1), tensor_frac=round(lin_tf / tf, 4),
                                            arithmetic_intensity=round(ai, 1),
                                            frac_of_min_peak_ai_bw=round(lin_tf / min(tf, ai * hbm / 1e3), 4)),
-           "kv_append": _roof("hbm", app_bytes / (t_app * 1e-3) / 1e9, hbm, "GB/s", "kv_append_kernel", app_bytes)}
+           "kv_append": _roof("hbm", app_bytes / (t_app * 1e-3) / 1e9, hbm, "GB/s", "kv_append_kernel", app_bytes,
+                              traffic=_traffic("kv_append", "append.cu"))}
     del q, k, v, ql, kl, vl, out, lo, kc, vc, st
     torch.cuda.empty_cache()
     return res
