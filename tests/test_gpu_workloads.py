@@ -173,9 +173,11 @@ def test_single_layer_decode_batch_full_size(hyb, devstatus):
 
 
 # ------------------------------------------------------------- long context
-def test_long_context_decode_sampled(hyb, devstatus):
+@pytest.mark.parametrize("fused", [False, True])
+def test_long_context_decode_sampled(hyb, devstatus, fused):
     """8 requests x 131072 tokens (8192 blocks each, randomly placed): sampled (request,
-    head) pairs against the oracle, appended rows bit-exact, Linear step in full."""
+    head) pairs against the oracle, appended rows bit-exact, Linear step in full. `fused`:
+    the append runs inside the decode (slots from the block table), as the bench's step."""
     db = W.decode_long_context(0)
     B, H, D, NB = db.B, db.H, db.D, db.pool.num_blocks
     n = int(db.seq_lens[0])
@@ -199,13 +201,20 @@ def test_long_context_decode_sampled(hyb, devstatus):
     ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, n, d)
     ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda")
     lens_d = to_dev(db.seq_lens)
-    hyb.check(hyb.hyb_slot_mapping(slot, to_dev(bt), to_dev(np.arange(B + 1, dtype=np.int32)),
-                                   to_dev(db.seq_lens - 1), B, B, d))
-    hyb.check(hyb.hyb_paged_kv_append(to_dev(k), to_dev(v), slot, B, kc, vc, d))
-    hyb.check(hyb.hyb_paged_attn_decode(out, to_dev(q), kc, vc, to_dev(bt), lens_d, B, n, d, ws, ws_n))
-    torch.cuda.synchronize()
-    sm = to_host(slot)
-    assert np.array_equal(sm, oracle.slot_mapping(bt, np.arange(B + 1), db.seq_lens - 1))
+    sm_ref = oracle.slot_mapping(bt, np.arange(B + 1), db.seq_lens - 1)
+    if fused:
+        hyb.check(hyb.hyb_paged_attn_decode_append(out, to_dev(q), to_dev(k), to_dev(v), None, kc, vc,
+                                                   to_dev(bt), lens_d, B, n, d, ws, ws_n))
+        torch.cuda.synchronize()
+        sm = sm_ref
+    else:
+        hyb.check(hyb.hyb_slot_mapping(slot, to_dev(bt), to_dev(np.arange(B + 1, dtype=np.int32)),
+                                       to_dev(db.seq_lens - 1), B, B, d))
+        hyb.check(hyb.hyb_paged_kv_append(to_dev(k), to_dev(v), slot, B, kc, vc, d))
+        hyb.check(hyb.hyb_paged_attn_decode(out, to_dev(q), kc, vc, to_dev(bt), lens_d, B, n, d, ws, ws_n))
+        torch.cuda.synchronize()
+        sm = to_host(slot)
+        assert np.array_equal(sm, sm_ref)
     for b in range(B):
         s = int(sm[b])
         assert np.array_equal(to_host(kc[s // 16, :, s % 16]), k[b])
