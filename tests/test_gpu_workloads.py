@@ -240,10 +240,12 @@ def test_long_context_decode_sampled(hyb, devstatus, fused):
 
 
 # ---------------------------------------------------- 32-layer hybrid decode
-def test_hybrid_32_layer_dispatch(hyb, devstatus):
+@pytest.mark.parametrize("slot_from_table", [False, True])
+def test_hybrid_32_layer_dispatch(hyb, devstatus, slot_from_table):
     """layer_types = [F,F,F,Lin] x 8, batch 64 with the 80/20 short/long mix: the dispatcher
     equals per-op calls bit for bit (outputs, caches, states), and layers 0 (Full) and 3
-    (Linear) match the oracle."""
+    (Linear) match the oracle. `slot_from_table`: no slot mapping in the metadata, so each
+    Full layer finds the new row's slot through the block table (the bench's 32-layer step)."""
     db = W.decode_hybrid_32layer(0)
     lt = db.extra["layer_types"]
     B, H, D, NB, MB = db.B, db.H, db.D, db.pool.num_blocks, db.pool.max_blocks
@@ -274,7 +276,8 @@ def test_hybrid_32_layer_dispatch(hyb, devstatus):
                                    to_dev(db.seq_lens - 1), B, B, d))
     ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, msl, d)
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
-    meta = hyb.batch_meta(B, B, seq_lens=lens, block_tables=bt, slot_mapping=slot, state_slots=slots, max_seq_len=msl)
+    meta = hyb.batch_meta(B, B, seq_lens=lens, block_tables=bt, slot_mapping=None if slot_from_table else slot,
+                          state_slots=slots, max_seq_len=msl)
     ios = [hyb.layer_io(io["out"], io["q"], io["k"], io["v"], io.get("k_cache"), io.get("v_cache"),
                         io.get("state_pool"), B) for io in layers_dev]
     hyb.check(hyb.hyb_layer_dispatch(lt, 32, 0, ios, meta, d, 64, ws, ws_n))
