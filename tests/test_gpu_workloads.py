@@ -157,6 +157,22 @@ def test_single_layer_decode_batch_full_size(hyb, devstatus):
         assert np.array_equal(kh[s // 16, :, s % 16], case.k[b])
     del kh
     assert_out_close(out, out_ref, "decode out")
+    # the bench's launch: the append fused into the decode, slots from the block table;
+    # bit-identical to the separate append + decode above
+    d = case.dims(hyb)
+    msl = int(db.seq_lens.max())
+    ws_n = hyb.hyb_paged_attn_decode_workspace_size(db.B, msl, d)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+    kc2, vc2 = to_dev(case.kc), to_dev(case.vc)
+    out2 = empty_rows((db.B, db.H, db.D), db.dtype)
+    hyb.check(hyb.hyb_paged_attn_decode_append(out2, to_dev(case.q), to_dev(case.k), to_dev(case.v), None, kc2, vc2,
+                                               to_dev(db.pool.block_tables), to_dev(db.seq_lens), db.B, msl, d,
+                                               ws, ws_n))
+    torch.cuda.synchronize()
+    assert torch.equal(out2.view(torch.int16), out.view(torch.int16))
+    assert torch.equal(kc2.view(torch.int16), kc.view(torch.int16))
+    assert torch.equal(vc2.view(torch.int16), vc.view(torch.int16))
+    del kc2, vc2
     # Linear step at the same shape (state 32 x 128 x 128 fp32 per request)
     g = W.rng(1)
     B, H, D = db.B, db.H, db.D
