@@ -174,9 +174,18 @@ hyb_status_t hyb_paged_attn_decode_append(void* out, const void* q, const void* 
  * split-K partials live in a 16 MiB array of device memory owned by the library (held
  * by every GPU that loads libhyb.so until the process exits); nothing is allocated.
  * - Returns HYB_ERR_UNSUPPORTED, launching nothing, when the partials would need more
- *   than 16 MiB (hyb_paged_attn_decode_workspace_size() > 16 MiB).
+ *   than 16 MiB (hyb_paged_attn_decode_workspace_size() > 16 MiB). A batch with more than
+ *   one split of 512 keys needs B x H x ceil(max_seq_len / 512) x (4 D + 8) bytes (with a
+ *   window, max_seq_len is capped near the window): at H = 32, D = 128 that allows
+ *   B x ceil(max_seq_len / 512) <= 1008, e.g. 64 requests up to 7 680 tokens. The
+ *   8 x 131 072-token long-context batch needs ~34 MB and is always rejected here.
+ * - Argument errors are reported exactly as hyb_paged_attn_decode reports them (same
+ *   checks, before any CUDA call); CUDA failures set hyb_last_cuda_error().
  * - The first call on a device looks up the array's device address (with that device
- *   current); make that first call before any stream capture on the device.
+ *   current); make that first call before any stream capture on the device. The address
+ *   is cached for the life of the process: after cudaDeviceReset on that device it is
+ *   stale and this entry point must not be called again (the device status word that
+ *   every entry point uses is cached the same way).
  * - All calls on a device share the array and it keeps the previous call's contents
  *   (nothing in it needs to start at zero). Calls whose kernels overlap on the GPU race
  *   on it: issue them one after another on one stream.

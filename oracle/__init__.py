@@ -209,20 +209,3 @@ def cache_bytes(L_full, L_linear, H, D, tokens, batch, kv_elem_bytes, state_elem
     tot = lib().oracle_cache_bytes(L_full, L_linear, H, D, tokens, batch, kv_elem_bytes,
                                    state_elem_bytes, C.byref(full), C.byref(lin))
     return int(tot), int(full.value), int(lin.value)
-
-
-def layer_dispatch_decode(layer_types, layers, seq_lens, block_tables, slot_map, state_slots, scale,
-                          block_size=BLOCK_SIZE):
-    """Decode through a list of layers in order [KV §2.2]: a Full layer appends its k/v at
-    slot_map and attends through the block table; a Linear layer steps its own state.
-    layers[l]: dict with q, k, v and k_cache/v_cache (Full, updated in place) or
-    state_pool (Linear, read only here). Returns per-layer (out, new_state or None)."""
-    res = []
-    for lt, io in zip(layer_types, layers):
-        if int(lt) == 0:
-            kv_append(io["k"], io["v"], slot_map, io["k_cache"], io["v_cache"], block_size)
-            res.append((full_decode(io["q"], io["k_cache"], io["v_cache"], block_tables, seq_lens,
-                                    scale, block_size), None))
-        else:
-            res.append(linear_step(io["q"], io["k"], io["v"], io["state_pool"], state_slots))
-    return res

@@ -109,6 +109,11 @@ def _p(x):
     return x.data_ptr()
 
 
+def _d(d):
+    """Pointer to a hyb_attn_dims_t (None passes NULL)."""
+    return None if d is None else C.byref(d)
+
+
 def _s(stream):
     if stream is None:
         import torch
@@ -154,22 +159,22 @@ def status_string(status: int) -> str:
 # ------------------------------------------------------------------ entry points
 def hyb_slot_mapping(slot_mapping, block_tables, cu_q_lens, ctx_lens, B, T, d, stream=None):
     return _lib.hyb_slot_mapping(_p(slot_mapping), _p(block_tables), _p(cu_q_lens), _p(ctx_lens),
-                                 B, T, C.byref(d), _s(stream))
+                                 B, T, _d(d), _s(stream))
 
 
 def hyb_paged_kv_append(k, v, slot_mapping, T, k_cache, v_cache, d, stream=None):
     return _lib.hyb_paged_kv_append(_p(k), _p(v), _p(slot_mapping), T, _p(k_cache), _p(v_cache),
-                                    C.byref(d), _s(stream))
+                                    _d(d), _s(stream))
 
 
 def hyb_paged_attn_decode_workspace_size(B, max_seq_len, d) -> int:
-    return int(_lib.hyb_paged_attn_decode_workspace_size(B, max_seq_len, C.byref(d)))
+    return int(_lib.hyb_paged_attn_decode_workspace_size(B, max_seq_len, _d(d)))
 
 
 def hyb_paged_attn_decode(out, q, k_cache, v_cache, block_tables, seq_lens, B, max_seq_len, d,
                           workspace, ws_bytes, stream=None):
     return _lib.hyb_paged_attn_decode(_p(out), _p(q), _p(k_cache), _p(v_cache), _p(block_tables),
-                                      _p(seq_lens), B, max_seq_len, C.byref(d), _p(workspace),
+                                      _p(seq_lens), B, max_seq_len, _d(d), _p(workspace),
                                       ws_bytes, _s(stream))
 
 
@@ -177,7 +182,7 @@ def hyb_paged_attn_decode_append(out, q, k, v, slot_mapping, k_cache, v_cache, b
                                  seq_lens, B, max_seq_len, d, workspace, ws_bytes, stream=None):
     return _lib.hyb_paged_attn_decode_append(_p(out), _p(q), _p(k), _p(v), _p(slot_mapping),
                                              _p(k_cache), _p(v_cache), _p(block_tables),
-                                             _p(seq_lens), B, max_seq_len, C.byref(d),
+                                             _p(seq_lens), B, max_seq_len, _d(d),
                                              _p(workspace), ws_bytes, _s(stream))
 
 
@@ -187,14 +192,14 @@ def hyb_paged_attn_decode_noalloc(out, q, k_cache, v_cache, block_tables, seq_le
     (for callers that cannot allocate device memory); see include/hyb.h."""
     return _lib.hyb_paged_attn_decode_noalloc(_p(out), _p(q), _p(k_cache), _p(v_cache),
                                               _p(block_tables), _p(seq_lens), B, max_seq_len,
-                                              C.byref(d), _s(stream))
+                                              _d(d), _s(stream))
 
 
 def hyb_paged_attn_prefill_causal(out, q, k_cache, v_cache, block_tables, cu_q_lens, ctx_lens,
                                   B, T, max_q_len, d, stream=None):
     return _lib.hyb_paged_attn_prefill_causal(_p(out), _p(q), _p(k_cache), _p(v_cache),
                                               _p(block_tables), _p(cu_q_lens), _p(ctx_lens), B,
-                                              T, max_q_len, C.byref(d), _s(stream))
+                                              T, max_q_len, _d(d), _s(stream))
 
 
 def hyb_linear_attn_step(out, q, k, v, state_pool, num_state_slots, state_slots, B, H, D, dtype,
@@ -241,7 +246,7 @@ def hyb_layer_dispatch(layer_types, L, mode, layers, meta, d, chunk_size, worksp
     meta: hyb_batch_meta_t (host struct of device pointers)."""
     lt = (C.c_int32 * max(L, 1))(*[int(x) for x in layer_types])
     io = (hyb_layer_io_t * max(L, 1))(*layers)
-    return _lib.hyb_layer_dispatch(lt, L, mode, io, C.byref(meta), C.byref(d), chunk_size,
+    return _lib.hyb_layer_dispatch(lt, L, mode, io, C.byref(meta), _d(d), chunk_size,
                                    _p(workspace), ws_bytes, _s(stream))
 
 

@@ -114,6 +114,18 @@ inline bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) 
 inline bool al(const void* p, unsigned a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 inline int esize_of(int dtype) { return dtype == HYB_BF16 ? 2 : 4; }
 
+thread_local cudaError_t g_last_cuda = cudaSuccess;
+
+}  // namespace
+
+namespace hyb {
+
+hyb_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return HYB_OK;
+  g_last_cuda = e;
+  return HYB_ERR_CUDA;
+}
+
 hyb_status_t check_dims(const hyb_attn_dims_t* d) {
   if (!d) return HYB_ERR_INVALID_ARG;
   if (d->num_heads <= 0 || d->head_dim <= 0 || d->num_blocks <= 0 || d->max_blocks_per_seq <= 0)
@@ -127,13 +139,26 @@ hyb_status_t check_dims(const hyb_attn_dims_t* d) {
   return HYB_OK;
 }
 
-thread_local cudaError_t g_last_cuda = cudaSuccess;
-
-hyb_status_t cuda_status(cudaError_t e) {
-  if (e == cudaSuccess) return HYB_OK;
-  g_last_cuda = e;
-  return HYB_ERR_CUDA;
+hyb_status_t check_decode_args(const void* out, const void* q, const void* kc, const void* vc,
+                               const int32_t* bt, const int32_t* seq_lens, int B, int max_seq_len,
+                               const hyb_attn_dims_t* d) {
+  hyb_status_t st = check_dims(d);
+  if (st != HYB_OK) return st;
+  if (B < 0 || max_seq_len < 0) return HYB_ERR_INVALID_ARG;
+  if (d->num_heads > 65535) return HYB_ERR_UNSUPPORTED;
+  if ((int64_t)max_seq_len > (int64_t)d->max_blocks_per_seq * d->block_size) return HYB_ERR_INVALID_ARG;
+  if (max_seq_len > (1 << 24)) return HYB_ERR_UNSUPPORTED;   // grid.z = splits <= 65535
+  if (!decode_supported(d->dtype, d->head_dim)) return HYB_ERR_UNSUPPORTED;
+  if (B == 0) return HYB_OK;
+  if (!out || !q || !kc || !vc || !bt || !seq_lens) return HYB_ERR_INVALID_ARG;
+  if (!al16(out) || !al16(q) || !al16(kc) || !al16(vc) || !al(bt, 4) || !al(seq_lens, 4))
+    return HYB_ERR_INVALID_ARG;
+  return HYB_OK;
 }
+
+}  // namespace hyb
+
+namespace {
 
 // ---- per-op checks (no launch) -----------------------------------------------------
 hyb_status_t check_append(const void* k, const void* v, const int64_t* slot, int T,
@@ -151,17 +176,8 @@ hyb_status_t check_append(const void* k, const void* v, const int64_t* slot, int
 hyb_status_t check_decode(const void* out, const void* q, const void* kc, const void* vc,
                           const int32_t* bt, const int32_t* seq_lens, int B, int max_seq_len,
                           const hyb_attn_dims_t* d, const void* ws, size_t ws_bytes) {
-  hyb_status_t st = check_dims(d);
-  if (st != HYB_OK) return st;
-  if (B < 0 || max_seq_len < 0) return HYB_ERR_INVALID_ARG;
-  if (d->num_heads > 65535) return HYB_ERR_UNSUPPORTED;
-  if ((int64_t)max_seq_len > (int64_t)d->max_blocks_per_seq * d->block_size) return HYB_ERR_INVALID_ARG;
-  if (max_seq_len > (1 << 24)) return HYB_ERR_UNSUPPORTED;   // grid.z = splits <= 65535
-  if (!decode_supported(d->dtype, d->head_dim)) return HYB_ERR_UNSUPPORTED;
-  if (B == 0) return HYB_OK;
-  if (!out || !q || !kc || !vc || !bt || !seq_lens) return HYB_ERR_INVALID_ARG;
-  if (!al16(out) || !al16(q) || !al16(kc) || !al16(vc) || !al(bt, 4) || !al(seq_lens, 4))
-    return HYB_ERR_INVALID_ARG;
+  hyb_status_t st = check_decode_args(out, q, kc, vc, bt, seq_lens, B, max_seq_len, d);
+  if (st != HYB_OK || B == 0) return st;
   const DecodePlan p = plan_decode(B, d->num_heads, d->head_dim, max_seq_len, d->window);
   if (p.ws_bytes > 0 && (!ws || ws_bytes < p.ws_bytes || !al16(ws))) return HYB_ERR_INVALID_ARG;
   return HYB_OK;

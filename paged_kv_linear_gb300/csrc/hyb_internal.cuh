@@ -20,6 +20,14 @@ void count_launch();                       // per-thread launch counter (hyb_lau
 unsigned* status_word();                   // this device's status word (nullptr on error)
 int num_sms();                             // SMs of the current device (cached)
 cudaError_t set_smem(const void* fn, int bytes);   // opt-in dynamic shared memory, once
+// HYB_OK for cudaSuccess; otherwise records e for hyb_last_cuda_error and returns HYB_ERR_CUDA
+hyb_status_t cuda_status(cudaError_t e);
+// argument checks shared by the entry points (no CUDA call, no launch)
+hyb_status_t check_dims(const hyb_attn_dims_t* d);
+// every decode check except the workspace's (B == 0 returns HYB_OK before the pointer checks)
+hyb_status_t check_decode_args(const void* out, const void* q, const void* kc, const void* vc,
+                               const int32_t* bt, const int32_t* seq_lens, int B, int max_seq_len,
+                               const hyb_attn_dims_t* d);
 
 // Programmatic dependent launch for the short kernels of a decode step: a kernel launched
 // this way may be scheduled while the previous kernel on the stream drains. It calls

@@ -32,3 +32,21 @@ def devstatus(hyb):
     """Clears the device status word before a test; yields a reader (status, flags)."""
     hyb.hyb_device_status(clear=True)
     yield lambda: hyb.hyb_device_status(clear=True)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """Worst achieved row-relative output error per test (the parity margin of each check)."""
+    try:
+        from gpu_helpers import RECORDS, ROW_REL
+    except ImportError:
+        return
+    if not RECORDS:
+        return
+    worst = {}
+    for tid, what, rel, abs_err in RECORDS:
+        if tid not in worst or rel > worst[tid][1]:
+            worst[tid] = (what, rel, abs_err)
+    tr = terminalreporter
+    tr.write_sep("-", f"output parity: worst row-relative error per test (bound {ROW_REL:g})")
+    for tid, (what, rel, abs_err) in sorted(worst.items(), key=lambda kv: -kv[1][1]):
+        tr.write_line(f"{rel:.2e}  abs {abs_err:.2e}  {tid}  [{what}]")

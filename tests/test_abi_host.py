@@ -179,3 +179,26 @@ def test_selftest_limit_checked_before_launch(hyb):
     """The bounded-wait self-test rejects a limit outside [1 us, 1 s] before any CUDA call."""
     assert hyb.hyb_selftest_bounded_waits(0, 0) == hyb.HYB_ERR_INVALID_ARG
     assert hyb.hyb_selftest_bounded_waits(1000001, 0) == hyb.HYB_ERR_INVALID_ARG
+
+
+def test_noalloc_decode_checks_arguments_like_the_workspace_decode(hyb):
+    """The allocation-free decode runs the workspace decode's own argument checks before
+    any CUDA call (this container has no GPU): same status for the same bad arguments."""
+    f = 1 << 20
+    d = hyb.dims(32, 128, 1000, 256)
+    cases = [
+        (f, f, f, f, f, f, 2, 64, None),                          # no dims
+        (None, f, f, f, f, f, 2, 64, d),                          # null output
+        (f + 2, f, f, f, f, f, 2, 64, d),                         # misaligned output
+        (f, f, f, f, f + 1, f, 2, 64, d),                         # misaligned block table
+        (f, f, f, f, f, f, -1, 64, d),                            # negative batch
+        (f, f, f, f, f, f, 2, 256 * 16 + 1, d),                   # beyond the block table
+        (f, f, f, f, f, f, 2, 64, hyb.dims(32, 96, 1000, 256)),   # head dim without a kernel
+        (f, f, f, f, f, f, 2, 64, hyb.dims(32, 128, 1000, 256, block_size=24)),
+    ]
+    for a in cases:
+        want = hyb.hyb_paged_attn_decode(*a, f, 1 << 24, 0)
+        assert want != hyb.HYB_OK
+        assert hyb.hyb_paged_attn_decode_noalloc(*a, 0) == want, a
+    # an empty batch is accepted before any pointer is looked at, and launches nothing
+    assert hyb.hyb_paged_attn_decode_noalloc(None, None, None, None, None, None, 0, 0, d, 0) == hyb.HYB_OK

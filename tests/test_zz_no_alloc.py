@@ -5,16 +5,18 @@ example a runtime that plans all device memory itself and hands an op nothing bu
 inputs and outputs, or a latency-critical loop that must not call cudaMalloc because it
 synchronises the device. Its split-K partials live in a fixed 16 MiB array owned by the
 library instead of a caller workspace. Here it is called through the C ABI twice in a
-row, on two different batches, and each result must match hyb_paged_attn_decode (with
-a caller workspace) within the tolerance the parity tests use; the second call also shows
-that what the first call left in the shared array does not leak into the next result.
+row, on two different batches. It runs the same kernels with the same split plan as
+hyb_paged_attn_decode (with a caller workspace), so each result must equal that entry
+point's bit for bit; the second call also shows that what the first call left in the
+shared array does not leak into the next result. A third batch with peaked scores is
+checked against the CPU oracle under the output rule the parity tests use.
 """
 import numpy as np
 import pytest
 import torch
 
 import workloads as W
-from gpu_helpers import assert_out_close, to_dev
+from gpu_helpers import assert_out_close, decode_case, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -45,12 +47,27 @@ def _both(hyb, b):
     return got, ref
 
 
-def test_noalloc_decode_matches_workspace_decode_on_two_calls_in_a_row(hyb):
+def test_noalloc_decode_equals_workspace_decode_on_two_calls_in_a_row(hyb):
     first = _batch(41, [4096, 17, 1500, 3000, 640, 2222, 9, 4000])
     second = _batch(42, [3500, 2048, 100, 4095, 1, 2900])
     for b in (first, second):
         got, ref = _both(hyb, b)
-        assert_out_close(got, ref.double().cpu().numpy(), "noalloc decode")
+        assert torch.equal(got.view(torch.int16), ref.view(torch.int16))   # same kernels, same plan
+    st, flags = hyb.hyb_device_status(clear=True)
+    assert st == 0, f"device status {flags:#x}"
+
+
+def test_noalloc_decode_matches_oracle_on_peaked_scores(hyb):
+    """Rising scores: the running max moves across every split, so the merge of the splits'
+    partials from the shared array must weight them right."""
+    c = decode_case(43, [4096, 513, 9000, 1], 8, 128, W.BF16, peaked="rise")
+    d = c.dims(hyb)
+    lens = c.ctx + 1
+    out = torch.full((c.B, c.H, c.D), float("nan"), dtype=torch.bfloat16, device="cuda")
+    hyb.check(hyb.hyb_paged_attn_decode_noalloc(out, to_dev(c.q), to_dev(c.okc), to_dev(c.ovc),
+                                                to_dev(c.pool.block_tables), to_dev(lens), c.B, int(lens.max()), d))
+    torch.cuda.synchronize()
+    assert_out_close(to_host(out), c.decode_ref(), "noalloc decode, peaked scores")
     st, flags = hyb.hyb_device_status(clear=True)
     assert st == 0, f"device status {flags:#x}"
 

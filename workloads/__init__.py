@@ -54,6 +54,28 @@ def rows(g: np.random.Generator, shape, D: int, dtype: int) -> np.ndarray:
     return bf16_round(x) if dtype == BF16 else x
 
 
+def unit_dirs(g: np.random.Generator, H: int, D: int) -> np.ndarray:
+    """One random unit vector per head, fp32 [H][D]."""
+    u = g.standard_normal(size=(H, D)).astype(np.float64)
+    return (u / np.linalg.norm(u, axis=1, keepdims=True)).astype(np.float32)
+
+
+def directed_rows(g: np.random.Generator, coef, u: np.ndarray, D: int, dtype: int,
+                  noise: float = 1.0) -> np.ndarray:
+    """Rows x[t][h] = coef[t][h] * u[h] + noise * N(0,1)/sqrt(D), drawn in fp32 and rounded
+    once to bf16 for BF16. coef is [T] (same for every head) or [T][H]; u is [H][D].
+    Gives inputs whose attention scores follow a chosen profile along the sequence
+    (peaked or moving softmax maxima) while the values stay N(0,1)/sqrt(D)-like."""
+    coef = np.asarray(coef, dtype=np.float32)
+    if coef.ndim == 1:
+        coef = coef[:, None]
+    T, H = coef.shape[0], u.shape[0]
+    x = g.standard_normal(size=(T, H, D), dtype=np.float32)
+    x *= np.float32(noise / math.sqrt(D))
+    x += coef[:, :, None] * u[None, :, :]
+    return bf16_round(x) if dtype == BF16 else x
+
+
 def esize(dtype: int) -> int:
     return 2 if dtype == BF16 else 4
 
