@@ -1,20 +1,24 @@
 #!/usr/bin/env python3
 """Benchmark of the hybrid-attention decode hot path on GB300 (one JSON line on rank 0).
 
-Workload (default, `decode_single_layer`): 32 requests, H=32, D=128, bf16 KV, fp32 linear
-state, seq_lens ~ U{128..4096} with blocks shuffled across a pool; one step = one decode
-token for every request through one Full layer (KV append at position seq_len - 1 fused
-into the split-K paged decode, plus the split combine) and one Linear layer (in-place state
-step). Metric: req-tokens/s per layer
-= B * layers / step time. Inputs live in HBM before timing; the per-step working set
-(~1.2 GB of KV and 128 MiB of state) is far larger than L2, so no flush is needed.
+Headline workload (`hybrid_32layer`): a 32-layer hybrid model, layer types
+[full, full, full, linear] x 8, batch 64 with 80 % of the requests around 128 cached tokens
+and 20 % around 2048 (lognormal), H=32, D=128, bf16 KV in 16-token blocks shuffled across a
+pool, fp32 linear states. One step = one decode token for every request through all 32
+layers in one hyb_layer_dispatch call: each Full layer is one launch of the paged decode
+with the KV append fused in (new row at seq_len - 1 through the block table) plus its split
+combine, each Linear layer one in-place state step. Metric: req-tokens/s per layer
+= B * 32 / step time. Inputs live in HBM before timing; a step streams ~15.8 GB of KV and
+state, far more than the 129 MB L2, so no flush is needed.
 
-`value` is device time (CUDA events on the launching stream). `e2e` is the same step
-through the public dispatcher (hyb_layer_dispatch) with the step's q/k/v and metadata
-copied from pinned host memory and the outputs copied back, inside the timed region.
-`--impl reference` times the CPU oracle instead (bounded sample per step, host cores).
-With torchrun (N > 1) every rank runs its own replica (the path shards by request with
-no exchange) and rank 0 reports the aggregate.
+`value` is device time (CUDA events on the launching stream). `e2e` is the same step through
+the same public call with all 32 layers' q/k/v and the batch metadata copied from pinned host
+memory and all outputs copied back, inside the timed region. `rows` time the other
+workloads (single-layer decode batch, 131K-context decode, chunked prefill, and the
+variants), each against its own roofline and, for the four workloads of the method, beside
+the CPU oracle. `--impl reference` times the CPU oracle on the headline workload instead
+(bounded sample per step, host cores). With torchrun (N > 1) every rank runs its own
+replica (the path shards by request with no exchange) and rank 0 reports the aggregate.
 """
 from __future__ import annotations
 
@@ -42,14 +46,14 @@ UNIT = "req-tokens/s per layer"
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2500)
-    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--workload", default="decode_single_layer",
-                    choices=["decode_single_layer", "hybrid_32layer", "prefill_chunked", "long_context_decode",
+    ap.add_argument("--workload", default="hybrid_32layer",
+                    choices=["hybrid_32layer", "decode_single_layer", "prefill_chunked", "long_context_decode",
                              "sliding_window", "state_precision", "block32", "bucketing", "prefill_lengths"],
-                    help="decode_single_layer is the headline; the others are timed alone (e.g. for profiling)")
+                    help="hybrid_32layer is the headline; the others are timed alone (e.g. for profiling)")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements of the other workloads")
     return ap.parse_args()
 
@@ -174,22 +178,7 @@ def traffic_record(kernel: str, src: str):
     return rec
 
 
-# ------------------------------------------------------------------ workload
-def build_workload(seed, device):
-    import torch
-    db = W.decode_single_layer(seed)
-    B, H, D, NB, MB = db.B, db.H, db.D, db.pool.num_blocks, db.pool.max_blocks
-    g = W.rng(seed + 1)
-    wl = dict(db=db, B=B, H=H, D=D, NB=NB, MB=MB)
-    wl["kc"] = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), seed * 10 + 1, D)
-    wl["vc"] = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), seed * 10 + 2, D)
-    wl["state"] = W.device_state_(torch.empty((B, H, D, D), device=device), seed * 10 + 3, db.seq_lens, D)
-    wl["host"] = {n: W.rows(g, (B, H, D), D, W.BF16) for n in ("qf", "kf", "vf", "ql", "kl", "vl")}
-    wl["slots_h"] = g.permutation(B).astype(np.int32)
-    return wl
-
-
-# ------------------------------------------------------------------ other rows
+# ------------------------------------------------------------------ timing helpers
 def _time(fn, stream, iters, warmup=3):
     """Average device time (ms) of fn() over `iters` calls, CUDA events on `stream`."""
     import torch
@@ -218,9 +207,229 @@ def _roof(bound, achieved, peak, unit, kernel, alg, traffic=None, **extra):
     return r
 
 
-def row_long_context(hyb, device, stream, iters, seed=0):
+def _u16(t):
+    """A device bf16 tensor as host bf16 bit patterns (numpy uint16)."""
+    import torch
+    return t.cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def _dev_bf16(a, device):
+    """Host bf16 bit patterns (numpy uint16) as a device bf16 tensor."""
+    import torch
+    return torch.from_numpy(np.ascontiguousarray(a).view(np.int16)).to(device).view(torch.bfloat16)
+
+
+def _check_device(hyb):
+    st_, fl = hyb.hyb_device_status(clear=True)
+    if st_ != 0:
+        raise RuntimeError(f"device-side check flags {fl:#x}")
+
+
+# ------------------------------------------------------------------ 32-layer hybrid batch
+def build_hybrid(seed, device):
+    """The 32-layer hybrid decode batch: every layer's q/k/v drawn on the host (bf16 bit
+    patterns, [L][3][B][H][D]); each Full layer's K and V pools and each Linear layer's state
+    pool filled on the device (seeded)."""
+    import torch
+    db = W.decode_hybrid_32layer(seed)
+    lt = [int(x) for x in db.extra["layer_types"]]
+    L = len(lt)
+    B, H, D, NB, MB = db.B, db.H, db.D, db.pool.num_blocks, db.pool.max_blocks
+    g = W.rng(seed + 9)
+    qkv = W.rows(g, (L, 3, B, H, D), D, W.BF16)
+    slots = g.permutation(B).astype(np.int32)
+    kv, st = {}, {}
+    for l, t in enumerate(lt):
+        if t == 0:
+            kv[l] = tuple(W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device),
+                                         base + l, D) for base in (100, 200))
+        else:
+            st[l] = W.device_state_(torch.empty((B, H, D, D), device=device), 300 + l, db.seq_lens, D)
+    return dict(db=db, lt=lt, L=L, B=B, H=H, D=D, NB=NB, MB=MB, qkv=qkv, slots=slots, kv=kv, st=st)
+
+
+def hybrid_bytes(wl):
+    """Algorithmic bytes of one Full-layer decode launch (K and V of every cached token read
+    once, q read, out written, the new K/V rows read and written into the cache) and of one
+    whole 32-layer step (every Linear layer reads and writes its fp32 states and moves its
+    q/k/v/out rows)."""
+    B, H, D = wl["B"], wl["H"], wl["D"]
+    tokens = int(wl["db"].seq_lens.sum())
+    full = tokens * H * D * 2 * 2 + 2 * B * H * D * 2 + 4 * B * H * D * 2
+    lin = B * H * D * D * 4 * 2 + 4 * B * H * D * 2
+    n_full = sum(1 for t in wl["lt"] if t == 0)
+    return full, lin, n_full * full + (wl["L"] - n_full) * lin
+
+
+def cpu_baseline_hybrid(wl, budget_s=8.0, max_passes=20):
+    """Times the CPU oracle (as it stands) on the whole 32-layer step: all 64 requests through
+    every layer in order (Full: slot of position seq_len - 1, KV append, paged decode; Linear:
+    state step). Every layer's pools are copied to the host once first (not timed); whole
+    passes are repeated until ~budget_s of CPU work."""
+    import oracle
+    db, lt, B, L, D = wl["db"], wl["lt"], wl["B"], wl["L"], wl["D"]
+    cores = oracle.set_threads(0)
+    qkv = wl["qkv"]
+    cu = np.arange(B + 1, dtype=np.int32)
+    pos = (db.seq_lens - 1).astype(np.int32)
+    host = {l: (tuple(_u16(x) for x in wl["kv"][l]) if t == 0 else wl["st"][l].cpu().numpy()) for l, t in enumerate(lt)}
+    passes, t_used = 0, 0.0
+    while passes < 1 or (t_used < budget_s and passes < max_passes):
+        for l, t in enumerate(lt):
+            t0 = time.perf_counter()
+            if t == 0:
+                kc, vc = host[l]
+                slot = oracle.slot_mapping(db.pool.block_tables, cu, pos)
+                oracle.kv_append(qkv[l, 1], qkv[l, 2], slot, kc, vc)
+                oracle.full_decode(qkv[l, 0], kc, vc, db.pool.block_tables, db.seq_lens, D ** -0.5)
+            else:
+                oracle.linear_step(qkv[l, 0], qkv[l, 1], qkv[l, 2], host[l], wl["slots"])
+            t_used += time.perf_counter() - t0
+        passes += 1
+    del host
+    return {"value": round(passes * B * L / t_used, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"the whole step, {passes} pass(es): all {B} requests x {L} layers (24 Full: slot, KV "
+                      f"append, paged decode; 8 Linear: state step), all heads; fp64 C oracle with OpenMP over "
+                      f"(request, head); {t_used:.1f} s of CPU work (host copies of the pools made once, not timed)"}
+
+
+# ------------------------------------------------------------------ single-layer decode batch
+def build_single_layer(seed, device):
+    import torch
+    db = W.decode_single_layer(seed)
+    B, H, D, NB, MB = db.B, db.H, db.D, db.pool.num_blocks, db.pool.max_blocks
+    g = W.rng(seed + 1)
+    wl = dict(db=db, B=B, H=H, D=D, NB=NB, MB=MB)
+    wl["kc"] = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), seed * 10 + 1, D)
+    wl["vc"] = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), seed * 10 + 2, D)
+    wl["state"] = W.device_state_(torch.empty((B, H, D, D), device=device), seed * 10 + 3, db.seq_lens, D)
+    wl["host"] = {n: W.rows(g, (B, H, D), D, W.BF16) for n in ("qf", "kf", "vf", "ql", "kl", "vl")}
+    wl["slots_h"] = g.permutation(B).astype(np.int32)
+    return wl
+
+
+def cpu_baseline_decode(wl, budget_s=6.0):
+    """Times the CPU oracle (as it stands) on the single-layer decode batch: whole passes over
+    the 32 requests (slot of position seq_len - 1, KV append, paged decode; Linear step), all
+    heads, repeated until ~budget_s of CPU work."""
+    import oracle
+    db, B, D = wl["db"], wl["B"], wl["D"]
+    cores = oracle.set_threads(0)
+    kc, vc = _u16(wl["kc"]), _u16(wl["vc"])
+    st = wl["state"].cpu().numpy()
+    hq = wl["host"]
+    cu = np.arange(B + 1, dtype=np.int32)
+    pos = (db.seq_lens - 1).astype(np.int32)
+    passes, t_used = 0, 0.0
+    while passes < 1 or t_used < budget_s:
+        t0 = time.perf_counter()
+        slot = oracle.slot_mapping(db.pool.block_tables, cu, pos)
+        oracle.kv_append(hq["kf"], hq["vf"], slot, kc, vc)
+        oracle.full_decode(hq["qf"], kc, vc, db.pool.block_tables, db.seq_lens, D ** -0.5)
+        oracle.linear_step(hq["ql"], hq["kl"], hq["vl"], st, wl["slots_h"])
+        t_used += time.perf_counter() - t0
+        passes += 1
+    return {"value": round(passes * B * 2 / t_used, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"the whole step, {passes} pass(es): all {B} requests x (Full: slot, KV append, paged "
+                      f"decode; Linear step), all heads; fp64 C oracle with OpenMP over (request, head); "
+                      f"{t_used:.1f} s"}
+
+
+def row_single_layer(hyb, device, stream, iters, seed=0, cpu=True):
+    """32 requests, seq_lens ~ U{128..4096}: one Full layer (paged decode with the KV append
+    fused, plus the split combine) and one Linear layer (in-place state step). The per-op
+    split comes from a second pass with an event between the two ops."""
+    import torch
+    hbm, _, _ = measured_peaks()
+    wl = build_single_layer(seed, device)
+    B, H, D, NB, MB, db = wl["B"], wl["H"], wl["D"], wl["NB"], wl["MB"], wl["db"]
+    d = hyb.dims(H, D, NB, MB, W.BF16)
+    x = {n: _dev_bf16(a, device) for n, a in wl["host"].items()}
+    bt = torch.from_numpy(db.pool.block_tables).to(device)
+    lens = torch.from_numpy(db.seq_lens).to(device)
+    slots = torch.from_numpy(wl["slots_h"]).to(device)
+    msl = int(db.seq_lens.max())
+    ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, msl, d)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=device)
+    out_f, out_l = (torch.empty((B, H, D), dtype=torch.bfloat16, device=device) for _ in range(2))
+    sh = stream.cuda_stream
+    dec = lambda: hyb.check(hyb.hyb_paged_attn_decode_append(out_f, x["qf"], x["kf"], x["vf"], None, wl["kc"],
+                                                             wl["vc"], bt, lens, B, msl, d, ws, ws_n, sh))
+    lin = lambda: hyb.check(hyb.hyb_linear_attn_step(out_l, x["ql"], x["kl"], x["vl"], wl["state"], B, slots,
+                                                     B, H, D, W.BF16, sh))
+    t_step = _time(lambda: (dec(), lin()), stream, iters)
+    # per-op split: an event between the ops (it holds back the programmatic early launch of
+    # the next kernel, so this pass runs a little slower than the step above)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(iters)]
+    with torch.cuda.stream(stream):
+        for e in evs:
+            e[0].record(stream)
+            dec()
+            e[1].record(stream)
+            lin()
+            e[2].record(stream)
+    stream.synchronize()
+    _check_device(hyb)
+    t_dec = float(np.mean([e[0].elapsed_time(e[1]) for e in evs]))
+    t_lin = float(np.mean([e[1].elapsed_time(e[2]) for e in evs]))
+    tokens = int(db.seq_lens.sum())
+    dec_bytes = tokens * H * D * 2 * 2 + 2 * B * H * D * 2 + 4 * B * H * D * 2
+    lin_bytes = B * H * D * D * 4 * 2
+    res = {"workload": "decode_single_layer: 32 requests, H=32, D=128, block 16, seq_lens U{128..4096}, "
+                       "1 Full paged-decode (KV append fused) + 1 Linear step",
+           "value": round(B * 2 / (t_step * 1e-3), 1), "unit": UNIT, "ms_per_step": round(t_step, 5),
+           "kv_tokens": tokens,
+           "ms": {"paged_decode": round(t_dec, 5), "linear_step": round(t_lin, 5)},
+           "roofline": _roof("hbm", dec_bytes / (t_dec * 1e-3) / 1e9, hbm, "GB/s",
+                             "paged_decode with the KV append fused (split-K + combine)", dec_bytes,
+                             traffic=_traffic("paged_decode", "decode.cu")),
+           "linear_step": _roof("hbm", lin_bytes / (t_lin * 1e-3) / 1e9, hbm, "GB/s",
+                                "linear_step (in the step: the decode before it evicts L2)", lin_bytes,
+                                traffic=_traffic("linear_step", "linear.cu")),
+           "l2": "no flush: per-step working set %.2f GB > 129 MB L2" % ((dec_bytes + lin_bytes) / 1e9)}
+    if cpu:
+        res["cpu_baseline"] = cpu_baseline_decode(wl)
+    del wl, x
+    torch.cuda.empty_cache()
+    return res
+
+
+def cpu_baseline_long(db, kc, vc, q_h, st, H, D, budget_s=6.0, max_passes=10):
+    """Times the CPU oracle (as it stands) on the whole 131K-context step: each of the 8
+    requests through the paged decode over its 8192 blocks and the Linear step. Each
+    request's blocks are gathered on the device and copied to the host once first (not
+    timed), in logical order; whole passes repeat until ~budget_s of CPU work."""
+    import torch
+    import oracle
+    cores = oracle.set_threads(0)
+    B = db.B
+    st_h = st.cpu().numpy()
+    kv = []
+    for b in range(B):
+        nb = int(db.pool.blocks_per_req[b])
+        idx = torch.from_numpy(db.pool.block_tables[b, :nb].astype(np.int64)).to(kc.device)
+        kv.append((_u16(kc.index_select(0, idx)), _u16(vc.index_select(0, idx)), np.arange(nb, dtype=np.int32)[None, :]))
+    passes, t_used = 0, 0.0
+    while passes < 1 or (t_used < budget_s and passes < max_passes):
+        for b in range(B):
+            kb, vb, tbl = kv[b]
+            t0 = time.perf_counter()
+            oracle.full_decode(q_h[b:b + 1], kb, vb, tbl, db.seq_lens[b:b + 1], D ** -0.5)
+            oracle.linear_step(q_h[b:b + 1], q_h[b:b + 1], q_h[b:b + 1], st_h, np.array([b], np.int32))
+            t_used += time.perf_counter() - t0
+        passes += 1
+    del kv
+    return {"value": round(passes * B * 2 / t_used, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"the whole step, {passes} pass(es): all {B} requests x (paged decode over 131072 tokens, "
+                      f"Linear step), all {H} heads; fp64 C oracle with OpenMP over (request, head); {t_used:.1f} s "
+                      f"(each request's blocks gathered to the host once first, not timed)"}
+
+
+def row_long_context(hyb, device, stream, iters, seed=0, cpu=True):
     """8 requests x 131072 tokens: split-K paged decode over 8192 random blocks each, and the
-    Linear step on 8 x 32 x 128 x 128 fp32 states."""
+    Linear step on 8 x 32 x 128 x 128 fp32 states. The Linear step's states (16.8 MB per
+    batch) would stay in L2 across back-to-back calls, so it rotates over 16 state pools
+    (268 MB, twice the L2)."""
     import torch
     hbm, _, _ = measured_peaks()
     db = W.decode_long_context(seed)
@@ -228,9 +437,11 @@ def row_long_context(hyb, device, stream, iters, seed=0):
     d = hyb.dims(H, D, NB, db.pool.max_blocks, W.BF16)
     kc = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), 51, D)
     vc = W.device_rows_(torch.empty_like(kc), 52, D)
-    st = W.device_state_(torch.empty((B, H, D, D), device=device), 53, db.seq_lens, D)
+    NR = 16
+    sts = [W.device_state_(torch.empty((B, H, D, D), device=device), 53 + i, db.seq_lens, D) for i in range(NR)]
     g = W.rng(seed + 5)
-    q = torch.from_numpy(W.rows(g, (B, H, D), D, W.BF16).view(np.int16)).to(device).view(torch.bfloat16)
+    q_h = W.rows(g, (B, H, D), D, W.BF16)
+    q = _dev_bf16(q_h, device)
     out = torch.empty_like(q)
     bt = torch.from_numpy(db.pool.block_tables).to(device)
     lens = torch.from_numpy(db.seq_lens).to(device)
@@ -239,86 +450,76 @@ def row_long_context(hyb, device, stream, iters, seed=0):
     ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, n, d)
     ws = torch.empty(ws_n, dtype=torch.uint8, device=device)
     sh = stream.cuda_stream
-    t_dec = _time(lambda: hyb.check(hyb.hyb_paged_attn_decode(out, q, kc, vc, bt, lens, B, n, d, ws, ws_n, sh)), stream, iters)
-    t_lin = _time(lambda: hyb.check(hyb.hyb_linear_attn_step(out, q, q, q, st, B, slots, B, H, D, W.BF16, sh)), stream, iters)
+    t_dec = _time(lambda: hyb.check(hyb.hyb_paged_attn_decode(out, q, kc, vc, bt, lens, B, n, d, ws, ws_n, sh)),
+                  stream, iters)
+    it = [0]
+
+    def lin():
+        it[0] += 1
+        hyb.check(hyb.hyb_linear_attn_step(out, q, q, q, sts[it[0] % NR], B, slots, B, H, D, W.BF16, sh))
+    t_lin = _time(lin, stream, max(iters, 4 * NR))
+    _check_device(hyb)
     dec_bytes = int(db.seq_lens.sum()) * H * D * 4 + 2 * B * H * D * 2
     lin_bytes = B * H * D * D * 8
     res = {"workload": "long_context_decode: 8 requests x 131072 tokens, H=32, D=128, 8192 random blocks each",
            "value": round(B * 2 / ((t_dec + t_lin) * 1e-3), 1), "unit": UNIT,
            "ms": {"paged_decode": round(t_dec, 4), "linear_step": round(t_lin, 4)},
-           "roofline": _roof("hbm", dec_bytes / (t_dec * 1e-3) / 1e9, hbm, "GB/s", "paged_decode (split-K + combine)", dec_bytes),
-           "linear_step": _roof("hbm", lin_bytes / (t_lin * 1e-3) / 1e9, hbm, "GB/s", "linear_step", lin_bytes)}
-    del kc, vc, st
+           "roofline": _roof("hbm", dec_bytes / (t_dec * 1e-3) / 1e9, hbm, "GB/s", "paged_decode (split-K + combine)",
+                             dec_bytes),
+           "linear_step": _roof("hbm", lin_bytes / (t_lin * 1e-3) / 1e9, hbm, "GB/s",
+                                f"linear_step, rotating over {NR} state pools ({NR * lin_bytes // 2 / 1e6:.0f} MB)",
+                                lin_bytes)}
+    if cpu:
+        res["cpu_baseline"] = cpu_baseline_long(db, kc, vc, q_h, sts[0], H, D)
+    del kc, vc, sts
     torch.cuda.empty_cache()
     return res
 
 
-def row_hybrid_32layer(hyb, device, stream, iters, seed=0):
-    """32 layers [F,F,F,Lin] x 8, batch 64 (80% ~128, 20% ~2048 tokens): one decode token per
-    request through all layers via hyb_layer_dispatch."""
-    import torch
-    hbm, _, _ = measured_peaks()
-    db = W.decode_hybrid_32layer(seed)
-    lt = db.extra["layer_types"]
-    B, H, D, NB, MB = db.B, db.H, db.D, db.pool.num_blocks, db.pool.max_blocks
-    d = hyb.dims(H, D, NB, MB, W.BF16)
-    g = W.rng(seed + 9)
-    mk = lambda: torch.from_numpy(W.rows(g, (B, H, D), D, W.BF16).view(np.int16)).to(device).view(torch.bfloat16)
-    keep, ios = [], []
-    for l, t in enumerate(lt):
-        q, k, v, o = mk(), mk(), mk(), torch.empty((B, H, D), dtype=torch.bfloat16, device=device)
-        if t == 0:
-            kc = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), 100 + l, D)
-            vc = W.device_rows_(torch.empty_like(kc), 200 + l, D)
-            keep += [q, k, v, o, kc, vc]
-            ios.append(hyb.layer_io(o, q, k, v, kc, vc))
-        else:
-            sp = W.device_state_(torch.empty((B, H, D, D), device=device), 300 + l, db.seq_lens, D)
-            keep += [q, k, v, o, sp]
-            ios.append(hyb.layer_io(o, q, k, v, state_pool=sp, num_state_slots=B))
-    bt = torch.from_numpy(db.pool.block_tables).to(device)
-    lens = torch.from_numpy(db.seq_lens).to(device)
-    slots = torch.from_numpy(g.permutation(B).astype(np.int32)).to(device)
-    msl = int(db.seq_lens.max())
-    ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, msl, d)
-    ws = torch.empty(ws_n, dtype=torch.uint8, device=device)
-    # no slot mapping: each Full layer appends its new rows at seq_len - 1 via the block table
-    meta = hyb.batch_meta(B, B, seq_lens=lens, block_tables=bt, state_slots=slots, max_seq_len=msl)
-    sh = stream.cuda_stream
-
-    def step():
-        hyb.check(hyb.hyb_layer_dispatch(lt, 32, 0, ios, meta, d, 64, ws, ws_n, sh))
-    hyb.hyb_launch_count(reset=True)
-    step()
-    launches = hyb.hyb_launch_count(reset=True)
-    t = _time(step, stream, iters)
-    # the same step captured once into a CUDA graph and replayed (no per-launch host work)
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.stream(stream):
-        step()                                   # every first-call set-up done before capture
-        stream.synchronize()
-        with torch.cuda.graph(graph, stream=stream):
-            step()
-    t_graph = _time(graph.replay, stream, iters)
-    n_full, n_lin = int((lt == 0).sum()), int((lt == 1).sum())
-    alg = n_full * (int(db.seq_lens.sum()) * H * D * 4 + 2 * B * H * D * 2) + n_lin * B * H * D * D * 8
-    res = {"workload": "hybrid_32layer: [full,full,full,linear] x 8, batch 64, 80% ~lognormal(128) / 20% ~lognormal(2048)",
-           "value": round(B * 32 / (t * 1e-3), 1), "unit": UNIT, "ms_per_step": round(t, 4),
-           "launches_per_step": int(launches),
-           "roofline": _roof("hbm", alg / (t * 1e-3) / 1e9, hbm, "GB/s", "whole 32-layer step (dispatch)", alg),
-           "cuda_graph": {"value": round(B * 32 / (t_graph * 1e-3), 1), "ms_per_step": round(t_graph, 4),
-                          "roofline": _roof("hbm", alg / (t_graph * 1e-3) / 1e9, hbm, "GB/s",
-                                            "whole 32-layer step (graph replay)", alg)}}
-    del graph
-    del keep, ios
-    torch.cuda.empty_cache()
-    return res
+def cpu_baseline_prefill(pb, k0, v0, q0, ql0, kl0, vl0, H, D, every=4):
+    """Times the CPU oracle (as it stands) on a labelled subset of the chunked-prefill workload
+    and extrapolates by work: request 0's slot mapping and KV append (all 8192 rows) and its
+    causal prefill on every `every`-th query row (a uniform sample of the causal triangle);
+    request 0's Linear prefill as the token recurrence over all 8192 tokens (all heads). The
+    full workload is 8 such requests and all query rows."""
+    import oracle
+    cores = oracle.set_threads(0)
+    n = int(pb.q_lens[0])
+    nb = (n + 15) // 16
+    g = W.rng(77)
+    tbl = g.permutation(nb).astype(np.int32)[None, :]
+    kc = np.zeros((nb, H, 16, D), np.uint16)
+    vc = np.zeros_like(kc)
+    cu = np.array([0, n], np.int32)
+    rows = np.arange(every - 1, n, every, dtype=np.int32)
+    t0 = time.perf_counter()
+    slot = oracle.slot_mapping(tbl, cu)
+    oracle.kv_append(k0, v0, slot, kc, vc)
+    t_app = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.full_prefill(q0, kc, vc, tbl, cu, None, D ** -0.5, rows=rows)
+    t_rows = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    oracle.linear_recurrence(ql0, kl0, vl0, cu)
+    t_lin = time.perf_counter() - t0
+    Bn = len(pb.q_lens)
+    keys_all = float(sum(m * (m + 1) / 2 for m in pb.q_lens.astype(np.float64)))
+    keys_rows = float((rows + 1).astype(np.float64).sum())
+    est = Bn * t_app + t_rows * keys_all / keys_rows + Bn * t_lin
+    T = int(pb.q_lens.sum())
+    return {"value": round(T * 2 / est, 2), "unit": "prompt tokens/s per layer", "cores": cores, "kind": "oracle",
+            "extrapolated": True,
+            "sample": f"request 0 of {Bn}: slot mapping + KV append of its {n} rows ({t_app:.2f} s), causal prefill "
+                      f"of every {every}th query row ({len(rows)} rows, {t_rows:.1f} s), token recurrence over its "
+                      f"{n} tokens ({t_lin:.1f} s), all {H} heads; extrapolated by work to {Bn} requests and every "
+                      f"row ({est:.0f} s estimated); fp64 C oracle with OpenMP over (request, head)"}
 
 
-def row_prefill(hyb, device, stream, iters, seed=0):
+def row_prefill(hyb, device, stream, iters, seed=0, cpu=True):
     """8 requests x 8192-token prompts, H=32, D=128: Full layer = slot mapping + KV append +
     tensor-core causal prefill over the paged cache; Linear layer = tensor-core chunked
-    prefill (chunk 64) from a zero state."""
+    prefill (interface chunk 64; the kernel computes 128-token chunks, which the chunk form
+    allows since it equals the recurrence for any cut) from a zero state."""
     import torch
     hbm, tf, _ = measured_peaks()
     pb = W.prefill_chunked(seed)
@@ -341,39 +542,44 @@ def row_prefill(hyb, device, stream, iters, seed=0):
     L = int(pb.q_lens.max())
     t_slot = _time(lambda: hyb.check(hyb.hyb_slot_mapping(slot, bt, cu, None, B, T, d, sh)), stream, iters)
     t_app = _time(lambda: hyb.check(hyb.hyb_paged_kv_append(k, v, slot, T, kc, vc, d, sh)), stream, iters)
-    t_pf = _time(lambda: hyb.check(hyb.hyb_paged_attn_prefill_causal(out, q, kc, vc, bt, cu, None, B, T, L, d, sh)), stream, iters)
+    t_pf = _time(lambda: hyb.check(hyb.hyb_paged_attn_prefill_causal(out, q, kc, vc, bt, cu, None, B, T, L, d, sh)),
+                 stream, iters)
+    lws = torch.empty(hyb.hyb_linear_attn_chunked_prefill_workspace_size(), dtype=torch.uint8, device=device)
     t_lin = _time(lambda: hyb.check(hyb.hyb_linear_attn_chunked_prefill(lo, ql, kl, vl, cu, None, st, B, slots, reset,
-                                                                        B, T, L, H, D, pb.chunk, W.BF16, sh)), stream, iters)
-    st_, fl = hyb.hyb_device_status(clear=True)
-    if st_ != 0:
-        raise RuntimeError(f"device-side check flags {fl:#x}")
+                                                                        B, T, L, H, D, pb.chunk, W.BF16, lws,
+                                                                        lws.numel(), sh)),
+                  stream, iters)
+    _check_device(hyb)
     n = pb.q_lens.astype(np.float64)
     pf_flops = 4.0 * H * D * float((n * (n + 1) / 2).sum())              # QK^T + PV over the causal triangle
-    lin_flops = T * H * (4.0 * pb.chunk * D + 4.0 * D * D)                # per token-head: 4CD + 4D^2
+    lin_flops = T * H * (4.0 * pb.chunk * D + 4.0 * D * D)                # per token-head: 4CD + 4D^2 at C = 64
     lin_bytes = 4 * T * H * D * 2 + B * H * D * D * 4                     # q,k,v read, o written, state written
     app_bytes = 2 * 2 * T * H * D * 2
     ai = lin_flops / lin_bytes
     lin_gbs = lin_bytes / (t_lin * 1e-3) / 1e9
     lin_tf = lin_flops / (t_lin * 1e-3) / 1e12
-    res = {"workload": "prefill_chunked: 8 requests x 8192-token prompts, H=32, D=128, chunk 64",
+    res = {"workload": "prefill_chunked: 8 requests x 8192-token prompts, H=32, D=128, interface chunk 64 "
+                       "(computed as 128-token chunks)",
            "value": round(T * 2 / ((t_slot + t_app + t_pf + t_lin) * 1e-3), 1), "unit": "prompt tokens/s per layer",
            "ms": {"slot_mapping": round(t_slot, 4), "kv_append": round(t_app, 4), "prefill_causal": round(t_pf, 4),
                   "linear_chunked_prefill": round(t_lin, 4)},
            "roofline": _roof("tensor", pf_flops / (t_pf * 1e-3) / 1e12, tf, "TFLOP/s", "prefill_tc_kernel (causal, paged)",
                              pf_flops, traffic=_traffic("prefill_tc", "prefill_tc.cu"),
                              peak_source="measured bf16_tflops (burst)"),
-           "linear_chunked_prefill": _roof("hbm", lin_gbs, hbm, "GB/s", "linear_prefill_tc_kernel", lin_bytes,
-                                           traffic=_traffic("linear_prefill_tc", "linear_tc.cu"),
+           "linear_chunked_prefill": _roof("hbm", lin_gbs, hbm, "GB/s", "linear_prefill_tc_kernel (128-token chunks)",
+                                           lin_bytes, traffic=_traffic("linear_prefill_tc", "linear_tc.cu"),
                                            tflops=round(lin_tf, 1), tensor_frac=round(lin_tf / tf, 4),
                                            arithmetic_intensity=round(ai, 1),
                                            frac_of_min_peak_ai_bw=round(lin_tf / min(tf, ai * hbm / 1e3), 4)),
            "kv_append": _roof("hbm", app_bytes / (t_app * 1e-3) / 1e9, hbm, "GB/s", "kv_append_kernel", app_bytes,
                               traffic=_traffic("kv_append", "append.cu"))}
+    if cpu:
+        n0 = int(pb.q_lens[0])
+        res["cpu_baseline"] = cpu_baseline_prefill(pb, _u16(k[:n0]), _u16(v[:n0]), _u16(q[:n0]), _u16(ql[:n0]),
+                                                   _u16(kl[:n0]), _u16(vl[:n0]), H, D)
     del q, k, v, ql, kl, vl, out, lo, kc, vc, st
     torch.cuda.empty_cache()
     return res
-
-
 def row_sliding_window(hyb, device, stream, iters, seed=0):
     """Sliding-window Full layers: decode of 8 requests x 131072 cached tokens with window
     8192 (only the window's blocks are read), and tensor-core causal prefill of 8 x 8192
@@ -432,67 +638,6 @@ def row_sliding_window(hyb, device, stream, iters, seed=0):
     torch.cuda.empty_cache()
     return res
 
-
-def row_state_precision(hyb, device, stream, iters, seed=0):
-    """Linear decode step with the fp32 state the pages prescribe vs bf16 and fp16 state
-    pools: time per step on 32 requests x 32 heads x 128 x 128, and the output drift of the
-    16-bit states against the fp32 state over 16384 decode steps (4 requests x 4 heads,
-    fp32 q/k/v, zero initial state)."""
-    import torch
-    hbm, _, _ = measured_peaks()
-    B, H, D = 32, 32, 128
-    g = W.rng(seed + 11)
-    mk = lambda: torch.from_numpy(W.rows(g, (B, H, D), D, W.BF16).view(np.int16)).to(device).view(torch.bfloat16)
-    q, k, v = mk(), mk(), mk()
-    out = torch.empty_like(q)
-    slots = torch.arange(B, dtype=torch.int32, device=device)
-    st32 = W.device_state_(torch.empty((B, H, D, D), device=device), 81, np.full(B, 2048), D)
-    st16 = {sd: st32.to(torch.bfloat16 if sd == W.BF16 else torch.float16) for sd in (W.BF16, hyb.HYB_F16)}
-    sh = stream.cuda_stream
-    t = {"fp32": _time(lambda: hyb.check(hyb.hyb_linear_attn_step(out, q, k, v, st32, B, slots, B, H, D, W.BF16, sh)),
-                       stream, iters)}
-    for sd, name in ((W.BF16, "bf16"), (hyb.HYB_F16, "fp16")):
-        t[name] = _time(lambda: hyb.check(hyb.hyb_linear_attn_step_lowp(out, q, k, v, st16[sd], sd, B, slots, B, H, D,
-                                                                        W.BF16, sh)), stream, iters)
-    byt = {"fp32": B * H * D * D * 8, "bf16": B * H * D * D * 4, "fp16": B * H * D * D * 4}
-    del st32, st16
-    # drift: the same fp32 q/k/v stream through the three state types
-    Bd, Hd, T = 4, 4, 16384
-    qs = W.device_rows_(torch.empty((T, Bd, Hd, D), device=device), 82, D)
-    ks = W.device_rows_(torch.empty_like(qs), 83, D)
-    vs = W.device_rows_(torch.empty_like(qs), 84, D)
-    outs = {n: torch.empty_like(qs) for n in ("fp32", "bf16", "fp16")}
-    pools = {"fp32": torch.zeros((Bd, Hd, D, D), device=device),
-             "bf16": torch.zeros((Bd, Hd, D, D), dtype=torch.bfloat16, device=device),
-             "fp16": torch.zeros((Bd, Hd, D, D), dtype=torch.float16, device=device)}
-    sl = torch.arange(Bd, dtype=torch.int32, device=device)
-    with torch.cuda.stream(stream):
-        for i in range(T):
-            hyb.check(hyb.hyb_linear_attn_step(outs["fp32"][i], qs[i], ks[i], vs[i], pools["fp32"], Bd, sl, Bd, Hd, D,
-                                               W.F32, sh))
-            hyb.check(hyb.hyb_linear_attn_step_lowp(outs["bf16"][i], qs[i], ks[i], vs[i], pools["bf16"], W.BF16, Bd, sl,
-                                                    Bd, Hd, D, W.F32, sh))
-            hyb.check(hyb.hyb_linear_attn_step_lowp(outs["fp16"][i], qs[i], ks[i], vs[i], pools["fp16"], hyb.HYB_F16, Bd,
-                                                    sl, Bd, Hd, D, W.F32, sh))
-    stream.synchronize()
-    st_, fl = hyb.hyb_device_status(clear=True)
-    if st_ != 0:
-        raise RuntimeError(f"device-side check flags {fl:#x}")
-    drift = {}
-    for n in ("bf16", "fp16"):
-        drift[n] = {}
-        for tt in (256, 1024, 4096, 16384):
-            ref = outs["fp32"][tt - 64:tt]
-            drift[n][str(tt)] = float((outs[n][tt - 64:tt] - ref).abs().max() / ref.abs().max())
-    del qs, ks, vs, outs, pools
-    torch.cuda.empty_cache()
-    return {"workload": "state_precision: linear step, 32 requests x 32 heads x 128 x 128; drift over 16384 steps",
-            "value": round(B / (t["fp32"] * 1e-3), 1), "unit": "req-tokens/s per layer (fp32 state linear step)",
-            "ms": {n: round(x, 4) for n, x in t.items()},
-            "roofline": {n: _roof("hbm", byt[n] / (t[n] * 1e-3) / 1e9, hbm, "GB/s", f"linear step, {n} state", byt[n])
-                         for n in t},
-            "drift_vs_fp32_state": {"metric": "max |o - o_fp32| / max |o_fp32| over the 64 steps before t",
-                                    "steps": T, **drift}}
 
 
 def row_block32(hyb, device, stream, iters, seed=0):
@@ -660,10 +805,85 @@ def row_prefill_lengths(hyb, device, stream, iters, seed=0):
     return res
 
 
-ROWS = {"long_context_decode": row_long_context, "hybrid_32layer": row_hybrid_32layer,
+def row_state_precision(hyb, device, stream, iters, seed=0):
+    """Linear decode step with the fp32 state the pages prescribe vs bf16 and fp16 state
+    pools: time per step on 32 requests x 32 heads x 128 x 128, and the output drift of the
+    16-bit states against the fp32 state over 16384 decode steps (4 requests x 4 heads,
+    fp32 q/k/v, zero initial state)."""
+    import torch
+    hbm, _, _ = measured_peaks()
+    B, H, D = 32, 32, 128
+    g = W.rng(seed + 11)
+    mk = lambda: torch.from_numpy(W.rows(g, (B, H, D), D, W.BF16).view(np.int16)).to(device).view(torch.bfloat16)
+    q, k, v = mk(), mk(), mk()
+    out = torch.empty_like(q)
+    slots = torch.arange(B, dtype=torch.int32, device=device)
+    # one pool per state type is 67 MB (fp32) or 34 MB (16-bit): back-to-back calls would be
+    # served from the 129 MB L2, so each type rotates over pools totalling 268 MB
+    st32 = [W.device_state_(torch.empty((B, H, D, D), device=device), 81 + i, np.full(B, 2048), D) for i in range(4)]
+    st16 = {sd: [st32[i % 4].to(torch.bfloat16 if sd == W.BF16 else torch.float16) for i in range(8)]
+            for sd in (W.BF16, hyb.HYB_F16)}
+    sh = stream.cuda_stream
+    it = [0]
+
+    def step32():
+        it[0] += 1
+        hyb.check(hyb.hyb_linear_attn_step(out, q, k, v, st32[it[0] % 4], B, slots, B, H, D, W.BF16, sh))
+
+    def step16(sd):
+        it[0] += 1
+        hyb.check(hyb.hyb_linear_attn_step_lowp(out, q, k, v, st16[sd][it[0] % 8], sd, B, slots, B, H, D, W.BF16, sh))
+    n_it = max(iters, 32)
+    t = {"fp32": _time(step32, stream, n_it)}
+    for sd, name in ((W.BF16, "bf16"), (hyb.HYB_F16, "fp16")):
+        t[name] = _time(lambda: step16(sd), stream, n_it)
+    byt = {"fp32": B * H * D * D * 8, "bf16": B * H * D * D * 4, "fp16": B * H * D * D * 4}
+    del st32, st16
+    # drift: the same fp32 q/k/v stream through the three state types
+    Bd, Hd, T = 4, 4, 16384
+    qs = W.device_rows_(torch.empty((T, Bd, Hd, D), device=device), 82, D)
+    ks = W.device_rows_(torch.empty_like(qs), 83, D)
+    vs = W.device_rows_(torch.empty_like(qs), 84, D)
+    outs = {n: torch.empty_like(qs) for n in ("fp32", "bf16", "fp16")}
+    pools = {"fp32": torch.zeros((Bd, Hd, D, D), device=device),
+             "bf16": torch.zeros((Bd, Hd, D, D), dtype=torch.bfloat16, device=device),
+             "fp16": torch.zeros((Bd, Hd, D, D), dtype=torch.float16, device=device)}
+    sl = torch.arange(Bd, dtype=torch.int32, device=device)
+    with torch.cuda.stream(stream):
+        for i in range(T):
+            hyb.check(hyb.hyb_linear_attn_step(outs["fp32"][i], qs[i], ks[i], vs[i], pools["fp32"], Bd, sl, Bd, Hd, D,
+                                               W.F32, sh))
+            hyb.check(hyb.hyb_linear_attn_step_lowp(outs["bf16"][i], qs[i], ks[i], vs[i], pools["bf16"], W.BF16, Bd, sl,
+                                                    Bd, Hd, D, W.F32, sh))
+            hyb.check(hyb.hyb_linear_attn_step_lowp(outs["fp16"][i], qs[i], ks[i], vs[i], pools["fp16"], hyb.HYB_F16, Bd,
+                                                    sl, Bd, Hd, D, W.F32, sh))
+    stream.synchronize()
+    st_, fl = hyb.hyb_device_status(clear=True)
+    if st_ != 0:
+        raise RuntimeError(f"device-side check flags {fl:#x}")
+    drift = {}
+    for n in ("bf16", "fp16"):
+        drift[n] = {}
+        for tt in (256, 1024, 4096, 16384):
+            ref = outs["fp32"][tt - 64:tt]
+            drift[n][str(tt)] = float((outs[n][tt - 64:tt] - ref).abs().max() / ref.abs().max())
+    del qs, ks, vs, outs, pools
+    torch.cuda.empty_cache()
+    return {"workload": "state_precision: linear step, 32 requests x 32 heads x 128 x 128; drift over 16384 steps",
+            "value": round(B / (t["fp32"] * 1e-3), 1), "unit": "req-tokens/s per layer (fp32 state linear step)",
+            "ms": {n: round(x, 4) for n, x in t.items()},
+            "roofline": {n: _roof("hbm", byt[n] / (t[n] * 1e-3) / 1e9, hbm, "GB/s",
+                                  f"linear step, {n} state, rotating over pools totalling 268 MB", byt[n])
+                         for n in t},
+            "drift_vs_fp32_state": {"metric": "max |o - o_fp32| / max |o_fp32| over the 64 steps before t",
+                                    "steps": T, **drift}}
+
+
+ROWS = {"decode_single_layer": row_single_layer, "long_context_decode": row_long_context,
         "prefill_chunked": row_prefill, "sliding_window": row_sliding_window,
         "state_precision": row_state_precision, "block32": row_block32, "bucketing": row_bucketing}
 EXTRA_ROWS = {"prefill_lengths": row_prefill_lengths}   # --workload only, not in the default rows
+CPU_ROWS = ("decode_single_layer", "long_context_decode", "prefill_chunked")   # rows timed beside the oracle
 
 
 def bench_ours(args, dist):
@@ -677,53 +897,62 @@ def bench_ours(args, dist):
 
     torch.cuda.set_device(dist.local)
     device = torch.device("cuda", dist.local)
-    if args.workload != "decode_single_layer":          # one other workload, timed alone
+    if args.workload != "hybrid_32layer":               # one other workload, timed alone
         stream = torch.cuda.Stream(device=device)
-        r = {**ROWS, **EXTRA_ROWS}[args.workload](hyb, device, stream, max(args.steps, 1), args.seed + dist.rank)
+        fn = {**ROWS, **EXTRA_ROWS}[args.workload]
+        kw = {"cpu": False} if args.workload in CPU_ROWS else {}
+        r = fn(hyb, device, stream, max(args.steps, 1), args.seed + dist.rank, **kw)
         r.update({"metric": METRIC, "n_gpus": dist.world, "steps": args.steps, "warmup": 3,
                   "higher_is_better": True, "dtype": "bf16", "data": "synthetic"})
         return r
-    wl = build_workload(args.seed + dist.rank, device)
-    B, H, D, NB, MB, db = wl["B"], wl["H"], wl["D"], wl["NB"], wl["MB"], wl["db"]
+    wl = build_hybrid(args.seed + dist.rank, device)
+    db, lt, L, B, H, D, NB, MB = (wl[n] for n in ("db", "lt", "L", "B", "H", "D", "NB", "MB"))
     d = hyb.dims(H, D, NB, MB, W.BF16)
-    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if a.dtype == np.uint16 else a).to(device)
-    bf = lambda a: dev(a).view(torch.bfloat16) if a.dtype == np.uint16 else dev(a)
-    x = {n: bf(a) for n, a in wl["host"].items()}
-    bt = dev(db.pool.block_tables)
-    lens = dev(db.seq_lens)
-    slots = dev(wl["slots_h"])
+    qkv = _dev_bf16(wl["qkv"], device)                  # [L][3][B][H][D]
+    out = torch.empty((L, B, H, D), dtype=torch.bfloat16, device=device)
+    bt = torch.from_numpy(db.pool.block_tables).to(device)
+    lens = torch.from_numpy(db.seq_lens).to(device)
+    slots = torch.from_numpy(wl["slots"]).to(device)
     msl = int(db.seq_lens.max())
     ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, msl, d)
     ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device=device)
-    out_f = torch.empty((B, H, D), dtype=torch.bfloat16, device=device)
-    out_l = torch.empty_like(out_f)
     stream = torch.cuda.Stream(device=device)
     sh = stream.cuda_stream
-    L = 2
-    n_ops = 2
-    names = ["paged_decode", "linear_step"]
 
-    def step(ev=None):
-        if ev: ev[0].record(stream)
-        # Full layer: KV append (at position seq_len - 1 through the block table) and paged
-        # decode in one launch, plus the split combine
-        hyb.check(hyb.hyb_paged_attn_decode_append(out_f, x["qf"], x["kf"], x["vf"], None, wl["kc"], wl["vc"],
-                                                   bt, lens, B, msl, d, ws, ws_n, sh))
-        if ev: ev[1].record(stream)
-        hyb.check(hyb.hyb_linear_attn_step(out_l, x["ql"], x["kl"], x["vl"], wl["state"], B, slots, B, H, D, W.BF16, sh))
-        if ev: ev[2].record(stream)
+    def layer_ios(qkv_t, out_t):
+        return [hyb.layer_io(out_t[l], qkv_t[l, 0], qkv_t[l, 1], qkv_t[l, 2], *wl["kv"][l]) if t == 0 else
+                hyb.layer_io(out_t[l], qkv_t[l, 0], qkv_t[l, 1], qkv_t[l, 2], state_pool=wl["st"][l],
+                             num_state_slots=B)
+                for l, t in enumerate(lt)]
+    ios = layer_ios(qkv, out)
+    # no slot mapping: each Full layer appends its new rows at seq_len - 1 through the block table
+    meta = hyb.batch_meta(B, B, seq_lens=lens, block_tables=bt, state_slots=slots, max_seq_len=msl)
 
-    for _ in range(args.warmup):
-        step()
+    def step():
+        hyb.check(hyb.hyb_layer_dispatch(lt, L, 0, ios, meta, d, 64, ws, ws_n, sh))
+
+    def step_by_layer(ev):
+        """The launches of step(), one public call per layer, with an event after each layer."""
+        ev[0].record(stream)
+        for l, t in enumerate(lt):
+            if t == 0:
+                hyb.check(hyb.hyb_paged_attn_decode_append(out[l], qkv[l, 0], qkv[l, 1], qkv[l, 2], None,
+                                                           *wl["kv"][l], bt, lens, B, msl, d, ws, ws_n, sh))
+            else:
+                hyb.check(hyb.hyb_linear_attn_step(out[l], qkv[l, 0], qkv[l, 1], qkv[l, 2], wl["st"][l], B, slots,
+                                                   B, H, D, W.BF16, sh))
+            ev[l + 1].record(stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
     torch.cuda.synchronize()
-    # An event recorded between two kernels keeps the second from launching while the first
-    # drains (programmatic dependent launch), so per-op events would slow the step they
-    # measure (0.222 against 0.205 ms here). One event pair brackets all K steps for the
-    # step time; every INSTR-th step also carries per-op events for the breakdown and the
-    # decode kernel's roofline.
-    INSTR = 8
-    instr = [s for s in range(args.steps) if s % INSTR == 0]
-    evs = {s: [torch.cuda.Event(enable_timing=True) for _ in range(n_ops + 1)] for s in instr}
+    # An event between two kernels holds back the early (programmatic dependent) launch of the
+    # second, so per-layer events slow the step they time. One event pair brackets all K
+    # steps for the step time; every INSTR-th step runs layer by layer with an event after
+    # each layer, for the per-layer split and the decode kernel's roofline.
+    INSTR = 10
+    evs = {s: [torch.cuda.Event(enable_timing=True) for _ in range(L + 1)] for s in range(0, args.steps, INSTR)}
     loop_ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
     clocks = ClockSampler(dist.local)
     clocks.start()
@@ -735,51 +964,73 @@ def bench_ours(args, dist):
     with torch.cuda.stream(stream):
         loop_ev[0].record(stream)
         for s in range(args.steps):
-            step(evs.get(s))
+            if s in evs:
+                step_by_layer(evs[s])
+            else:
+                step()
         loop_ev[1].record(stream)
     torch.cuda.synchronize()
     clocks.mark("t1")
     launches = hyb.hyb_launch_count(reset=True)
     dist.barrier()
     clocks.stop()
-    per_op = np.zeros(n_ops)
-    step_ms = []                                  # instrumented steps (per-op events)
-    for e in evs.values():
-        step_ms.append(e[0].elapsed_time(e[n_ops]))
-        for i in range(n_ops):
-            per_op[i] += e[i].elapsed_time(e[i + 1])
-    per_op /= len(evs)
     ms_step = dist.max(loop_ev[0].elapsed_time(loop_ev[1]) / args.steps)
-    units = dist.sum(B * L)                       # request-tokens per layer-step over all ranks
+    units = dist.sum(B * L)                              # request-tokens per layer-step over all ranks
     value = units / (ms_step * 1e-3)
-    st, flags = hyb.hyb_device_status(clear=True)
-    if st != 0:
-        raise RuntimeError(f"device-side check flags {flags:#x}")
+    layer_ms = np.array([[e[l].elapsed_time(e[l + 1]) for l in range(L)] for e in evs.values()])
+    _check_device(hyb)
+    is_full = np.array([t == 0 for t in lt])
+    full_ms = float(layer_ms[:, is_full].mean())
+    lin_ms = float(layer_ms[:, ~is_full].mean())
 
-    # ---- roofline of the dominant kernel (paged decode: split-K kernel + combine)
-    hbm_peak, tf_peak, peak_kind = measured_peaks()
-    tokens = int(db.seq_lens.sum())
-    # K+V read, q read, out write, and the new K/V rows read and written into the cache
-    alg_bytes = tokens * H * D * 2 * 2 + 2 * B * H * D * 2 + 4 * B * H * D * 2
-    achieved = alg_bytes / (per_op[0] * 1e-3) / 1e9
-    trec = traffic_record("paged_decode", "decode.cu")
-    roofline = {"kernel": "paged_decode with the KV append fused (split-K + combine)", "bound": "hbm",
-                "achieved": round(achieved, 1),
-                "peak": hbm_peak, "unit": "GB/s", "frac": round(achieved / hbm_peak, 4),
+    # ---- roofline of the dominant kernel: a Full layer's paged decode (KV append fused,
+    # split-K kernel + combine), averaged over the 24 Full layers of the instrumented steps
+    hbm_peak, _, peak_kind = measured_peaks()
+    full_bytes, lin_bytes, step_bytes = hybrid_bytes(wl)
+    achieved = full_bytes / (full_ms * 1e-3) / 1e9
+    trec = traffic_record("paged_decode_hybrid", "decode.cu")
+    roofline = {"kernel": "paged_decode with the KV append fused (split-K + combine), one Full layer of the step",
+                "bound": "hbm", "achieved": round(achieved, 1), "peak": hbm_peak, "unit": "GB/s",
+                "frac": round(achieved / hbm_peak, 4),
                 "traffic": (int(trec["bytes_per_launch"]) if trec else None),
-                "algorithmic_bytes": alg_bytes, "peak_source": f"{peak_kind} hbm_gbs"}
-    lin_bytes = B * H * D * D * 4 * 2
-    ops = {n: {"ms": round(float(t), 5)} for n, t in zip(names, per_op)}
-    ops["paged_decode"]["GB/s"] = round(achieved, 1)
-    ops["linear_step"]["GB/s"] = round(lin_bytes / (per_op[1] * 1e-3) / 1e9, 1)
-    ops["linear_step"]["frac"] = round(ops["linear_step"]["GB/s"] / hbm_peak, 4)
-    ops["linear_step"]["traffic"] = _traffic("linear_step", "linear.cu")
+                "algorithmic_bytes": full_bytes, "launches_averaged": int(is_full.sum()) * len(evs),
+                "peak_source": f"{peak_kind} hbm_gbs"}
+    n_full = int(is_full.sum())
+    ops = {"full_layer": {"ms": round(full_ms, 5), "GB/s": round(achieved, 1), "layers": n_full,
+                          "share_of_step": round(n_full * full_ms / float(layer_ms.sum(1).mean()), 4)},
+           "linear_layer": {"ms": round(lin_ms, 5), "GB/s": round(lin_bytes / (lin_ms * 1e-3) / 1e9, 1),
+                            "frac": round(lin_bytes / (lin_ms * 1e-3) / 1e9 / hbm_peak, 4), "layers": L - n_full,
+                            "share_of_step": round((L - n_full) * lin_ms / float(layer_ms.sum(1).mean()), 4)},
+           "note": (f"per-layer times from the {len(evs)} layer-by-layer steps (every {INSTR}th), which run "
+                    "without the early launch between layers")}
+    step_roof = _roof("hbm", step_bytes / (ms_step * 1e-3) / 1e9, hbm_peak, "GB/s", "whole 32-layer step (dispatch)",
+                      step_bytes)
+
+    # ---- step-time distribution: a separate pass, one event pair per step
+    NP = 200
+    pev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(NP)]
+    with torch.cuda.stream(stream):
+        for a, b in pev:
+            a.record(stream)
+            step()
+            b.record(stream)
+    torch.cuda.synchronize()
+    per_step = np.array([a.elapsed_time(b) for a, b in pev])
+
+    # ---- the same step captured once into a CUDA graph and replayed
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        step()
+        stream.synchronize()
+        with torch.cuda.graph(graph, stream=stream):
+            step()
+    t_graph = _time(graph.replay, stream, 100)
+    del graph
 
     # ---- end to end through the public dispatcher, host buffers, copies timed. All of a
-    # step's inputs sit in one pinned host buffer and go over in one copy; both layers'
-    # outputs come back in one copy.
-    host_arrays = dict(wl["host"])
-    host_arrays.update({"lens": db.seq_lens, "bt": db.pool.block_tables, "slots": wl["slots_h"]})
+    # step's inputs (32 layers' q/k/v and the batch metadata) sit in one pinned host buffer and
+    # go over in one copy; all 32 layers' outputs come back in one copy.
+    host_arrays = {"qkv": wl["qkv"], "lens": db.seq_lens, "bt": db.pool.block_tables, "slots": wl["slots"]}
     offs, total = {}, 0
     for n, a in host_arrays.items():
         offs[n] = total
@@ -802,17 +1053,11 @@ def bench_ours(args, dist):
             t = t.view(torch.bfloat16) if a.dtype == np.uint16 else t.view(getattr(torch, a.dtype.name))
             return t.view(a.shape)
 
-        d_in = {n: dview(n) for n in wl["host"]}
-        d_meta = {n: dview(n) for n in ("lens", "bt", "slots")}
-        out_all = torch.empty(2 * B * H * D, dtype=torch.bfloat16, device=device)
-        e_out_f, e_out_l = out_all[:B * H * D].view(B, H, D), out_all[B * H * D:].view(B, H, D)
-        meta = hyb.batch_meta(B, B, seq_lens=d_meta["lens"], block_tables=d_meta["bt"],
-                              state_slots=d_meta["slots"], max_seq_len=msl)   # new rows at seq_len - 1 via the table
-        ios = [hyb.layer_io(e_out_f, d_in["qf"], d_in["kf"], d_in["vf"], wl["kc"], wl["vc"]),
-               hyb.layer_io(e_out_l, d_in["ql"], d_in["kl"], d_in["vl"], state_pool=wl["state"],
-                            num_state_slots=B)]
-        sets.append(dict(d_all=d_all, d_meta=d_meta, out_all=out_all, meta=meta, ios=ios,
-                         h_out=torch.empty(2 * B * H * D, dtype=torch.int16).pin_memory(),
+        out_all = torch.empty((L, B, H, D), dtype=torch.bfloat16, device=device)
+        e_meta = hyb.batch_meta(B, B, seq_lens=dview("lens"), block_tables=dview("bt"), state_slots=dview("slots"),
+                                max_seq_len=msl)
+        sets.append(dict(d_all=d_all, out_all=out_all, meta=e_meta, ios=layer_ios(dview("qkv"), out_all),
+                         h_out=torch.empty(out_all.numel(), dtype=torch.int16).pin_memory(),
                          loaded=torch.cuda.Event(), computed=torch.cuda.Event(), read=torch.cuda.Event()))
     d2h = sets[0]["h_out"].numel() * sets[0]["h_out"].element_size()
     h2d_stream = torch.cuda.Stream(device=device)   # one stream per direction: a read-back
@@ -826,14 +1071,14 @@ def bench_ours(args, dist):
             st["d_all"].copy_(h_all, non_blocking=True)
             st["loaded"].record(h2d_stream)
         stream.wait_event(st["loaded"])
-        hyb.check(hyb.hyb_layer_dispatch([0, 1], 2, 0, st["ios"], st["meta"], d, 64, ws, ws_n, sh))
+        hyb.check(hyb.hyb_layer_dispatch(lt, L, 0, st["ios"], st["meta"], d, 64, ws, ws_n, sh))
         st["computed"].record(stream)
         d2h_stream.wait_event(st["computed"])
         with torch.cuda.stream(d2h_stream):
-            st["h_out"].copy_(st["out_all"].view(torch.int16), non_blocking=True)
+            st["h_out"].copy_(st["out_all"].view(-1).view(torch.int16), non_blocking=True)
             st["read"].record(d2h_stream)
 
-    e2e_steps = max(10, min(args.steps, 500))
+    e2e_steps = max(10, min(args.steps, 200))
     with torch.cuda.stream(stream):
         for i in range(3):
             e2e_step(i)
@@ -850,132 +1095,110 @@ def bench_ours(args, dist):
         torch.cuda.synchronize()
     e2e_ms = dist.max(e0.elapsed_time(e1) / e2e_steps)
     e2e_val = units / (e2e_ms * 1e-3)
+    _check_device(hyb)
+    del sets
 
     # ---- CPU oracle beside it (rank 0, N = 1 only)
-    cpu = None
-    if dist.world == 1:
-        cpu = cpu_baseline_decode(wl, budget_s=10.0)
+    cpu = cpu_baseline_hybrid(wl) if dist.world == 1 else None
 
-    # ---- the other rows of the hot path, each against its own roofline (N = 1 only)
+    # ---- the other workloads, each against its own roofline (N = 1 only)
     rows = None
     if dist.world == 1 and not args.no_rows:
-        del wl
+        tokens = int(db.seq_lens.sum())
+        del wl, qkv, out, ios
         torch.cuda.empty_cache()
         rows = {name: fn(hyb, device, stream, 20, args.seed) for name, fn in ROWS.items()}
+    else:
+        tokens = int(db.seq_lens.sum())
 
-    return {
+    res = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": dist.world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "ms_per_step_p50": round(float(np.percentile(step_ms, 50)), 5),
-        "ms_per_step_p99": round(float(np.percentile(step_ms, 99)), 5),
-        "timing": (f"ms_per_step: one CUDA event pair around all {args.steps} steps; p50/p99 and ops: "
-                   f"the {len(evs)} steps (every {INSTR}th) that also carry per-op events"),
+        "ms_per_step_p50": round(float(np.percentile(per_step, 50)), 5),
+        "ms_per_step_p99": round(float(np.percentile(per_step, 99)), 5),
+        "timing": (f"ms_per_step: one CUDA event pair around all {args.steps} steps; p50/p99: a separate pass "
+                   f"of {NP} steps with one event pair each"),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded N(0,1)/sqrt(D) q/k/v, shuffled block pool, N(0,seq/D^2) states)",
-        "config": {"workload": "decode_single_layer: 32 requests, H=32, D=128, block 16, seq_lens U{128..4096}, "
-                               "1 Full paged-decode + 1 Linear step", "B": B, "H": H, "D": D,
-                   "layers": ["full", "linear"], "kv_tokens": tokens, "pool_blocks": NB,
-                   "l2": "no flush: per-step working set %.2f GB > 129 MB L2" % ((alg_bytes + lin_bytes) / 1e9),
+        "config": {"workload": "hybrid_32layer: 32 layers [full,full,full,linear] x 8, batch 64 (80% ~lognormal(128), "
+                               "20% ~lognormal(2048) cached tokens), H=32, D=128, block 16, one decode token per "
+                               "request through all layers",
+                   "B": B, "H": H, "D": D, "layers": "[full,full,full,linear] x 8", "kv_tokens": tokens,
+                   "pool_blocks": NB,
+                   "l2": "no flush: per-step working set %.2f GB > 129 MB L2" % (step_bytes / 1e9),
                    "parallelism": f"replicas x{dist.world}"},
-        "roofline": roofline, "ops": ops,
+        "roofline": roofline, "step_roofline": step_roof, "ops": ops,
+        "cuda_graph": {"value": round(units / (t_graph * 1e-3), 1), "ms_per_step": round(t_graph, 5),
+                       "note": "the same step captured once and replayed (no per-launch host work)"},
         "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
-                "path": "hyb_layer_dispatch; inputs in one pinned buffer, one copy each way, "
+                "path": "hyb_layer_dispatch over all 32 layers; inputs in one pinned buffer, one copy each way, "
                         "on copy streams double-buffered against the compute stream"},
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
         "rows": rows,
     }
-
-
-def cpu_baseline_decode(wl, budget_s=15.0, requests=None):
-    """Times the CPU oracle (as it stands) on a bounded sample of the same workload: whole
-    requests through the Full-layer decode and the Linear step, all heads."""
-    import oracle
-    db = wl["db"]
-    H, D = wl["H"], wl["D"]
-    cores = oracle.set_threads(0)
-    kc = wl["kc"].cpu().view(__import__("torch").int16).numpy().view(np.uint16)
-    vc = wl["vc"].cpu().view(__import__("torch").int16).numpy().view(np.uint16)
-    st = wl["state"].cpu().numpy()
-    hq = wl["host"]
-    done, t_used = 0, 0.0
-    order = list(range(wl["B"])) if requests is None else list(requests)
-    passes = 0
-    while t_used < budget_s:             # repeat the whole batch until ~budget_s of CPU work
-        for b in order:
-            t0 = time.perf_counter()
-            oracle.full_decode(hq["qf"][b:b + 1], kc, vc, db.pool.block_tables[b:b + 1],
-                               db.seq_lens[b:b + 1], D ** -0.5)
-            oracle.linear_step(hq["ql"][b:b + 1], hq["kl"][b:b + 1], hq["vl"][b:b + 1], st,
-                               wl["slots_h"][b:b + 1])
-            t_used += time.perf_counter() - t0
-            done += 1
-            if t_used > budget_s:
-                break
-        passes += 1
-    res = {"value": round(done * 2 / t_used, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-           "sample": f"{done} request-steps ({passes} pass(es) over the {wl['B']} requests, all {H} heads; "
-                     f"Full decode + Linear step), fp64 C oracle with OpenMP over (request, head), "
-                     f"{t_used:.1f} s"}
-    # the same oracle on one core, over a short sample (first requests of the batch)
-    oracle.set_threads(1)
-    done1, t1 = 0, 0.0
-    for b in order:
-        if t1 > budget_s / 5:
-            break
-        t0 = time.perf_counter()
-        oracle.full_decode(hq["qf"][b:b + 1], kc, vc, db.pool.block_tables[b:b + 1], db.seq_lens[b:b + 1], D ** -0.5)
-        oracle.linear_step(hq["ql"][b:b + 1], hq["kl"][b:b + 1], hq["vl"][b:b + 1], st, wl["slots_h"][b:b + 1])
-        t1 += time.perf_counter() - t0
-        done1 += 1
-    oracle.set_threads(cores)
-    res["single_thread"] = {"value": round(done1 * 2 / t1, 2), "unit": UNIT, "cores": 1,
-                            "sample": f"the first {done1} requests of the batch, {t1:.1f} s"}
     return res
 
 
 def bench_reference(args, dist):
-    """The CPU oracle as the reference arm: each step is one request (rotating through the
-    batch) through both layers, on the host cores."""
+    """The CPU oracle as the reference arm, on the headline workload: each step is the batch's
+    requests through one period [full, full, full, linear] of the 32-layer pattern (rotating
+    over the requests when the run is long), on the host cores."""
     if dist.rank != 0:
         return None
     import oracle
     oracle.build()
-    db = W.decode_single_layer(args.seed)
-    g = W.rng(args.seed + 1)
+    db = W.decode_hybrid_32layer(args.seed)
+    g = W.rng(args.seed + 9)
     B, H, D = db.B, db.H, db.D
     cores = oracle.set_threads(0)
-    # pool contents for the sampled requests only (host-drawn, same shapes)
-    kc = np.empty((db.pool.num_blocks, H, 16, D), np.uint16)
-    vc = np.empty_like(kc)
-    gk = W.rng(args.seed + 7)
-    kc[:] = W.rows(gk, kc.shape, D, W.BF16)
-    vc[:] = W.rows(gk, vc.shape, D, W.BF16)
+    period = [0, 0, 0, 1]
+    P = len(period)
+    # One K and one V pool image (0.36 GB each, larger than the host caches) shared by the
+    # period's Full layers; each layer has its own q/k/v rows.
+    import torch
+    kc, vc = (W.device_rows_(torch.empty((db.pool.num_blocks, H, 16, D), dtype=torch.bfloat16), 100 + i, D)
+              .view(torch.int16).numpy().view(np.uint16) for i in range(2))     # host tensors, seeded
+    qkv = W.rows(g, (P, 3, B, H, D), D, W.BF16)
     st = W.synthetic_state(g, B, H, D, db.seq_lens)
-    q, k, v = (W.rows(g, (B, H, D), D, W.BF16) for _ in range(3))
-    slots = np.arange(B, dtype=np.int32)
+    slots = g.permutation(B).astype(np.int32)
+    # requests per step: the whole batch unless the run is long (keeps it to a few minutes)
+    R = max(1, min(B, (B * 100) // max(args.steps + args.warmup, 1)))
 
-    def one(b):
-        oracle.full_decode(q[b:b + 1], kc, vc, db.pool.block_tables[b:b + 1], db.seq_lens[b:b + 1], D ** -0.5)
-        oracle.linear_step(q[b:b + 1], k[b:b + 1], v[b:b + 1], st, slots[b:b + 1])
+    def one(i):
+        r = np.arange(i * R, i * R + R) % B
+        bt, ln = db.pool.block_tables[r], db.seq_lens[r]
+        cu = np.arange(R + 1, dtype=np.int32)
+        for l, t in enumerate(period):
+            q, k, v = qkv[l, 0][r], qkv[l, 1][r], qkv[l, 2][r]
+            if t == 0:
+                slot = oracle.slot_mapping(bt, cu, (ln - 1).astype(np.int32))
+                oracle.kv_append(k, v, slot, kc, vc)
+                oracle.full_decode(q, kc, vc, bt, ln, D ** -0.5)
+            else:
+                oracle.linear_step(q, k, v, st, slots[r])
 
     for i in range(args.warmup):
-        one(i % B)
+        one(i)
     t0 = time.perf_counter()
     for i in range(args.steps):
-        one(i % B)
+        one(i)
     dt = time.perf_counter() - t0
     ms = dt * 1e3 / args.steps
-    val = 2 / (ms * 1e-3)
+    val = R * P / (ms * 1e-3)
+    sample = (f"{R} of the {B} requests per step (rotating) through one period [full, full, full, linear] of the "
+              f"32-layer pattern (Full: slot, KV append, paged decode; Linear: state step), all {H} heads; the "
+              f"period's Full layers share one 0.36 GB K and V pool image")
     return {"impl": "reference", "metric": METRIC, "value": round(val, 2), "unit": UNIT, "n_gpus": dist.world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": "decode_single_layer: 32 requests, H=32, D=128, block 16, seq_lens U{128..4096}, "
-                                   "1 Full paged-decode + 1 Linear step", "sample_per_step": "1 request, all heads"},
-            "cpu_baseline": {"value": round(val, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-                             "sample": "1 request per step (rotating over the 32), all 32 heads, Full decode + Linear step"},
+            "config": {"workload": "hybrid_32layer: 32 layers [full,full,full,linear] x 8, batch 64 (80% "
+                                   "~lognormal(128), 20% ~lognormal(2048) cached tokens), H=32, D=128, block 16, "
+                                   "one decode token per request through all layers",
+                       "sample_per_step": sample},
+            "cpu_baseline": {"value": round(val, 2), "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": round(val, 2), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
 
 
@@ -994,3 +1217,4 @@ def main():
 
 if __name__ == "__main__":
     main()
+

@@ -266,13 +266,18 @@ hyb_status_t hyb_linear_attn_step_lowp(void* out, const void* q, const void* k, 
  * kernel (same contract).
  * The tensor-core kernel is a cooperative launch of at most one CTA per SM that shares all
  * (request, head) chains' chunks out evenly; a chain cut between two CTAs is handed over
- * through its own state slot, with a flag in a small library-owned array (128 KiB of device
- * memory per GPU) that names the call (a per-call epoch, bumped by a one-thread kernel
- * launched just before, and the launch's grid id). Calls on one stream, eager or captured
- * in graphs, need nothing more. Calls whose kernels overlap on the GPU (two streams) can
- * overwrite each other's flags: a waiting CTA then gives up after ~2 s and sets
- * HYB_DEVERR_TIMEOUT. A flag is only ever accepted from its own call, so overlap never
- * yields a silently wrong state.
+ * through its own state slot, announced by a flag that names the call (a per-call epoch,
+ * bumped by a one-thread kernel launched just before, and the launch's grid id). The epoch
+ * and the flags live in `workspace` (device memory, 8-byte aligned, at least
+ * hyb_linear_attn_chunked_prefill_workspace_size() bytes, owned by the caller; its contents
+ * need no initialisation and must be left alone between calls). The library keeps no handoff
+ * state of its own: calls with distinct workspaces may run at the same time on any streams.
+ * Calls that share one workspace must not overlap on the GPU (calls in order on one stream,
+ * eager or captured in graphs, never do); if they do, a waiting CTA gives up after ~2 s and
+ * sets HYB_DEVERR_TIMEOUT. A flag is only ever accepted from its own call, so overlap never
+ * yields a silently wrong state. The CUDA-core kernel ignores the workspace, but it is
+ * checked the same way. A missing, misaligned or short workspace is HYB_ERR_INVALID_ARG
+ * (nothing launched) when B > 0.
  * ------------------------------------------------------------------------- */
 hyb_status_t hyb_linear_attn_chunked_prefill(void* out, const void* q, const void* k,
                                              const void* v, const int32_t* cu_seqlens,
@@ -281,7 +286,11 @@ hyb_status_t hyb_linear_attn_chunked_prefill(void* out, const void* q, const voi
                                              const int32_t* state_slots, const uint8_t* reset,
                                              int32_t B, int32_t T, int32_t max_len, int32_t H,
                                              int32_t D, int32_t chunk_size, int32_t dtype,
-                                             void* stream);
+                                             void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of device workspace hyb_linear_attn_chunked_prefill needs (a fixed 2 056: one
+ * 64-bit epoch and one 64-bit flag per CTA, at most 256 CTAs). */
+size_t hyb_linear_attn_chunked_prefill_workspace_size(void);
 
 /* -------------------------------------------------------------------------
  * A7. Layer dispatch [KV §2.2: layer types registered from the model config,
@@ -302,7 +311,9 @@ hyb_status_t hyb_linear_attn_chunked_prefill(void* out, const void* q, const voi
  * Every layer's arguments are checked before the first launch. Results equal the
  * per-op calls bit for bit. workspace serves the decode calls (see A3) and must hold
  * hyb_paged_attn_decode_workspace_size() bytes for the largest window among the layers
- * (window 0 when any FULL layer is present).
+ * (window 0 when any FULL layer is present). In prefill mode it serves the LINEAR layers'
+ * chunked prefill instead (one after another in stream order, sharing it) and must hold
+ * hyb_linear_attn_chunked_prefill_workspace_size() bytes when a LINEAR layer is present.
  * ------------------------------------------------------------------------- */
 typedef struct {
   void* out;                 /* [T][H][D]                                   */

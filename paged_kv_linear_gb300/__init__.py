@@ -69,7 +69,8 @@ def _load():
         "hyb_linear_attn_step": [p, p, p, p, p, i32, p, i32, i32, i32, i32, p],
         "hyb_linear_attn_step_lowp": [p, p, p, p, p, i32, i32, p, i32, i32, i32, i32, p],
         "hyb_linear_attn_chunked_prefill": [p, p, p, p, p, p, p, i32, p, p, i32, i32, i32, i32,
-                                            i32, i32, i32, p],
+                                            i32, i32, i32, p, sz, p],
+        "hyb_linear_attn_chunked_prefill_workspace_size": ([], sz),
         "hyb_layer_dispatch": [p, i32, i32, p, p, p, i32, p, sz, p],
         "hyb_cache_bytes": ([i32, i32, i32, i32, i64, i32, i32, i32, p, p], u64),
         "hyb_device_status": [p, i32],
@@ -219,11 +220,15 @@ def hyb_linear_attn_step_lowp(out, q, k, v, state_pool, state_dtype, num_state_s
 
 def hyb_linear_attn_chunked_prefill(out, q, k, v, cu_seqlens, ctx_lens, state_pool,
                                     num_state_slots, state_slots, reset, B, T, max_len, H, D,
-                                    chunk_size, dtype, stream=None):
+                                    chunk_size, dtype, workspace, ws_bytes, stream=None):
     return _lib.hyb_linear_attn_chunked_prefill(
         _p(out), _p(q), _p(k), _p(v), _p(cu_seqlens), _p(ctx_lens), _p(state_pool),
         num_state_slots, _p(state_slots), _p(reset), B, T, max_len, H, D, chunk_size, dtype,
-        _s(stream))
+        _p(workspace), ws_bytes, _s(stream))
+
+
+def hyb_linear_attn_chunked_prefill_workspace_size() -> int:
+    return int(_lib.hyb_linear_attn_chunked_prefill_workspace_size())
 
 
 def layer_io(out=None, q=None, k=None, v=None, k_cache=None, v_cache=None, state_pool=None,

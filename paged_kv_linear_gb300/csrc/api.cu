@@ -221,13 +221,15 @@ hyb_status_t check_linear_common(const void* out, const void* q, const void* k, 
 hyb_status_t check_linear_prefill(const void* out, const void* q, const void* k, const void* v,
                                   const int32_t* cu, const int32_t* ctx, const float* pool,
                                   int NS, const int32_t* slots, const uint8_t* reset, int B, int T,
-                                  int max_len, int H, int D, int C, int dtype) {
+                                  int max_len, int H, int D, int C, int dtype, const void* ws,
+                                  size_t ws_bytes) {
   hyb_status_t st = check_linear_common(out, q, k, v, pool, NS, slots, B, H, D, dtype);
   if (st != HYB_OK) return st;
   if (C <= 0 || T < 0 || max_len < 0 || max_len > T) return HYB_ERR_INVALID_ARG;
   if (!linear_prefill_tc_supported(dtype, D, C) && D > 128) return HYB_ERR_UNSUPPORTED;
   if (B == 0) return HYB_OK;
   if (!cu || !al(cu, 4) || (ctx && !al(ctx, 4))) return HYB_ERR_INVALID_ARG;
+  if (!ws || !al(ws, 8) || ws_bytes < kLinPrefillWsBytes) return HYB_ERR_INVALID_ARG;
   (void)reset;
   return HYB_OK;
 }
@@ -265,12 +267,12 @@ hyb_status_t run_prefill(void* out, const void* q, const void* kc, const void* v
 hyb_status_t run_linear_prefill(void* out, const void* q, const void* k, const void* v,
                                 const int32_t* cu, const int32_t* ctx, float* pool, int NS,
                                 const int32_t* slots, const uint8_t* reset, int B, int T,
-                                int max_len, int H, int D, int C, int dtype, unsigned* status,
-                                cudaStream_t s) {
+                                int max_len, int H, int D, int C, int dtype, void* ws,
+                                unsigned* status, cudaStream_t s) {
   if (B == 0) return HYB_OK;
   if (linear_prefill_tc_supported(dtype, D, C))
     return cuda_status(launch_linear_prefill_tc(out, q, k, v, cu, ctx, pool, NS, slots, reset,
-                                                B, T, max_len, H, C, status, s));
+                                                B, T, max_len, H, C, ws, status, s));
   return cuda_status(launch_linear_prefill_simt(out, q, k, v, cu, ctx, pool, NS, slots, reset,
                                                 B, H, D, C, dtype, status, s));
 }
@@ -402,17 +404,19 @@ hyb_status_t hyb_linear_attn_chunked_prefill(void* out, const void* q, const voi
                                              const int32_t* state_slots, const uint8_t* reset,
                                              int32_t B, int32_t T, int32_t max_len, int32_t H,
                                              int32_t D, int32_t chunk_size, int32_t dtype,
-                                             void* stream) {
+                                             void* workspace, size_t ws_bytes, void* stream) {
   hyb_status_t st = check_linear_prefill(out, q, k, v, cu_seqlens, ctx_lens, state_pool,
                                          num_state_slots, state_slots, reset, B, T, max_len, H, D,
-                                         chunk_size, dtype);
+                                         chunk_size, dtype, workspace, ws_bytes);
   if (st != HYB_OK || B == 0) return st;
   unsigned* sw = status_word();
   if (!sw) return HYB_ERR_CUDA;
   return run_linear_prefill(out, q, k, v, cu_seqlens, ctx_lens, state_pool, num_state_slots,
-                            state_slots, reset, B, T, max_len, H, D, chunk_size, dtype, sw,
-                            (cudaStream_t)stream);
+                            state_slots, reset, B, T, max_len, H, D, chunk_size, dtype,
+                            workspace, sw, (cudaStream_t)stream);
 }
+
+size_t hyb_linear_attn_chunked_prefill_workspace_size(void) { return kLinPrefillWsBytes; }
 
 // ---- dispatch trace (HYB_TRACE set in the environment): a line per layer on stderr naming
 // its kernels, and a CUDA event before the first layer and after each layer, kept per host
@@ -513,7 +517,8 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
                                      meta->state_slots, B, H, D, dt)
                : check_linear_prefill(io.out, io.q, io.k, io.v, meta->cu_q_lens, meta->ctx_lens,
                                       io.state_pool, io.num_state_slots, meta->state_slots,
-                                      meta->reset, B, T, meta->max_q_len, H, D, chunk_size, dt);
+                                      meta->reset, B, T, meta->max_q_len, H, D, chunk_size, dt,
+                                      workspace, ws_bytes);
     } else {
       return HYB_ERR_INVALID_ARG;
     }
@@ -560,8 +565,8 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
                                                 dt, sw, s))
                : run_linear_prefill(io.out, io.q, io.k, io.v, meta->cu_q_lens, meta->ctx_lens,
                                     io.state_pool, io.num_state_slots, meta->state_slots,
-                                    meta->reset, B, T, meta->max_q_len, H, D, chunk_size, dt, sw,
-                                    s);
+                                    meta->reset, B, T, meta->max_q_len, H, D, chunk_size, dt,
+                                    workspace, sw, s);
     }
     if (st != HYB_OK) return st;
     if (trace) {

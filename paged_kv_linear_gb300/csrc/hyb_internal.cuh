@@ -100,10 +100,14 @@ cudaError_t launch_linear_prefill_simt(void* out, const void* q, const void* k, 
                                        int H, int D, int C, int dtype, unsigned* status,
                                        cudaStream_t s);
 bool linear_prefill_tc_supported(int dtype, int D, int C);
+// Handoff workspace of the tensor-core chunked prefill: a per-call epoch and one flag per CTA
+// (at most kLinMaxCtas CTAs), 64-bit words.
+constexpr int kLinMaxCtas = 256;
+constexpr size_t kLinPrefillWsBytes = 8 * (1 + kLinMaxCtas);
 cudaError_t launch_linear_prefill_tc(void* out, const void* q, const void* k, const void* v,
                                      const int32_t* cu, const int32_t* ctx, float* pool, int NS,
                                      const int32_t* slots, const uint8_t* reset, int B, int T,
-                                     int max_len, int H, int C, unsigned* status,
+                                     int max_len, int H, int C, void* ws, unsigned* status,
                                      cudaStream_t s);
 bool prefill_tc_supported(int dtype, int D);
 cudaError_t launch_prefill_tc(void* out, const void* q, const void* kc, const void* vc,

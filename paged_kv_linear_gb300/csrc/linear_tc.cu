@@ -87,17 +87,16 @@ static_assert(sizeof(Bars) <= 256, "barriers overflow their shared-memory slot")
 // A handoff is announced by a flag that names the call: the call's epoch (a counter that a
 // one-thread kernel bumps right before every launch, in stream order, so graph replays get
 // fresh epochs too) and the launch's grid id (distinct for launches that run at the same
-// time). A waiting CTA accepts only its own call's value, never one left by another call.
-constexpr int kMaxCtas = 256;                // grid limit (one CTA per SM)
-constexpr int kRegions = 64;                 // flag sets, chosen by the launch's grid id
-// handoff flags: entry p holds the tag of the call whose CTA p has written the state of the
-// chain it cut (at its first boundary) to the pool.
-__device__ unsigned long long g_lin_handoff[kRegions][kMaxCtas];
-__device__ unsigned g_lin_epoch;
+// time). A waiting CTA accepts only its own call's value, never one left by an earlier call.
+// Epoch and flags live in the caller's workspace: hs[0] is the epoch, hs[1 + p] holds the tag
+// of the call whose CTA p has written the state of the chain it cut (at its first boundary)
+// to the pool. The library itself holds no handoff state, so calls with distinct workspaces
+// never see each other's flags.
+constexpr int kMaxCtas = kLinMaxCtas;        // grid limit (one CTA per SM)
 
-__global__ void linear_handoff_epoch_kernel() {
+__global__ void linear_handoff_epoch_kernel(unsigned long long* hs) {
   pdl_wait();                                // everything before it in the stream is done
-  g_lin_epoch += 1;
+  hs[0] += 1;
 }
 
 struct Plan {
@@ -305,7 +304,8 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
                          const __grid_constant__ CUtensorMap tv, __nv_bfloat16* __restrict__ out,
                          const int32_t* __restrict__ cu, const int32_t* __restrict__ ctx,
                          float* __restrict__ pool, int NS, const int32_t* __restrict__ slots,
-                         const uint8_t* __restrict__ reset, int B, int H, unsigned* status) {
+                         const uint8_t* __restrict__ reset, int B, int H,
+                         unsigned long long* __restrict__ hs, unsigned* status) {
   const int p = blockIdx.x, P = gridDim.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   __shared__ Plan plan_sh;
@@ -334,9 +334,9 @@ linear_prefill_tc_kernel(const __grid_constant__ CUtensorMap tq,
   __syncthreads();
   if (plan_sh.head_u < 0 && plan_sh.tail_u < 0 && plan_sh.full_u0 >= plan_sh.full_u1) return;
   const unsigned long long gid = grid_id();
-  unsigned long long* const handoff = g_lin_handoff[gid % kRegions];
+  unsigned long long* const handoff = hs + 1;
   const unsigned long long tag =
-      ((unsigned long long)*reinterpret_cast<volatile unsigned*>(&g_lin_epoch) << 32) | (gid & 0xffffffffull);
+      (*reinterpret_cast<volatile unsigned long long*>(hs) << 32) | (gid & 0xffffffffull);
   Walk walk;
 #define NEXT_RUN(sg) next_run(walk, plan_sh, cu, ctx, slots, reset, pool, NS, H, sg)
 
@@ -655,7 +655,7 @@ bool linear_prefill_tc_supported(int dtype, int D, int C) {
 cudaError_t launch_linear_prefill_tc(void* out, const void* q, const void* k, const void* v,
                                      const int32_t* cu, const int32_t* ctx, float* pool, int NS,
                                      const int32_t* slots, const uint8_t* reset, int B, int T,
-                                     int max_len, int H, int C, unsigned* status,
+                                     int max_len, int H, int C, void* ws, unsigned* status,
                                      cudaStream_t s) {
   (void)max_len;
   (void)C;
@@ -670,7 +670,8 @@ cudaError_t launch_linear_prefill_tc(void* out, const void* q, const void* k, co
     return cudaErrorInvalidValue;
   cudaError_t e = set_smem((const void*)linear_prefill_tc_kernel, kSmem);
   if (e != cudaSuccess) return e;
-  e = launch_pdl(linear_handoff_epoch_kernel, dim3(1), dim3(1), 0, s);
+  unsigned long long* hs = static_cast<unsigned long long*>(ws);
+  e = launch_pdl(linear_handoff_epoch_kernel, dim3(1), dim3(1), 0, s, hs);
   count_launch();
   if (e != cudaSuccess) return e;
   // One CTA per SM at most (the shared memory allows no more), all resident at once: a CTA
@@ -689,7 +690,7 @@ cudaError_t launch_linear_prefill_tc(void* out, const void* q, const void* k, co
   cfg.numAttrs = 1;
   e = cudaLaunchKernelEx(&cfg, linear_prefill_tc_kernel, mq, mk, mv,
                          static_cast<__nv_bfloat16*>(out), cu, ctx, pool, NS, slots, reset, B, H,
-                         status);
+                         hs, status);
   count_launch();
   return e;
 }

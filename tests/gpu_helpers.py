@@ -38,6 +38,14 @@ def to_dev(a: np.ndarray, dtype_code: int | None = None, device="cuda"):
     return torch.from_numpy(a).to(device)
 
 
+def lin_ws(device="cuda"):
+    """(workspace, bytes) for one hyb_linear_attn_chunked_prefill call: a fresh device
+    buffer of the size the library asks for (its contents need no initialisation)."""
+    import paged_kv_linear_gb300 as hyb
+    n = hyb.hyb_linear_attn_chunked_prefill_workspace_size()
+    return torch.empty(n, dtype=torch.uint8, device=device), n
+
+
 def to_host(t: torch.Tensor) -> np.ndarray:
     t = t.detach().cpu().contiguous()
     if t.dtype == torch.bfloat16:

@@ -92,8 +92,16 @@ def test_bad_arguments_rejected_before_launch(hyb):
     assert hyb.hyb_linear_attn_step(fake, fake, fake, fake, fake, 0, fake, 2, 4, 128, 1, 0) == hyb.HYB_ERR_INVALID_ARG
     assert hyb.hyb_linear_attn_step(fake, fake, fake, fake, fake, 4, fake, 2, 4, 128, 7, 0) == hyb.HYB_ERR_INVALID_ARG
     assert hyb.hyb_linear_attn_step(fake, fake, fake, fake, fake, 4, fake, 2, 4, 48, 1, 0) == hyb.HYB_ERR_UNSUPPORTED
-    # chunk size 0
-    assert hyb.hyb_linear_attn_chunked_prefill(fake, fake, fake, fake, fake, None, fake, 4, fake, None, 2, 128, 64, 4, 128, 0, 1, 0) == hyb.HYB_ERR_INVALID_ARG
+    # chunked linear prefill: chunk size 0; the handoff workspace missing, short or misaligned
+    n_lw = hyb.hyb_linear_attn_chunked_prefill_workspace_size()
+    assert n_lw == 8 * (1 + 256)                 # one epoch word and one flag per CTA (<= 256 CTAs)
+    lp = lambda C, ws, n, B=2: hyb.hyb_linear_attn_chunked_prefill(fake, fake, fake, fake, fake, None, fake, 4, fake,
+                                                                   None, B, 128, 64, 4, 128, C, 1, ws, n, 0)
+    assert lp(0, fake, n_lw) == hyb.HYB_ERR_INVALID_ARG
+    assert lp(64, None, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert lp(64, fake, n_lw - 8) == hyb.HYB_ERR_INVALID_ARG
+    assert lp(64, fake + 4, n_lw) == hyb.HYB_ERR_INVALID_ARG
+    assert lp(64, None, 0, B=0) == hyb.HYB_OK    # empty batch: nothing to do, nothing needed
 
 
 def test_dispatch_rejects_shared_caches_and_bad_types(hyb):
@@ -111,6 +119,11 @@ def test_dispatch_rejects_shared_caches_and_bad_types(hyb):
     # Linear layer without a state pool
     lin = hyb.layer_io(out=f, q=f, k=f, v=f, num_state_slots=2)
     assert hyb.hyb_layer_dispatch([1], 1, 0, [lin], meta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
+    # prefill mode: a Linear layer needs the chunked prefill's handoff workspace
+    pmeta = hyb.batch_meta(2, 4, block_tables=f, slot_mapping=f, cu_q_lens=f, state_slots=f, max_q_len=2)
+    linp = hyb.layer_io(out=f, q=f, k=f, v=f, state_pool=f + 4096, num_state_slots=2)
+    assert hyb.hyb_layer_dispatch([1], 1, 1, [linp], pmeta, d, 64, None, 0, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_layer_dispatch([1], 1, 1, [linp], pmeta, d, 64, f + 8192, 64, 0) == hyb.HYB_ERR_INVALID_ARG
     # empty plan is a no-op
     assert hyb.hyb_layer_dispatch([], 0, 0, [], meta, d, 64, None, 0, 0) == hyb.HYB_OK
 

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_helpers import (assert_out_close, assert_states_close, empty_rows, poisoned_pool,
+from gpu_helpers import (lin_ws, assert_out_close, assert_states_close, empty_rows, poisoned_pool,
                          same_bytes, to_dev, to_host)
 
 pytestmark = pytest.mark.gpu
@@ -129,7 +129,7 @@ def _linear_gpu(hyb, c, chunk=64, ctx=None, pool_d=None):
     hyb.check(hyb.hyb_linear_attn_chunked_prefill(
         out, to_dev(c["q"]), to_dev(c["k"]), to_dev(c["v"]), to_dev(c["cu"]),
         None if ctx is None else to_dev(np.asarray(ctx, np.int32)), pool_d, c["NS"], to_dev(c["slots"]),
-        to_dev(c["reset"]), c["B"], c["T"], int(c["lens"].max()), c["H"], c["D"], chunk, W.BF16))
+        to_dev(c["reset"]), c["B"], c["T"], int(c["lens"].max()), c["H"], c["D"], chunk, W.BF16, *lin_ws()))
     torch.cuda.synchronize()
     return out, pool_d
 
@@ -156,12 +156,13 @@ def test_chunked_linear_split_calls_equal_one_call(hyb, devstatus):
     o_ref, s_ref = oracle.linear_recurrence(q, k, v, [0, n])
     pool = torch.zeros((1, H, D, D), device="cuda")
     outs = []
+    lws = lin_ws()                                       # one workspace, calls in stream order
     for lo, hi in ((0, split), (split, n)):
         out = empty_rows((hi - lo, H, D), W.BF16)
         hyb.check(hyb.hyb_linear_attn_chunked_prefill(
             out, to_dev(q[lo:hi]), to_dev(k[lo:hi]), to_dev(v[lo:hi]), to_dev(np.array([0, hi - lo], np.int32)),
             to_dev(np.array([lo], np.int32)), pool, 1, to_dev(np.zeros(1, np.int32)),
-            to_dev(np.array([1 if lo == 0 else 0], np.uint8)), 1, hi - lo, hi - lo, H, D, 64, W.BF16))
+            to_dev(np.array([1 if lo == 0 else 0], np.uint8)), 1, hi - lo, hi - lo, H, D, 64, W.BF16, *lws))
         outs.append(to_host(out))
     torch.cuda.synchronize()
     assert_out_close(np.concatenate(outs), o_ref)
@@ -216,10 +217,11 @@ def test_chunked_linear_graph_replays_with_new_inputs(hyb, devstatus):
     cu_d, slots_d, reset_d = to_dev(c["cu"]), to_dev(c["slots"]), to_dev(c["reset"])
     pool_d = to_dev(c["pool"])
     out = empty_rows((c["T"], c["H"], c["D"]), W.BF16)
+    lws = lin_ws()                                       # kept for every replay
 
     def call():
         hyb.check(hyb.hyb_linear_attn_chunked_prefill(out, qd, kd, vd, cu_d, None, pool_d, c["NS"], slots_d,
-                                                      reset_d, c["B"], c["T"], 300, c["H"], c["D"], 64, W.BF16))
+                                                      reset_d, c["B"], c["T"], 300, c["H"], c["D"], 64, W.BF16, *lws))
 
     call()                                               # first call outside the capture
     torch.cuda.synchronize()
@@ -241,6 +243,35 @@ def test_chunked_linear_graph_replays_with_new_inputs(hyb, devstatus):
     assert devstatus() == (0, 0)
 
 
+def test_chunked_linear_two_streams_at_once(hyb, devstatus):
+    """Two chunked-prefill calls, each with its own handoff workspace, issued on two streams
+    back to back, four times: grids of 16 CTAs leave room for both to be resident at once,
+    and the unequal chains (16 and 3 chunks) make each call hand states between its CTAs.
+    Both calls finish without a handoff timeout and each equals the recurrence on its own
+    inputs: a call only ever reads its own workspace's flags."""
+    cases = [_linear_case(700 + i, [2000, 300], H=8) for i in range(2)]
+    refs = [oracle.linear_recurrence(c["q"], c["k"], c["v"], c["cu"], c["pool"], c["slots"], c["reset"])
+            for c in cases]
+    dev = []
+    for c in cases:
+        dev.append(dict(q=to_dev(c["q"]), k=to_dev(c["k"]), v=to_dev(c["v"]), cu=to_dev(c["cu"]),
+                        slots=to_dev(c["slots"]), reset=to_dev(c["reset"]), ws=lin_ws(),
+                        out=empty_rows((c["T"], c["H"], c["D"]), W.BF16)))
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    for rep in range(4):
+        pools = [to_dev(c["pool"]) for c in cases]
+        torch.cuda.synchronize()
+        for c, x, pool, s in zip(cases, dev, pools, streams):
+            hyb.check(hyb.hyb_linear_attn_chunked_prefill(
+                x["out"], x["q"], x["k"], x["v"], x["cu"], None, pool, c["NS"], x["slots"], x["reset"], c["B"],
+                c["T"], int(c["lens"].max()), c["H"], c["D"], 64, W.BF16, *x["ws"], s))
+        torch.cuda.synchronize()
+        for i, (c, x, pool, (o_ref, s_ref)) in enumerate(zip(cases, dev, pools, refs)):
+            assert_out_close(x["out"], o_ref, f"call {i}, round {rep}")
+            assert_states_close(to_host(pool)[c["slots"]], s_ref, f"call {i}, round {rep} state")
+        assert devstatus() == (0, 0)
+
+
 def test_chunked_linear_full_workload_sampled(hyb, devstatus):
     """8 requests x 8192 tokens, H=32, D=128, chunk 64, zero initial state: whole output
     shape computed on the GPU; sampled (request, head) chains against the recurrence."""
@@ -255,7 +286,7 @@ def test_chunked_linear_full_workload_sampled(hyb, devstatus):
     out = empty_rows((T, H, D), W.BF16)
     hyb.check(hyb.hyb_linear_attn_chunked_prefill(out, to_dev(q), to_dev(k), to_dev(v), to_dev(cu), None, pool, B,
                                                   to_dev(slots), to_dev(np.ones(B, np.uint8)), B, T, 8192, H, D, 64,
-                                                  W.BF16))
+                                                  W.BF16, *lin_ws()))
     torch.cuda.synchronize()
     outh, st = to_host(out), to_host(pool)
     for b, h in [(0, 0), (0, 1), (3, 17), (5, 9), (7, 31)]:
@@ -294,12 +325,12 @@ def test_prefill_dispatch_equals_per_op_calls(hyb, devstatus):
                                   reset=reset, max_q_len=int(lens.max()))
             hyb.check(hyb.hyb_layer_dispatch([0, 1], 2, 1, [hyb.layer_io(fo, q, k, v, kc, vc),
                                                             hyb.layer_io(lo, ql, kl, vl, state_pool=st, num_state_slots=B)],
-                                             meta, d, 64, None, 0))
+                                             meta, d, 64, *lin_ws()))
         else:
             hyb.check(hyb.hyb_paged_kv_append(k, v, slot, T, kc, vc, d))
             hyb.check(hyb.hyb_paged_attn_prefill_causal(fo, q, kc, vc, bt, cu_d, None, B, T, int(lens.max()), d))
             hyb.check(hyb.hyb_linear_attn_chunked_prefill(lo, ql, kl, vl, cu_d, None, st, B, slots, reset, B, T,
-                                                          int(lens.max()), H, D, 64, W.BF16))
+                                                          int(lens.max()), H, D, 64, W.BF16, *lin_ws()))
         torch.cuda.synchronize()
         res.append([to_host(x) for x in (fo, lo, kc, vc, st)])
     for a, b in zip(*res):

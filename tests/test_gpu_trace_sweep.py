@@ -7,7 +7,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_helpers import assert_out_close, decode_case, empty_rows, same_bytes, to_dev, to_host
+from gpu_helpers import lin_ws, assert_out_close, decode_case, empty_rows, same_bytes, to_dev, to_host
 
 pytestmark = pytest.mark.gpu
 
@@ -118,7 +118,7 @@ def test_prefill_kernels_are_deterministic(hyb, devstatus):
         st = torch.zeros((len(lens), H, D, D), device="cuda")
         hyb.check(hyb.hyb_linear_attn_chunked_prefill(lo, q, k, v, cu_d, None, st, len(lens),
                                                       to_dev(np.arange(len(lens), dtype=np.int32)), None,
-                                                      len(lens), T, int(lens.max()), H, D, 64, W.BF16))
+                                                      len(lens), T, int(lens.max()), H, D, 64, W.BF16, *lin_ws()))
         torch.cuda.synchronize()
         res.append((to_host(out), to_host(lo), to_host(st)))
     assert all(same_bytes(a, b) for a, b in zip(res[0], res[1]))

@@ -10,7 +10,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_helpers import (PagedCase as Case, assert_out_close, decode_case as _decode_case,
+from gpu_helpers import (lin_ws, PagedCase as Case, assert_out_close, decode_case as _decode_case,
                          decode_gpu as _decode_gpu, empty_rows, released as _released,
                          same_bytes, to_dev, to_host)
 
@@ -136,8 +136,9 @@ def test_dispatch_sliding_layers_equal_per_op_calls(hyb, devstatus, mode, bs):
     slot = torch.empty(T, dtype=torch.int64, device="cuda")
     hyb.check(hyb.hyb_slot_mapping(slot, bt, cu_d, ctx_d, B, T, d0))
     msl = int((c.ctx + c.qlens).max())
-    ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, msl, d0)
-    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+    # one workspace for both modes: decode partials, or the Linear prefill's handoff flags
+    ws_n = max(hyb.hyb_paged_attn_decode_workspace_size(B, msl, d0), hyb.hyb_linear_attn_chunked_prefill_workspace_size())
+    ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda")
     st0 = W.synthetic_state(W.rng(472), B, H, D, c.ctx + c.qlens)
     slots_d = to_dev(np.arange(B, dtype=np.int32))
     reset_d = to_dev(np.zeros(B, np.uint8))
@@ -166,7 +167,7 @@ def test_dispatch_sliding_layers_equal_per_op_calls(hyb, devstatus, mode, bs):
             else:
                 hyb.check(hyb.hyb_linear_attn_chunked_prefill(outs2[l], q, k, v, cu_d, ctx_d, pools2[l], B,
                                                               slots_d, reset_d, B, T, int(c.qlens.max()),
-                                                              H, D, 64, W.BF16))
+                                                              H, D, 64, W.BF16, *lin_ws()))
             continue
         dl = c.dims(hyb, windows[l])
         hyb.check(hyb.hyb_paged_kv_append(k, v, slot, T, kcs2[l], vcs2[l], dl))

@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import workloads as W
-from gpu_helpers import (as_f64, assert_out_close, assert_states_close, empty_rows,
+from gpu_helpers import (lin_ws, as_f64, assert_out_close, assert_states_close, empty_rows,
                          poisoned_pool, to_dev, to_host)
 from test_gpu_decode import DecodeStep
 
@@ -54,12 +54,12 @@ def _tiny_flow(hyb, use_dispatch, chunk):
         meta = hyb.batch_meta(B, T, block_tables=bt, slot_mapping=slot, cu_q_lens=cu_d,
                               state_slots=slots_d, reset=reset_d, max_q_len=int(prompts.max()))
         layers = [hyb.layer_io(fo, q, k, v, kc, vc), hyb.layer_io(lo, ql, kl, vl, state_pool=st_pool, num_state_slots=3)]
-        hyb.check(hyb.hyb_layer_dispatch([0, 1], 2, 1, layers, meta, d, chunk, None, 0))
+        hyb.check(hyb.hyb_layer_dispatch([0, 1], 2, 1, layers, meta, d, chunk, *lin_ws()))
     else:
         hyb.check(hyb.hyb_paged_kv_append(k, v, slot, T, kc, vc, d))
         hyb.check(hyb.hyb_paged_attn_prefill_causal(fo, q, kc, vc, bt, cu_d, None, B, T, int(prompts.max()), d))
         hyb.check(hyb.hyb_linear_attn_chunked_prefill(lo, ql, kl, vl, cu_d, None, st_pool, 3, slots_d,
-                                                      reset_d, B, T, int(prompts.max()), H, D, chunk, W.F32))
+                                                      reset_d, B, T, int(prompts.max()), H, D, chunk, W.F32, *lin_ws()))
     res["full_out"].append(to_host(fo))
     res["lin_out"].append(to_host(lo))
     ws = torch.empty(1 << 16, dtype=torch.uint8, device="cuda")
