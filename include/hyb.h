@@ -129,7 +129,8 @@ hyb_status_t hyb_paged_kv_append(const void* k, const void* v, const int64_t* sl
  * ranges of blocks (split-K) and merges the partial softmax states; `workspace`
  * holds the partials and must have hyb_paged_attn_decode_workspace_size() bytes
  * (0 is allowed when that size is 0). The result does not depend on how other
- * requests in the batch are split.
+ * requests in the batch are split. Limits: B <= 65535, num_heads <= 65535 and
+ * max_seq_len <= 2^24 (beyond them: HYB_ERR_UNSUPPORTED, nothing launched).
  * ------------------------------------------------------------------------- */
 size_t hyb_paged_attn_decode_workspace_size(int32_t B, int32_t max_seq_len,
                                             const hyb_attn_dims_t* d);

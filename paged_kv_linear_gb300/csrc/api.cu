@@ -7,7 +7,9 @@
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
+#include <map>
 #include <set>
+#include <tuple>
 #include <utility>
 #include <vector>
 
@@ -91,6 +93,20 @@ cudaError_t set_smem(const void* fn, int bytes) {
   return e;
 }
 
+int max_ctas_per_sm(const void* fn, int threads, int smem) {
+  const int d = cur_dev();
+  if (d < 0) return 1;
+  static std::map<std::tuple<const void*, int, int, int>, int> cache;
+  std::lock_guard<std::mutex> lk(g_mu);
+  const auto key = std::make_tuple(fn, d, threads, smem);
+  auto it = cache.find(key);
+  if (it != cache.end()) return it->second;
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess || n < 1) n = 1;
+  cache[key] = n;
+  return n;
+}
+
 // Address of this device's status word (looked up once per device, with it current).
 unsigned* status_word() {
   const int d = cur_dev();
@@ -145,9 +161,9 @@ hyb_status_t check_decode_args(const void* out, const void* q, const void* kc, c
   hyb_status_t st = check_dims(d);
   if (st != HYB_OK) return st;
   if (B < 0 || max_seq_len < 0) return HYB_ERR_INVALID_ARG;
-  if (d->num_heads > 65535) return HYB_ERR_UNSUPPORTED;
+  if (d->num_heads > 65535 || B > 65535) return HYB_ERR_UNSUPPORTED;   // grid.z = heads, grid.y = rows
   if ((int64_t)max_seq_len > (int64_t)d->max_blocks_per_seq * d->block_size) return HYB_ERR_INVALID_ARG;
-  if (max_seq_len > (1 << 24)) return HYB_ERR_UNSUPPORTED;   // grid.z = splits <= 65535
+  if (max_seq_len > (1 << 24)) return HYB_ERR_UNSUPPORTED;   // bounds the split-K workspace
   if (!decode_supported(d->dtype, d->head_dim)) return HYB_ERR_UNSUPPORTED;
   if (B == 0) return HYB_OK;
   if (!out || !q || !kc || !vc || !bt || !seq_lens) return HYB_ERR_INVALID_ARG;

@@ -68,6 +68,8 @@ def test_bad_arguments_rejected_before_launch(hyb):
     # head_dim without a kernel
     d7 = hyb.dims(4, 24, 100, 8)
     assert hyb.hyb_paged_attn_decode(fake, fake, fake, fake, fake, fake, 2, 32, d7, None, 0, 0) == hyb.HYB_ERR_UNSUPPORTED
+    # more rows than the decode grid takes (grid.y = rows <= 65535)
+    assert hyb.hyb_paged_attn_decode(fake, fake, fake, fake, fake, fake, 65536, 32, d, fake, 1 << 20, 0) == hyb.HYB_ERR_UNSUPPORTED
     # max_seq_len beyond the block table's capacity (8 blocks x 16)
     assert hyb.hyb_paged_attn_decode(fake, fake, fake, fake, fake, fake, 2, 129, d, fake, 1 << 20, 0) == hyb.HYB_ERR_INVALID_ARG
     # workspace too small for a split sequence
