@@ -254,13 +254,13 @@ hyb_status_t check_linear_prefill(const void* out, const void* q, const void* k,
 hyb_status_t run_decode(void* out, const void* q, const void* kc, const void* vc,
                         const int32_t* bt, const int32_t* seq_lens, int B, int max_seq_len,
                         const hyb_attn_dims_t* d, void* ws, unsigned* status, cudaStream_t s,
-                        const DecodeAppend* app = nullptr) {
+                        const DecodeAppend* app = nullptr, bool early = false) {
   if (B == 0) return HYB_OK;
   const DecodePlan p = plan_decode(B, d->num_heads, d->head_dim, max_seq_len, d->window);
   return cuda_status(launch_paged_decode(out, q, kc, vc, bt, seq_lens, nullptr, nullptr, B, 0,
                                          d->num_heads, d->head_dim, d->dtype, d->num_blocks,
                                          d->max_blocks_per_seq, d->block_size, max_seq_len,
-                                         d->scale, d->window, p, ws, status, s, app));
+                                         d->scale, d->window, p, ws, status, s, app, early));
 }
 
 hyb_status_t run_prefill(void* out, const void* q, const void* kc, const void* vc,
@@ -563,9 +563,11 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
       hyb_attn_dims_t dl = *d;
       dl.window = io.window;
       if (mode == HYB_MODE_DECODE) {         // append fused into the decode launch
+        // after the first layer, the kernel before this one is a layer of this dispatch,
+        // which writes none of this layer's cache and none of the batch metadata
         const DecodeAppend app{io.k, io.v, meta->slot_mapping};
         st = run_decode(io.out, io.q, io.k_cache, io.v_cache, meta->block_tables, meta->seq_lens,
-                        B, meta->max_seq_len, &dl, workspace, sw, s, &app);
+                        B, meta->max_seq_len, &dl, workspace, sw, s, &app, l > 0);
       } else {
         st = cuda_status(launch_kv_append(io.k, io.v, meta->slot_mapping, T, H, D, esize_of(dt),
                                           d->num_blocks, d->block_size, io.k_cache, io.v_cache,
@@ -578,7 +580,7 @@ hyb_status_t hyb_layer_dispatch(const int32_t* layer_types, int32_t L, int32_t m
       st = mode == HYB_MODE_DECODE
                ? cuda_status(launch_linear_step(io.out, io.q, io.k, io.v, io.state_pool,
                                                 io.num_state_slots, meta->state_slots, B, H, D,
-                                                dt, sw, s))
+                                                dt, sw, s, l > 0))
                : run_linear_prefill(io.out, io.q, io.k, io.v, meta->cu_q_lens, meta->ctx_lens,
                                     io.state_pool, io.num_state_slots, meta->state_slots,
                                     meta->reset, B, T, meta->max_q_len, H, D, chunk_size, dt,

@@ -107,12 +107,16 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict_
                     int rsh, int max_len, float scale_log2, int window, int max_splits,
                     float* __restrict__ ws_acc, float2* __restrict__ ws_ml,
                     const T* __restrict__ k_new, const T* __restrict__ v_new,
-                    const int64_t* __restrict__ slot_map, unsigned* status) {
+                    const int64_t* __restrict__ slot_map, int early, unsigned* status) {
   using E = Elt<T>;
   using S = DecodeShape<T, D>;
   constexpr int VEC = S::VEC, LPR = S::LPR, TPI = S::TPI, ITER = S::ITER, TILE = S::TILE;
 
-  pdl_wait();                              // inputs may come from the previous kernel
+  // early (decode after another layer of the same dispatch): this layer's cache, block table
+  // and lengths are not written by the kernels before it, so the row's length and block ids
+  // are read and its first K/V tiles requested before waiting for the previous kernel; q and
+  // the new row (which a model computes from the previous layer) are read after the wait.
+  if (!early) pdl_wait();                  // inputs may come from the previous kernel
   // decode: grid (splits, rows, H), the split index fastest; prefill: (rows, H, 1)
   const int h = PREFILL ? blockIdx.y : blockIdx.z, split = PREFILL ? 0 : blockIdx.x;
   int b, r, n_raw;                         // request, packed row of q/out, keys to attend
@@ -149,6 +153,7 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict_
   // warp that loads that position's tile also patches the row into shared memory, so the
   // attention sees exactly what an append followed by the decode would.
   int patch_sub = -1;                      // 16-token sub-tile holding position n - 1, if patched
+  int64_t app_slot = -1;                   // where this step's row goes (-1: nowhere)
   if (!PREFILL && k_new && split == nsplit - 1) {
     const int bsz = kBlockSize << rsh;
     int64_t slot = -1;
@@ -163,15 +168,7 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict_
       slot = -1;
     }
     if (slot >= 0) {
-      if (warp == kNW - 1) {
-        const int64_t blk = slot / bsz, off = slot - blk * bsz;
-        const int64_t dst = ((blk * H + h) * bsz + off) * D;
-        const int64_t src = ((int64_t)r * H + h) * D;
-        for (int e = lane; e < kRowChunks; e += 32) {
-          reinterpret_cast<uint4*>(kc + dst)[e] = reinterpret_cast<const uint4*>(k_new + src)[e];
-          reinterpret_cast<uint4*>(vc + dst)[e] = reinterpret_cast<const uint4*>(v_new + src)[e];
-        }
-      }
+      app_slot = slot;                     // stored below, once the inputs may be read
       if (n >= 1) {
         const int s_last = (n - 1) / kBlockSize;
         const int pb = btrow[s_last >> rsh];
@@ -186,14 +183,6 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict_
   float* red_ml = red_acc + kNW * D;
 
   const int c = lane % LPR, rr = lane / LPR;
-  float qf[VEC];
-  {
-    const uint4 u = *reinterpret_cast<const uint4*>(q + ((int64_t)r * H + h) * D + c * VEC);
-    E::unpack(u, qf);
-#pragma unroll
-    for (int e = 0; e < VEC; ++e) qf[e] *= scale_log2;
-  }
-
   const int first = blk_begin + warp;   // this warp's logical blocks: first + i*kNW
   const int ntiles = first < blk_end ? (blk_end - first + kNW - 1) / kNW : 0;
   // 16-token sub-tile s lives in block btrow[s >> rsh], rows (s & sub_mask) * 16 onwards
@@ -218,6 +207,25 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict_
   };
   if (lane == 0)
     for (int i = 0; i < min(kNST, ntiles); ++i) issue(i);
+
+  if (early) pdl_wait();
+  if (app_slot >= 0 && warp == kNW - 1) {  // the append: this step's row into its slot
+    const int bsz = kBlockSize << rsh;
+    const int64_t blk = app_slot / bsz, off = app_slot - blk * bsz;
+    const int64_t dst = ((blk * H + h) * bsz + off) * D;
+    const int64_t src = ((int64_t)r * H + h) * D;
+    for (int e = lane; e < kRowChunks; e += 32) {
+      reinterpret_cast<uint4*>(kc + dst)[e] = reinterpret_cast<const uint4*>(k_new + src)[e];
+      reinterpret_cast<uint4*>(vc + dst)[e] = reinterpret_cast<const uint4*>(v_new + src)[e];
+    }
+  }
+  float qf[VEC];
+  {
+    const uint4 u = *reinterpret_cast<const uint4*>(q + ((int64_t)r * H + h) * D + c * VEC);
+    E::unpack(u, qf);
+#pragma unroll
+    for (int e = 0; e < VEC; ++e) qf[e] *= scale_log2;
+  }
 
   float m = -INFINITY, l = 0.f, acc[VEC];
 #pragma unroll
@@ -387,11 +395,15 @@ __global__ void __launch_bounds__(128)
 decode_combine_kernel(T* __restrict__ out, const int32_t* __restrict__ seq_lens, int H, int MBt,
                       int max_len, int window, int max_splits, const float* __restrict__ ws_acc,
                       const float2* __restrict__ ws_ml) {
-  pdl_wait();
+  // seq_lens was read by the decode launched just before, after its own wait: rows with one
+  // split leave before waiting, and the next kernel may launch at once (it waits for this
+  // one to complete before reading anything it writes)
   const int r = blockIdx.x, h = blockIdx.y;
   const int n = clamp_len(seq_lens[r], max_len, MBt);
   const int nsplit = decode_splits(n, window);
   if (nsplit <= 1) return;
+  pdl_trigger();
+  pdl_wait();
   const int64_t rh = (int64_t)r * H + h;
   const float2* ml = ws_ml + rh * max_splits;
   const float* acc = ws_acc + rh * max_splits * D;
@@ -431,7 +443,6 @@ decode_combine_kernel(T* __restrict__ out, const int32_t* __restrict__ seq_lens,
     }
     Elt<T>::store(out + rh * D + t, L > 0.f ? A / L : 0.f);
   }
-  pdl_trigger();
 }
 
 template <typename T, int D>
@@ -439,12 +450,13 @@ cudaError_t launch_typed(void* out, const void* q, const void* kc, const void* v
                          const int32_t* bt, const int32_t* seq_lens, const int32_t* cu,
                          const int32_t* ctx, int R, int max_q, int H, int NB, int MB,
                          int bs, int max_len, float scale, int window, const DecodePlan& plan,
-                         void* ws, unsigned* status, cudaStream_t s, const DecodeAppend* app) {
+                         void* ws, unsigned* status, cudaStream_t s, const DecodeAppend* app,
+                         bool early) {
   using Sh = DecodeShape<T, D>;
   const bool prefill = cu != nullptr, win = window > 0;
   using K = void (*)(T*, const T*, T*, T*, const int32_t*, const int32_t*, const int32_t*,
                      const int32_t*, int, int, int, int, int, int, float, int, int, float*,
-                     float2*, const T*, const T*, const int64_t*, unsigned*);
+                     float2*, const T*, const T*, const int64_t*, int, unsigned*);
   const int rsh = log2_int(bs / kBlockSize);
   const K kern = prefill ? (win ? paged_decode_kernel<T, D, true, true>
                                 : paged_decode_kernel<T, D, true, false>)
@@ -467,7 +479,7 @@ cudaError_t launch_typed(void* out, const void* q, const void* kc, const void* v
                  bt, seq_lens, cu, ctx, max_q, H, NB, MB, rsh, max_len, scale_log2, window,
                  max_splits, ws_acc, ws_ml, fused ? (const T*)app->k : (const T*)nullptr,
                  fused ? (const T*)app->v : (const T*)nullptr,
-                 fused ? app->slot : (const int64_t*)nullptr, status);
+                 fused ? app->slot : (const int64_t*)nullptr, (early && !prefill) ? 1 : 0, status);
   count_launch();
   if (e != cudaSuccess || max_splits == 1) return e;
   e = launch_pdl(decode_combine_kernel<T, D>, dim3(R, H), dim3(128), 0, s, (T*)out, seq_lens, H,
@@ -501,12 +513,12 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* kc, const 
                                 const int32_t* ctx, int R, int max_q, int H, int D, int dtype,
                                 int NB, int MB, int bs, int max_len, float scale, int window,
                                 const DecodePlan& plan, void* ws, unsigned* status,
-                                cudaStream_t s, const DecodeAppend* app) {
+                                cudaStream_t s, const DecodeAppend* app, bool early) {
   if (R == 0 || (cu && max_q == 0)) return cudaSuccess;
 #define HYB_DEC(T, DD)                                                                       \
   if (D == DD)                                                                               \
     return launch_typed<T, DD>(out, q, kc, vc, bt, seq_lens, cu, ctx, R, max_q, H, NB, MB, bs, \
-                               max_len, scale, window, plan, ws, status, s, app);
+                               max_len, scale, window, plan, ws, status, s, app, early);
   if (dtype == HYB_BF16) {
     HYB_DEC(__nv_bfloat16, 16)
     HYB_DEC(__nv_bfloat16, 32)

@@ -74,6 +74,10 @@ bool decode_supported(int dtype, int D);
 // at slot[r] (-1: none) inside the decode launch, and the attention sees them; equal to a
 // KV append with the same slots followed by the decode, for slot[r] = -1 or the slot of
 // position seq_lens[r] - 1.
+// early (decode mode): the previous kernel on the stream writes neither this call's cache nor
+// its block table, lengths or slot mapping (true for every decode of a dispatch after its
+// first layer); the kernel then reads those and requests its first K/V tiles before waiting
+// for the previous kernel to complete.
 struct DecodeAppend {
   const void* k;
   const void* v;
@@ -84,7 +88,8 @@ cudaError_t launch_paged_decode(void* out, const void* q, const void* kc, const 
                                 const int32_t* ctx, int R, int max_q, int H, int D, int dtype,
                                 int NB, int MB, int bs, int max_len, float scale, int window,
                                 const DecodePlan& plan, void* ws, unsigned* status,
-                                cudaStream_t s, const DecodeAppend* app = nullptr);
+                                cudaStream_t s, const DecodeAppend* app = nullptr,
+                                bool early = false);
 
 bool linear_supported(int dtype, int D);
 // 16-bit state pool (state_dtype HYB_BF16 or HYB_F16), same shapes as launch_linear_step
@@ -92,9 +97,10 @@ cudaError_t launch_linear_step_lowp(void* out, const void* q, const void* k, con
                                     void* pool, int state_dtype, int NS, const int32_t* slots,
                                     int B, int H, int D, int dtype, unsigned* status,
                                     cudaStream_t s);
+// early: as for the decode (the previous kernel writes neither this pool nor the slots)
 cudaError_t launch_linear_step(void* out, const void* q, const void* k, const void* v,
                                float* pool, int NS, const int32_t* slots, int B, int H, int D,
-                               int dtype, unsigned* status, cudaStream_t s);
+                               int dtype, unsigned* status, cudaStream_t s, bool early = false);
 cudaError_t launch_linear_prefill_simt(void* out, const void* q, const void* k, const void* v,
                                        const int32_t* cu, const int32_t* ctx, float* pool,
                                        int NS, const int32_t* slots, const uint8_t* reset, int B,

@@ -57,12 +57,15 @@ template <typename T, int D>
 __global__ void __launch_bounds__(StepShape<D>::THREADS)
 linear_step_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __restrict__ k,
                    const T* __restrict__ v, float* __restrict__ pool, int NS,
-                   const int32_t* __restrict__ slots, int H, unsigned* status) {
+                   const int32_t* __restrict__ slots, int H, int early, unsigned* status) {
   using Sh = StepShape<D>;
   constexpr int COLS = Sh::COLS, TPR = Sh::TPR, RPP = Sh::RPP, PASSES = Sh::PASSES;
   __shared__ float red[RPP][COLS];
 
-  pdl_wait();
+  // early (a step after another layer of the same dispatch): the state pool and the slots are
+  // not written by the kernels before it, so the state is loaded before waiting for the
+  // previous kernel; q, k and v (which a model computes from the previous layer) after.
+  if (!early) pdl_wait();
   const int cb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int slot = slots[b];
   if (slot < 0 || slot >= NS) {
@@ -78,6 +81,7 @@ linear_step_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __rest
 #pragma unroll
   for (int p = 0; p < PASSES; ++p)
     st[p] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(rg + p * RPP) * D + col));
+  if (early) pdl_wait();
   const float v0 = ldf(v + rowq + col), v1 = ldf(v + rowq + col + 1);
   const float v2 = ldf(v + rowq + col + 2), v3 = ldf(v + rowq + col + 3);
 
@@ -242,12 +246,12 @@ linear_prefill_simt_kernel(T* __restrict__ out, const T* __restrict__ q,
 template <typename T, int D>
 cudaError_t step_typed(void* out, const void* q, const void* k, const void* v, float* pool,
                        int NS, const int32_t* slots, int B, int H, unsigned* status,
-                       cudaStream_t s) {
+                       cudaStream_t s, bool early) {
   using Sh = StepShape<D>;
   dim3 grid(D / Sh::COLS, H, B);
   const cudaError_t e = launch_pdl(linear_step_kernel<T, D>, grid, dim3(Sh::THREADS), 0, s, (T*)out,
                                    (const T*)q, (const T*)k, (const T*)v, pool, NS, slots, H,
-                                   status);
+                                   early ? 1 : 0, status);
   count_launch();
   return e;
 }
@@ -289,10 +293,10 @@ bool linear_supported(int dtype, int D) {
 
 cudaError_t launch_linear_step(void* out, const void* q, const void* k, const void* v,
                                float* pool, int NS, const int32_t* slots, int B, int H, int D,
-                               int dtype, unsigned* status, cudaStream_t s) {
+                               int dtype, unsigned* status, cudaStream_t s, bool early) {
   if (B == 0) return cudaSuccess;
 #define HYB_STEP(T, DD) \
-  if (D == DD) return step_typed<T, DD>(out, q, k, v, pool, NS, slots, B, H, status, s);
+  if (D == DD) return step_typed<T, DD>(out, q, k, v, pool, NS, slots, B, H, status, s, early);
   if (dtype == HYB_BF16) {
     HYB_STEP(__nv_bfloat16, 16) HYB_STEP(__nv_bfloat16, 32) HYB_STEP(__nv_bfloat16, 64)
     HYB_STEP(__nv_bfloat16, 128) HYB_STEP(__nv_bfloat16, 256)
