@@ -208,6 +208,10 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict_
   if (lane == 0)
     for (int i = 0; i < min(kNST, ntiles); ++i) issue(i);
 
+  // The next kernel may launch now: it waits for this one to complete before reading what
+  // this one writes. (A kernel that is not early has already waited, so whatever an early
+  // kernel launched after it reads before its own wait was complete before this launch.)
+  pdl_trigger();
   if (early) pdl_wait();
   if (app_slot >= 0 && warp == kNW - 1) {  // the append: this step's row into its slot
     const int bsz = kBlockSize << rsh;
@@ -320,7 +324,6 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict_
     for (int e = 0; e < VEC; ++e) acc[e] = 0.f;
   }
 
-  pdl_trigger();                           // the next kernel may launch; it waits for our stores
   // merge the token sub-rows of the warp (lanes with the same c)
 #pragma unroll
   for (int o = LPR; o < 32; o <<= 1)

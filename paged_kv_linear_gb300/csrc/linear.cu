@@ -81,6 +81,7 @@ linear_step_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __rest
 #pragma unroll
   for (int p = 0; p < PASSES; ++p)
     st[p] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(rg + p * RPP) * D + col));
+  pdl_trigger();                           // the next kernel may launch (it waits for this one)
   if (early) pdl_wait();
   const float v0 = ldf(v + rowq + col), v1 = ldf(v + rowq + col + 1);
   const float v2 = ldf(v + rowq + col + 2), v3 = ldf(v + rowq + col + 3);
@@ -101,7 +102,6 @@ linear_step_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __rest
     o2 = fmaf(qi, s.z, o2);
     o3 = fmaf(qi, s.w, o3);
   }
-  pdl_trigger();
   red[rg][tc * 4 + 0] = o0;
   red[rg][tc * 4 + 1] = o1;
   red[rg][tc * 4 + 2] = o2;
