@@ -1008,6 +1008,7 @@ def bench_ours(args, dist):
                           "share_of_step": round(n_full * full_ms / step_inst_ms, 4)},
            "linear_layer": {"ms": round(lin_ms, 5), "GB/s": round(lin_bytes / (lin_ms * 1e-3) / 1e9, 1),
                             "frac": round(lin_bytes / (lin_ms * 1e-3) / 1e9 / hbm_peak, 4), "layers": L - n_full,
+                            "traffic": _traffic("linear_step_hybrid", "linear.cu"),
                             "share_of_step": round((L - n_full) * lin_ms / step_inst_ms, 4)},
            "instrumented_step_ms": round(step_inst_ms, 5),
            "note": (f"from the {len(evs)} instrumented steps (every {INSTR}th), one dispatch call per run of "
