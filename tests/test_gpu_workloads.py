@@ -457,3 +457,78 @@ def test_dispatch_step_captured_in_cuda_graph_replays_bit_identically(hyb, devst
         for x, y in (zip(a, b) if isinstance(a, tuple) else [(a, b)]):
             assert torch.equal(x.view(torch.uint8), y.view(torch.uint8))
     assert devstatus() == (0, 0)
+
+
+def test_dispatch_sees_inputs_written_just_before_it(hyb, devstatus):
+    """Every layer of a decode dispatch after the first reads its lengths, block ids and cache
+    tiles (a Linear layer: its state) before waiting for the kernel launched before it. Here
+    every input of the call (q/k/v, caches, states and the batch metadata) is written on the
+    same stream right before the dispatch, with no synchronisation, the largest copies last;
+    the outputs, caches and states must equal per-op calls made after everything settled."""
+    lens = np.array([3000, 40, 700, 5, 1500, 128, 513, 2048], np.int32)
+    B, H, D = len(lens), 4, 128
+    lt = [0, 0, 1, 0, 0, 0, 1, 0]
+    g = W.rng(901)
+    pool = W.block_pool(g, lens, slack=8.0)              # a big pool: long copies
+    NB, MB = pool.num_blocks, pool.max_blocks
+    d = hyb.dims(H, D, NB, MB, W.BF16)
+    msl = int(lens.max())
+    slots_h = g.permutation(B).astype(np.int32)
+    true = []
+    for l, t in enumerate(lt):
+        x = {n: to_dev(W.rows(g, (B, H, D), D, W.BF16)) for n in ("q", "k", "v")}
+        if t == 0:
+            x["k_cache"] = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device="cuda"), 5000 + l, D)
+            x["v_cache"] = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device="cuda"), 6000 + l, D)
+        else:
+            x["state_pool"] = W.device_state_(torch.empty((B, H, D, D), device="cuda"), 7000 + l, lens, D)
+        true.append(x)
+    meta_true = {"lens": to_dev(lens), "bt": to_dev(pool.block_tables), "slots": to_dev(slots_h)}
+    torch.cuda.synchronize()
+    # the dispatch's own buffers hold NaN / garbage until the copies below land
+    bufs = [{n: torch.full_like(v, float("nan")) for n, v in x.items()} for x in true]
+    outs = [torch.empty((B, H, D), dtype=torch.bfloat16, device="cuda") for _ in lt]
+    meta_bufs = {"lens": torch.zeros_like(meta_true["lens"]), "bt": torch.full_like(meta_true["bt"], -1),
+                 "slots": torch.full_like(meta_true["slots"], -1)}
+    ws_n = hyb.hyb_paged_attn_decode_workspace_size(B, msl, d)
+    ws = torch.empty(max(ws_n, 16), dtype=torch.uint8, device="cuda")
+    meta = hyb.batch_meta(B, B, seq_lens=meta_bufs["lens"], block_tables=meta_bufs["bt"],
+                          state_slots=meta_bufs["slots"], max_seq_len=msl)
+    ios = [hyb.layer_io(outs[l], b["q"], b["k"], b["v"], b.get("k_cache"), b.get("v_cache"), b.get("state_pool"), B)
+           for l, b in enumerate(bufs)]
+    s = torch.cuda.current_stream()
+    for n in meta_bufs:
+        meta_bufs[n].copy_(meta_true[n])
+    for b, x in zip(bufs, true):
+        for n in ("q", "k", "v"):
+            b[n].copy_(x[n])
+    for b, x in reversed(list(zip(bufs, true))):         # caches of the last layers last
+        for n in ("k_cache", "v_cache", "state_pool"):
+            if n in b:
+                b[n].copy_(x[n])
+    hyb.check(hyb.hyb_layer_dispatch(lt, len(lt), 0, ios, meta, d, 64, ws, ws_n, s.cuda_stream))
+    torch.cuda.synchronize()
+    # per-op reference on the settled inputs
+    ref_out = []
+    slot = torch.empty(B, dtype=torch.int64, device="cuda")
+    hyb.check(hyb.hyb_slot_mapping(slot, meta_true["bt"], to_dev(np.arange(B + 1, dtype=np.int32)),
+                                   to_dev(lens - 1), B, B, d))
+    for t, x in zip(lt, true):
+        o = torch.empty((B, H, D), dtype=torch.bfloat16, device="cuda")
+        if t == 0:
+            hyb.check(hyb.hyb_paged_kv_append(x["k"], x["v"], slot, B, x["k_cache"], x["v_cache"], d))
+            hyb.check(hyb.hyb_paged_attn_decode(o, x["q"], x["k_cache"], x["v_cache"], meta_true["bt"],
+                                                meta_true["lens"], B, msl, d, ws, ws_n))
+        else:
+            hyb.check(hyb.hyb_linear_attn_step(o, x["q"], x["k"], x["v"], x["state_pool"], B, meta_true["slots"],
+                                               B, H, D, W.BF16))
+        ref_out.append(o)
+    torch.cuda.synchronize()
+    for l, (b, x) in enumerate(zip(bufs, true)):
+        assert torch.equal(outs[l].view(torch.int16), ref_out[l].view(torch.int16)), f"layer {l} output"
+        for n in ("k_cache", "v_cache"):
+            if n in b:
+                assert torch.equal(b[n].view(torch.int16), x[n].view(torch.int16)), f"layer {l} {n}"
+        if "state_pool" in b:
+            assert torch.equal(b["state_pool"].view(torch.int32), x["state_pool"].view(torch.int32)), f"layer {l} state"
+    assert devstatus() == (0, 0)
