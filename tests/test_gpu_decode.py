@@ -83,6 +83,23 @@ def test_decode_step_matches_oracle(hyb, devstatus, dtype, H, D, lens):
     assert devstatus() == (0, 0)
 
 
+def test_decode_at_the_largest_batch_the_grid_takes(hyb, devstatus):
+    """65 535 rows, the most the decode grid holds (rows are its y dimension): short rows with
+    one split and every 1000th row long enough for two, so both the split kernel and the
+    combine run over the whole batch; the step matches the oracle (slots bit-exact)."""
+    B = 65535
+    g = W.rng(555)
+    lens = g.integers(1, 41, size=B).astype(np.int32)
+    lens[::1000] = 600
+    case = DecodeStep(556, lens, 1, 16, W.F32)
+    sm_ref, kc_ref, vc_ref, out_ref = case.oracle_run()
+    slot, kc, vc, out = case.gpu_run(hyb)
+    assert np.array_equal(to_host(slot), sm_ref)
+    assert same_bytes(to_host(kc), kc_ref) and same_bytes(to_host(vc), vc_ref)
+    assert_out_close(out, out_ref, "decode out, 65535 rows")
+    assert devstatus() == (0, 0)
+
+
 def test_decode_zero_length_gives_zeros(hyb, devstatus):
     case = DecodeStep(7, [5, 1, 40], 4, 128, W.BF16)
     d = case.dims(hyb)
