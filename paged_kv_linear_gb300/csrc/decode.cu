@@ -16,6 +16,14 @@
 // small kernel (log-sum-exp combine). The split size is a constant number of blocks, so
 // a request's result does not depend on the rest of the batch.
 //
+// The grid is (split, row, head) with the split index fastest. In a batch of mixed lengths
+// most CTAs of the grid have no split to run; with the split index slowest, the long rows'
+// later splits were dispatched behind planes of such empty CTAs and ran alone at the end.
+//
+// In a decode dispatch, a Full layer after the first reads its row length and block ids and
+// requests its first K/V tiles before waiting for the previous kernel (which writes neither
+// this layer's cache nor the batch metadata); q and the new row are read after the wait.
+//
 // The same kernel serves as the CUDA-core causal prefill for shapes without a
 // tensor-core kernel (PREFILL = true: one row per packed query token, n = position + 1,
 // one CTA walks all of the row's blocks).
