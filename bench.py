@@ -1106,6 +1106,12 @@ def bench_ours(args, dist):
     e2e_ms = dist.max(e0.elapsed_time(e1) / e2e_steps)
     e2e_val = units / (e2e_ms * 1e-3)
     _check_device(hyb)
+    # The Full layers' outputs are the same every step (same inputs; the append rewrites the
+    # same slots): the last end-to-end step's host copy must equal the device-timed step's.
+    last = sets[(e2e_steps - 1) % 2]["h_out"].view(L, B, H, D)
+    dev_out = out.view(torch.int16).cpu()
+    full_idx = [l for l, t in enumerate(lt) if t == 0]
+    e2e_match = bool(torch.equal(last[full_idx], dev_out[full_idx]))
     del sets
 
     # ---- CPU oracle beside it (rank 0, N = 1 only)
@@ -1143,7 +1149,8 @@ def bench_ours(args, dist):
         "e2e": {"value": round(e2e_val, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h),
                 "path": "hyb_layer_dispatch over all 32 layers; inputs in one pinned buffer, one copy each way, "
-                        "on copy streams double-buffered against the compute stream"},
+                        "on copy streams double-buffered against the compute stream",
+                "full_layer_outputs_equal_device_step": e2e_match},
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),
         "cpu_baseline": cpu,
