@@ -10,7 +10,7 @@ import torch
 import oracle
 import workloads as W
 from gpu_helpers import (lin_ws, as_f64, assert_out_close, assert_states_close, empty_rows,
-                         poisoned_pool, to_dev, to_host)
+                         poisoned_pool, same_bytes, to_dev, to_host)
 from test_gpu_decode import DecodeStep
 
 pytestmark = pytest.mark.gpu
@@ -282,7 +282,9 @@ def test_hybrid_32_layer_dispatch(hyb, devstatus, slot_from_table):
             io["state_pool"] = W.device_state_(torch.empty((B, H, D, D), device="cuda"), 3000 + l, db.seq_lens, D)
         layers_dev.append(io)
     before = {0: (to_host(layers_dev[0]["k_cache"]), to_host(layers_dev[0]["v_cache"])),
-              3: to_host(layers_dev[3]["state_pool"])}
+              3: to_host(layers_dev[3]["state_pool"]),
+              30: (to_host(layers_dev[30]["k_cache"]), to_host(layers_dev[30]["v_cache"])),
+              31: to_host(layers_dev[31]["state_pool"])}
     clones = [{k2: (v2.clone() if k2 in ("k_cache", "v_cache", "state_pool") else v2) for k2, v2 in io.items()}
               for io in layers_dev]
     for io in clones:
@@ -322,6 +324,19 @@ def test_hybrid_32_layer_dispatch(hyb, devstatus, slot_from_table):
     o_ref, s_ref = oracle.linear_step(q, k, v, before[3], to_host(slots))
     assert_out_close(layers_dev[3]["out"], o_ref, "layer 3")
     assert_states_close(to_host(layers_dev[3]["state_pool"])[to_host(slots)], s_ref)
+    # and the last Full and Linear layers, which read their cache / state before waiting
+    # for the layer before them
+    kc30, vc30 = before[30]
+    q, k, v = host_in[30]
+    oracle.kv_append(k, v, sm, kc30, vc30)
+    ref = oracle.full_decode(q, kc30, vc30, db.pool.block_tables, db.seq_lens, 1 / math.sqrt(D))
+    assert_out_close(layers_dev[30]["out"], ref, "layer 30")
+    assert same_bytes(to_host(layers_dev[30]["k_cache"]), kc30) and same_bytes(to_host(layers_dev[30]["v_cache"]), vc30)
+    del kc30, vc30
+    q, k, v = host_in[31]
+    o_ref, s_ref = oracle.linear_step(q, k, v, before[31], to_host(slots))
+    assert_out_close(layers_dev[31]["out"], o_ref, "layer 31")
+    assert_states_close(to_host(layers_dev[31]["state_pool"])[to_host(slots)], s_ref)
     assert devstatus() == (0, 0)
 
 
