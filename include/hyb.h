@@ -237,7 +237,7 @@ hyb_status_t hyb_linear_attn_step(void* out, const void* q, const void* k, const
  * drift over long sequences, while the vLLM/SGLang page stores it in fp16. This entry
  * point exists to measure that trade: same contract as hyb_linear_attn_step, but
  * state_pool holds state_dtype = HYB_BF16 or HYB_F16 elements ([num_slots][H][D][D],
- * 16-bit each, 8-byte aligned rows), and each element is updated as
+ * 16-bit each, 16-byte aligned), and each element is updated as
  *     S[i][j] <- round16(fmaf(k[i], v[j], float(S[i][j])))      (round to nearest even)
  *     out[j]  = sum_i q[i] * float(S[i][j])                      (after the update)
  * Half the state bytes of the fp32 step, at the cost of rounding every update to 8 (bf16)

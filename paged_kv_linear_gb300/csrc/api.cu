@@ -404,7 +404,7 @@ hyb_status_t hyb_linear_attn_step_lowp(void* out, const void* q, const void* k, 
                                        void* stream) {
   if (state_dtype != HYB_BF16 && state_dtype != HYB_F16) return HYB_ERR_INVALID_ARG;
   hyb_status_t st = check_linear_common(out, q, k, v, state_pool, num_state_slots, state_slots,
-                                        B, H, D, dtype, 8);
+                                        B, H, D, dtype);   // 16-byte aligned pool
   if (st != HYB_OK || B == 0) return st;
   unsigned* sw = status_word();
   if (!sw) return HYB_ERR_CUDA;

@@ -137,14 +137,24 @@ struct State16<__half> {
   }
 };
 
-// Same decomposition as linear_step_kernel; each thread's 4 state columns are one 8-byte
-// load and store.
+// 16-bit state: each thread takes 8 state columns, one 16-byte load and store per row, so
+// a thread keeps as many bytes in flight as the fp32 step does with its 4 columns.
+template <int D>
+struct StepShape16 {
+  static constexpr int COLS = D < 64 ? D : 64;              // state columns per CTA
+  static constexpr int TPR = COLS / 8;                      // threads per row (8 columns each)
+  static constexpr int THREADS = D * TPR < 256 ? D * TPR : 256;
+  static constexpr int RPP = THREADS / TPR;                 // rows per pass
+  static constexpr int PASSES = D / RPP;
+  static_assert(PASSES * RPP == D && TPR >= 1, "shape");
+};
+
 template <typename T, typename S16, int D>
-__global__ void __launch_bounds__(StepShape<D>::THREADS)
+__global__ void __launch_bounds__(StepShape16<D>::THREADS)
 linear_step_lowp_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __restrict__ k,
                         const T* __restrict__ v, uint16_t* __restrict__ pool, int NS,
                         const int32_t* __restrict__ slots, int H, unsigned* status) {
-  using Sh = StepShape<D>;
+  using Sh = StepShape16<D>;
   using Q = State16<S16>;
   constexpr int COLS = Sh::COLS, TPR = Sh::TPR, RPP = Sh::RPP, PASSES = Sh::PASSES;
   __shared__ float red[RPP][COLS];
@@ -156,41 +166,45 @@ linear_step_lowp_kernel(T* __restrict__ out, const T* __restrict__ q, const T* _
     return;
   }
   const int tc = threadIdx.x % TPR, rg = threadIdx.x / TPR;
-  const int col = cb * COLS + tc * 4;
+  const int col = cb * COLS + tc * 8;
   const int64_t rowq = ((int64_t)b * H + h) * D;
   uint16_t* S = pool + ((int64_t)slot * H + h) * D * D;
 
-  uint2 st[PASSES];
+  uint4 st[PASSES];
 #pragma unroll
   for (int p = 0; p < PASSES; ++p)
-    st[p] = __ldcs(reinterpret_cast<const uint2*>(S + (int64_t)(rg + p * RPP) * D + col));
-  const float v0 = ldf(v + rowq + col), v1 = ldf(v + rowq + col + 1);
-  const float v2 = ldf(v + rowq + col + 2), v3 = ldf(v + rowq + col + 3);
+    st[p] = __ldcs(reinterpret_cast<const uint4*>(S + (int64_t)(rg + p * RPP) * D + col));
+  float vv[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) vv[e] = ldf(v + rowq + col + e);
 
-  float o0 = 0.f, o1 = 0.f, o2 = 0.f, o3 = 0.f;
+  float o[8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) o[e] = 0.f;
 #pragma unroll
   for (int p = 0; p < PASSES; ++p) {
     const int i = rg + p * RPP;
     const float ki = ldf(k + rowq + i), qi = ldf(q + rowq + i);
-    uint2 w;
-    w.x = Q::pack(fmaf(ki, v0, Q::get(st[p].x, 0)), fmaf(ki, v1, Q::get(st[p].x, 1)));
-    w.y = Q::pack(fmaf(ki, v2, Q::get(st[p].y, 0)), fmaf(ki, v3, Q::get(st[p].y, 1)));
-    __stcs(reinterpret_cast<uint2*>(S + (int64_t)i * D + col), w);
-    o0 = fmaf(qi, Q::get(w.x, 0), o0);               // the output reads the rounded state
-    o1 = fmaf(qi, Q::get(w.x, 1), o1);
-    o2 = fmaf(qi, Q::get(w.y, 0), o2);
-    o3 = fmaf(qi, Q::get(w.y, 1), o3);
+    const uint32_t in[4] = {st[p].x, st[p].y, st[p].z, st[p].w};
+    uint32_t w[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c)
+      w[c] = Q::pack(fmaf(ki, vv[2 * c], Q::get(in[c], 0)), fmaf(ki, vv[2 * c + 1], Q::get(in[c], 1)));
+    __stcs(reinterpret_cast<uint4*>(S + (int64_t)i * D + col), make_uint4(w[0], w[1], w[2], w[3]));
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {                    // the output reads the rounded state
+      o[2 * c] = fmaf(qi, Q::get(w[c], 0), o[2 * c]);
+      o[2 * c + 1] = fmaf(qi, Q::get(w[c], 1), o[2 * c + 1]);
+    }
   }
-  red[rg][tc * 4 + 0] = o0;
-  red[rg][tc * 4 + 1] = o1;
-  red[rg][tc * 4 + 2] = o2;
-  red[rg][tc * 4 + 3] = o3;
+#pragma unroll
+  for (int e = 0; e < 8; ++e) red[rg][tc * 8 + e] = o[e];
   __syncthreads();
   for (int j = threadIdx.x; j < COLS; j += Sh::THREADS) {
-    float o = 0.f;
+    float acc = 0.f;
 #pragma unroll 8
-    for (int g = 0; g < RPP; ++g) o += red[g][j];
-    stf(out + rowq + cb * COLS + j, o);
+    for (int g = 0; g < RPP; ++g) acc += red[g][j];
+    stf(out + rowq + cb * COLS + j, acc);
   }
 }
 
@@ -260,7 +274,7 @@ template <typename T, typename S16, int D>
 cudaError_t step_lowp_typed(void* out, const void* q, const void* k, const void* v, void* pool,
                             int NS, const int32_t* slots, int B, int H, unsigned* status,
                             cudaStream_t s) {
-  using Sh = StepShape<D>;
+  using Sh = StepShape16<D>;
   dim3 grid(D / Sh::COLS, H, B);
   linear_step_lowp_kernel<T, S16, D><<<grid, Sh::THREADS, 0, s>>>(
       (T*)out, (const T*)q, (const T*)k, (const T*)v, static_cast<uint16_t*>(pool), NS, slots, H,

@@ -175,8 +175,9 @@ def test_lowp_state_step_arguments(hyb):
     # state dtype must be bf16 or fp16
     for bad in (hyb.HYB_F32, 7):
         assert hyb.hyb_linear_attn_step_lowp(f, f, f, f, f, bad, 4, f, 2, 4, 128, hyb.HYB_BF16, 0) == hyb.HYB_ERR_INVALID_ARG
-    # a 16-bit pool needs 8-byte alignment (4-element rows), not 16
+    # a 16-bit pool is read in 16-byte pieces (8 columns): 16-byte alignment
     assert hyb.hyb_linear_attn_step_lowp(f, f, f, f, f + 4, hyb.HYB_F16, 4, f, 2, 4, 128, hyb.HYB_BF16, 0) == hyb.HYB_ERR_INVALID_ARG
+    assert hyb.hyb_linear_attn_step_lowp(f, f, f, f, f + 8, hyb.HYB_F16, 4, f, 2, 4, 128, hyb.HYB_BF16, 0) == hyb.HYB_ERR_INVALID_ARG
     # no slots, unsupported head dim
     assert hyb.hyb_linear_attn_step_lowp(f, f, f, f, f, hyb.HYB_BF16, 0, f, 2, 4, 128, hyb.HYB_BF16, 0) == hyb.HYB_ERR_INVALID_ARG
     assert hyb.hyb_linear_attn_step_lowp(f, f, f, f, f, hyb.HYB_BF16, 4, f, 2, 4, 48, hyb.HYB_BF16, 0) == hyb.HYB_ERR_UNSUPPORTED
