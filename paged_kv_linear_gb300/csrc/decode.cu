@@ -425,20 +425,30 @@ decode_combine_kernel(T* __restrict__ out, const int32_t* __restrict__ seq_lens,
     } else if (nsplit <= 16) {
       combine_few<16, D>(ml, acc, nsplit, t, L, A);
     } else {
+      // long rows: 32 splits' loads in flight per round (the sums keep split order)
+      constexpr int kR = 32;
       float M = -INFINITY;
-      for (int s = 0; s < nsplit; ++s) M = fmaxf(M, ml[s].x);
-      if (M != -INFINITY) {
-        int s = 0;
-        for (; s + 8 <= nsplit; s += 8) {
-          float2 v[8];
-          float a[8];
+      int s = 0;
+      for (; s + kR <= nsplit; s += kR) {
+        float m[kR];
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < kR; ++u) m[u] = ml[s + u].x;
+#pragma unroll
+        for (int u = 0; u < kR; ++u) M = fmaxf(M, m[u]);
+      }
+      for (; s < nsplit; ++s) M = fmaxf(M, ml[s].x);
+      if (M != -INFINITY) {
+        s = 0;
+        for (; s + kR <= nsplit; s += kR) {
+          float2 v[kR];
+          float a[kR];
+#pragma unroll
+          for (int u = 0; u < kR; ++u) {
             v[u] = ml[s + u];
             a[u] = acc[(int64_t)(s + u) * D + t];
           }
 #pragma unroll
-          for (int u = 0; u < 8; ++u) {
+          for (int u = 0; u < kR; ++u) {
             const float sc = fast_exp2(v[u].x - M);
             L = fmaf(v[u].y, sc, L);
             A = fmaf(a[u], sc, A);
