@@ -7,9 +7,7 @@
 #include <cstdio>
 #include <cstdlib>
 #include <mutex>
-#include <map>
 #include <set>
-#include <tuple>
 #include <utility>
 #include <vector>
 
@@ -91,20 +89,6 @@ cudaError_t set_smem(const void* fn, int bytes) {
   cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess) g_smem_done.insert({fn, d});
   return e;
-}
-
-int max_ctas_per_sm(const void* fn, int threads, int smem) {
-  const int d = cur_dev();
-  if (d < 0) return 1;
-  static std::map<std::tuple<const void*, int, int, int>, int> cache;
-  std::lock_guard<std::mutex> lk(g_mu);
-  const auto key = std::make_tuple(fn, d, threads, smem);
-  auto it = cache.find(key);
-  if (it != cache.end()) return it->second;
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, threads, smem) != cudaSuccess || n < 1) n = 1;
-  cache[key] = n;
-  return n;
 }
 
 // Address of this device's status word (looked up once per device, with it current).

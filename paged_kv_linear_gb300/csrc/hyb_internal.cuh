@@ -20,7 +20,6 @@ void count_launch();                       // per-thread launch counter (hyb_lau
 unsigned* status_word();                   // this device's status word (nullptr on error)
 int num_sms();                             // SMs of the current device (cached)
 cudaError_t set_smem(const void* fn, int bytes);   // opt-in dynamic shared memory, once
-int max_ctas_per_sm(const void* fn, int threads, int smem);   // resident CTAs per SM (cached)
 // HYB_OK for cudaSuccess; otherwise records e for hyb_last_cuda_error and returns HYB_ERR_CUDA
 hyb_status_t cuda_status(cudaError_t e);
 // argument checks shared by the entry points (no CUDA call, no launch)
