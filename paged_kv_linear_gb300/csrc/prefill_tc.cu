@@ -6,23 +6,30 @@
 // read through the per-request block table (§2.1) so a cached prefix is attended as well.
 //
 // GB300 design. One CTA per (pair of 128-query tiles, head, request); heavy (late) pairs
-// are scheduled first. Warp roles: two TMA warps (K ring, V ring), one MMA warp and two
-// softmax warpgroups, one per query tile, one thread per query row (the row's max and sum
-// stay in that thread). K and V come straight from the paged pool: each 128-key tile is
-// eight 16-token blocks, each fetched with two TMA boxes (16 rows x 64 columns, SW128) at
-// the row the block table names (a block of bs tokens is bs / 16 such 16-row pieces); each
-// TMA warp reads the block ids 32 pieces at a time and shares the rows with shuffles. Per key tile j and query tile t:
+// are scheduled first. Warp roles: two TMA warps (K ring, V ring), one MMA-issuing thread, a
+// landing warp and two softmax warpgroups, one per query tile, one thread per query row (the
+// row's max and sum stay in that thread). K and V come straight from the paged pool: each
+// 128-key tile is eight 16-token blocks, each fetched with two TMA boxes (16 rows x 64
+// columns, SW128) at the row the block table names (a block of bs tokens is bs / 16 such
+// 16-row pieces); each TMA warp reads the block ids 32 pieces at a time and shares the rows
+// with shuffles. Per key tile j and query tile t:
 //   S_t = Q_t K_j^T   128 x 128 x 128  A = Q_t (K-major), B = K_j (K-major)  -> TMEM
 //   O_t += P_t V_j    128 x 128 x 128  A = P_t (TMEM),    B = V_j (MN-major) -> TMEM
 // TMEM holds S_0 | S_1 | O_0 | O_1 (4 x 128 columns). The softmax threads read S_t, write
 // bf16 P_t into the first 64 columns of the same S_t region, and P V reads it from there:
-// P never touches shared memory. The MMA warp issues, per key tile,
+// P never touches shared memory. The MMA thread issues, per key tile,
 //   P_0 V_j, Q_0 K_{j+1}^T, P_1 V_j, Q_1 K_{j+1}^T
 // so the tensor core works on one query tile while the other tile's softmax runs; the
 // tensor pipe executes in issue order, so Q_t K_{j+1}^T overwrites P_t only after P_t V_j
 // has read it, and its completion (the "S full" barrier) also tells the softmax threads
 // that O_t is up to date. O stays in TMEM; a row is rescaled only when its running max
 // grows by more than 2^8 (exponents stay <= 2^8, exact after the final division).
+//
+// tcgen05.mma returns only once the tensor pipe has taken the instruction (the issuing
+// thread runs an MMA or two ahead of the pipe), so any wait or commit on that thread between
+// two groups of MMAs idles the pipe for its whole latency (measured ~50-120 cycles each).
+// The MMA thread therefore does nothing per key step but wait for P_t and commit S_t; the
+// ring bookkeeping (data landed, slots free) runs on the landing warp (see Bars).
 //
 // Sliding window (window > 0, a query at position i sees keys i - window < p <= i): each
 // query tile walks the key tiles from the one holding its first query's window start;
@@ -47,7 +54,8 @@ constexpr int kOffV = kOffK + kNK * kTile;
 constexpr int kOffBar = kOffV + kNV * kTile;
 constexpr int kSmem = kOffBar + 1024 + 1024;  // barriers + 1 KiB alignment slack
 constexpr int kNSW = 8;                      // softmax warps: 4 per query tile
-constexpr int kWarpTmaK = kNSW, kWarpTmaV = kNSW + 1, kWarpMma = kNSW + 2;   // + 1 idle warp
+constexpr int kWarpTmaK = kNSW, kWarpTmaV = kNSW + 1, kWarpMma = kNSW + 2, kWarpLand = kNSW + 3;
+constexpr int kNSF = 4;                      // "step done" ring (see Bars)
 constexpr int kThreads = (kNSW + 4) * 32;    // three full warpgroups
 // Register split (setmaxnreg): the launch gives 384 threads x 168 registers (three warps
 // per SM sub-partition). The producer warpgroup drops to 104 and the two softmax warpgroups
@@ -62,8 +70,18 @@ constexpr int kTailGroups = 16;              // (request, head) groups scheduled
 constexpr uint32_t kIdescQK = idesc_bf16(128, 128, 0, 0);
 constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 0, 1);   // A = P from TMEM
 
+// The MMA-issuing thread does nothing per key step but wait for P_t (pfull) and commit S_t
+// (sfull): tcgen05.mma blocks until the tensor pipe takes it, so every other wait or commit
+// on that thread idles the pipe. The ring bookkeeping is done by other warps:
+//  - the landing warp waits for V_j and K_{j+1} to land (and zeroes V rows a partially
+//    valid last piece leaves stale) before it adds its arrival to pfull[t] for key tile j;
+//  - a ring slot is free once the key step that read it is done. The step before key tile j
+//    is done when its last MMA, Q_t K_j^T of the last query tile t reading key tile j,
+//    completes (the commit on sfull[t] covers every earlier MMA); the landing warp waits for
+//    that S (the softmax needs it before P_j anyway) and arrives on stepf[(j - jA) % kNSF].
+//    Four slots: a producer waiting for a step can never see its slot two phases on.
 struct Bars {
-  uint64_t qfull, kfull[kNK], kempty[kNK], vfull[kNV], vempty[kNV];
+  uint64_t qfull, kfull[kNK], vfull[kNV], stepf[kNSF];
   uint64_t sfull[2], pfull[2], odone[2], drain;    // per query tile
 };
 
@@ -91,6 +109,14 @@ __device__ __forceinline__ float max3f(float a, float b, float c) {
   float d;
   asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
   return d;
+}
+
+// Whole warp: rows [r0, r1) of a [128 keys][128] bf16 V tile (two SW128 sub-tiles) := 0.
+__device__ __forceinline__ void zero_v_rows(uint8_t* tile, int r0, int r1, int lane) {
+  for (int e = lane; e < (r1 - r0) * 16; e += 32) {
+    const int r = r0 + e / 16, sb = (e >> 3) & 1, ch = e & 7;
+    *reinterpret_cast<uint4*>(tile + sb * kSubQ + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
+  }
 }
 
 // Key-tile range [lo, hi) of one query tile and its key bound.
@@ -157,11 +183,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
   if (warp == kWarpMma) {
     if (lane == 0) {
       mbar_init(&bars->qfull, 1);
-      for (int i = 0; i < kNK; ++i) { mbar_init(&bars->kfull[i], 1); mbar_init(&bars->kempty[i], 1); }
-      for (int i = 0; i < kNV; ++i) { mbar_init(&bars->vfull[i], 1); mbar_init(&bars->vempty[i], 1); }
+      for (int i = 0; i < kNK; ++i) mbar_init(&bars->kfull[i], 1);
+      for (int i = 0; i < kNV; ++i) mbar_init(&bars->vfull[i], 1);
+      for (int i = 0; i < kNSF; ++i) mbar_init(&bars->stepf[i], 1);
       for (int t = 0; t < 2; ++t) {
         mbar_init(&bars->sfull[t], 1);
-        mbar_init(&bars->pfull[t], 128);
+        mbar_init(&bars->pfull[t], 128 + 1);          // softmax threads + landing warp
         mbar_init(&bars->odone[t], 1);
       }
       mbar_init(&bars->drain, 1);
@@ -186,7 +213,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
       const int depth = isk ? kNK : kNV;
       uint8_t* const ring = sm + (isk ? kOffK : kOffV);
       uint64_t* const fullb = isk ? bars->kfull : bars->vfull;
-      uint64_t* const emptyb = isk ? bars->kempty : bars->vempty;
       bool ok = true;
       int issued = 0;
       if (lane == 0) {
@@ -220,9 +246,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
           nbox += blk[bi] >= 0 ? 2 : 0;
         }
         const int slot = jj % depth;
-        if (jj >= depth) {
-          ok = __all_sync(0xffffffffu, mbar_wait(&emptyb[slot], ((jj - depth) / depth) & 1));
+        if (jj >= depth) {                               // slot free: step jj - 3 done
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->stepf[(jj - 2) % kNSF], ((jj - 2) / kNSF) & 1));
           if (!ok) break;
+        }
+        // V rows that hold no key of this call must be finite (P is 0 there, but 0 x NaN is
+        // NaN): the pieces that are not loaded are zeroed here, before the loads; the rows
+        // past kv_end inside a partially valid last piece by the landing warp.
+        const int kb = (jA + jj) * kBN;
+        const int vhead = jj == 0 ? blk_lo * 16 - kb : 0;
+        const int vtail16 = min(kBN, (kv_end - kb + 15) & ~15);
+        if (!isk && (vhead > 0 || vtail16 < kBN)) {
+          zero_v_rows(ring + slot * kTile, 0, vhead, lane);
+          zero_v_rows(ring + slot * kTile, vtail16, kBN, lane);
+          fence_async_smem();
+          __syncwarp();
         }
         if (lane == 0) {
           uint8_t* dst = ring + slot * kTile;
@@ -242,96 +280,102 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
         for (int j = max(0, issued - depth); j < issued; ++j)
           mbar_wait(&fullb[j % depth], (j / depth) & 1, 100000000ull);
       }
-    } else if (warp == kWarpMma) {
-      // ------------------------------------------------------------ MMA warp
+    } else if (warp == kWarpLand) {
+      // ------------------------------------------------------------ landing warp
+      // Per key tile j: (1) the step before it is done -> stepf; (2) once V_j and K_{j+1} have
+      // landed, one arrival on pfull[t] per query tile t that reads V_j (the MMA thread waits
+      // for P_t anyway). It gates pfull, so it is never two phases behind on any barrier.
+      // every phase of each barrier is observed in order (K_0 too), so a parity wait never
+      // mistakes a phase two on for the one it waits for
+      const int lo0 = tr[0].lo, hi0 = tr[0].hi, lo1 = tr[1].lo, hi1 = tr[1].hi;
+      bool ok = __all_sync(0xffffffffu, mbar_wait(&bars->kfull[0], 0));
+      for (int jj = 0; jj < nloc && ok; ++jj) {
+        const int j = jA + jj;
+        // the last query tile reading key tile j (tile 1 unless its range misses j); its
+        // S_j is number j - lo of that tile
+        const bool b = j >= lo1 && j < hi1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->sfull[b ? 1 : 0], (j - (b ? lo1 : lo0)) & 1));
+        if (!ok) break;
+        if (lane == 0) mbar_arrive(&bars->stepf[jj % kNSF]);
+        ok = __all_sync(0xffffffffu, mbar_wait(&bars->vfull[jj % kNV], (jj / kNV) & 1));
+        if (!ok) break;
+        const int vtail = kv_end - j * kBN;
+        if (vtail < kBN && (vtail & 15) != 0) {          // rows past kv_end in the last piece
+          zero_v_rows(sm + kOffV + (jj % kNV) * kTile, vtail, min(kBN, (vtail + 15) & ~15), lane);
+          fence_async_smem();
+          __syncwarp();
+        }
+        if (jj + 1 < nloc) {
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->kfull[(jj + 1) % kNK], ((jj + 1) / kNK) & 1));
+          if (!ok) break;
+        }
+        if (lane == 0) {
+          if (j >= lo0 && j < hi0) mbar_arrive(&bars->pfull[0]);
+          if (j >= lo1 && j < hi1) mbar_arrive(&bars->pfull[1]);
+        }
+        __syncwarp();
+      }
+      if (!ok && lane == 0) flag(status, HYB_DEVERR_TIMEOUT);
+    } else if (warp == kWarpMma && lane == 0) {
+      // ------------------------------------------------------------ MMA issue (one thread)
+      // Per key tile j: wait for P_0 (which also means V_j and K_{j+1} have landed), P_0 V_j,
+      // Q_0 K_{j+1}^T + commit; the same for tile 1. Nothing else: every extra instruction on
+      // this thread between two MMA groups leaves the tensor pipe idle.
       bool ok = true;
-      // descriptors built once; every MMA below adds a compile-time or per-tile offset
       const uint64_t qdesc = sw128_desc(smem_u32(q_s), 16, 1024);
       const uint64_t kdesc = sw128_desc(smem_u32(sm + kOffK), 16, 1024);
       const uint64_t vdesc = sw128_desc(smem_u32(sm + kOffV), kSubQ, 1024);
-      auto active = [&](int t, int j) { return j >= tr[t].lo && j < tr[t].hi; };
+      const int lo0 = tr[0].lo, hi0 = tr[0].hi, lo1 = tr[1].lo, hi1 = tr[1].hi;
       auto issue_qk = [&](int t, int ks) {               // S_t = Q_t K^T, K from ring slot ks
-        if (lane == 0) {
-          tc_fence_after();
-          const uint64_t qd = desc_add(qdesc, t * kTile);
-          const uint64_t kd = desc_add(kdesc, ks * kTile);
+        tc_fence_after();
+        const uint64_t qd = desc_add(qdesc, t * kTile);
+        const uint64_t kd = desc_add(kdesc, ks * kTile);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            const uint32_t off = (k >> 2) * kSubQ + (k & 3) * 32;
-            tc_mma(tmem + t * 128, desc_add(qd, off), desc_add(kd, off), kIdescQK, k > 0);
-          }
-          tc_commit(&bars->sfull[t]);
+        for (int k = 0; k < 8; ++k) {
+          const uint32_t off = (k >> 2) * kSubQ + (k & 3) * 32;
+          tc_mma(tmem + t * 128, desc_add(qd, off), desc_add(kd, off), kIdescQK, k > 0);
         }
-        __syncwarp();
+        tc_commit(&bars->sfull[t]);
       };
-      int npv[2] = {0, 0};                               // P V products issued per query tile
-      ok = __all_sync(0xffffffffu, mbar_wait(&bars->qfull, 0));
-      if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bars->kfull[0], 0));
+      auto issue_pv = [&](int t, int vs, bool first) {   // O_t += P_t V_j
+        tc_fence_after();
+        const uint64_t vd = desc_add(vdesc, vs * kTile);
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+          tc_mma_ta(tmem + kColO + t * 128, tmem + t * 128 + k * 8, desc_add(vd, k * 2048), kIdescPV,
+                    (!first || k > 0) ? 1u : 0u);
+      };
+      ok = mbar_wait(&bars->qfull, 0) && mbar_wait(&bars->kfull[0], 0);
       if (ok) {
-        for (int t = 0; t < 2; ++t)
-          if (active(t, jA)) issue_qk(t, 0);
-        if (lane == 0) tc_commit(&bars->kempty[0]);
-        __syncwarp();
+        if (lo0 <= jA && jA < hi0) issue_qk(0, 0);
+        if (lo1 <= jA && jA < hi1) issue_qk(1, 0);
       }
+      int npv0 = 0, npv1 = 0;                            // P V products issued per query tile
       for (int jj = 0; jj < nloc && ok; ++jj) {
         const int j = jA + jj, vs = jj % kNV, ks1 = (jj + 1) % kNK;
-        ok = __all_sync(0xffffffffu, mbar_wait(&bars->vfull[vs], (jj / kNV) & 1));
-        if (!ok) break;
-        uint8_t* v_s = sm + kOffV + vs * kTile;
-        // V rows that were not loaded := 0 (P is 0 there, but stale shared memory may hold
-        // NaN): rows past kv_end in the last tile, rows before the window's first block
-        const int kb = j * kBN;
-        const int head = jj == 0 ? blk_lo * 16 - kb : 0;
-        const int tail = kv_end - kb;
-        if (head > 0 || tail < kBN) {
-          auto zero_rows = [&](int r0, int r1) {
-            for (int e = lane; e < (r1 - r0) * 16; e += 32) {
-              const int r = r0 + e / 16, sb = (e >> 3) & 1, ch = e & 7;
-              *reinterpret_cast<uint4*>(v_s + sb * kSubQ + r * 128 + ch * 16) = make_uint4(0, 0, 0, 0);
-            }
-          };
-          if (head > 0) zero_rows(0, head);
-          if (tail < kBN) zero_rows(tail, kBN);
-          fence_async_smem();
+        const bool now0 = lo0 <= j && j < hi0, next0 = lo0 <= j + 1 && j + 1 < hi0;
+        const bool now1 = lo1 <= j && j < hi1, next1 = lo1 <= j + 1 && j + 1 < hi1;
+        if (now0) {
+          ok = mbar_wait(&bars->pfull[0], npv0 & 1);
+          if (!ok) break;
+          issue_pv(0, vs, npv0 == 0);
+          ++npv0;
         }
-        __syncwarp();
-        bool kready = false;
-        for (int t = 0; t < 2 && ok; ++t) {
-          const bool now = active(t, j), next = active(t, j + 1);
-          if (now) {                                     // O_t += P_t V_j once P_t is written
-            ok = __all_sync(0xffffffffu, mbar_wait(&bars->pfull[t], npv[t] & 1));
-            if (!ok) break;
-            if (lane == 0) {
-              tc_fence_after();
-              const uint64_t vd = desc_add(vdesc, vs * kTile);
-              const uint32_t pt_col = tmem + t * 128;
-#pragma unroll
-              for (int k = 0; k < 8; ++k)
-                tc_mma_ta(tmem + kColO + t * 128, pt_col + k * 8, desc_add(vd, k * 2048), kIdescPV,
-                          (npv[t] > 0 || k > 0) ? 1u : 0u);
-            }
-            if (lane == 0 && (t == 1 || !active(1, j)))   // last reader of V_j: free its slot
-              tc_commit(&bars->vempty[vs]);               // as soon as this P V completes
-            __syncwarp();
-            ++npv[t];
-          }
-          if (next) {                                    // then S_t = Q_t K_{j+1}^T (overwrites P_t)
-            if (!kready) {
-              ok = __all_sync(0xffffffffu, mbar_wait(&bars->kfull[ks1], ((jj + 1) / kNK) & 1));
-              if (!ok) break;
-              kready = true;
-            }
-            issue_qk(t, ks1);
-          } else if (now) {
-            if (lane == 0) tc_commit(&bars->odone[t]);   // O_t complete
-            __syncwarp();
-          }
+        if (next0) issue_qk(0, ks1);                     // tile 0 is active from jA on: now0
+        else if (now0) tc_commit(&bars->odone[0]);       // O_0 complete
+        if (now1) {
+          ok = mbar_wait(&bars->pfull[1], npv1 & 1);
+          if (!ok) break;
+          issue_pv(1, vs, npv1 == 0);
+          ++npv1;
+        } else if (next1) {                              // tile 1's window starts at j + 1
+          ok = mbar_wait(&bars->kfull[ks1], ((jj + 1) / kNK) & 1);
+          if (!ok) break;
         }
-        if (!ok) break;
-        if (lane == 0 && kready) tc_commit(&bars->kempty[ks1]);
-        __syncwarp();
+        if (next1) issue_qk(1, ks1);
+        else if (now1) tc_commit(&bars->odone[1]);       // O_1 complete
       }
-      if (!ok && lane == 0) {
+      if (!ok) {
         flag(status, HYB_DEVERR_TIMEOUT);
         tc_commit(&bars->drain);
         mbar_wait(&bars->drain, 0, 100000000ull);
