@@ -246,8 +246,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
           nbox += blk[bi] >= 0 ? 2 : 0;
         }
         const int slot = jj % depth;
-        if (jj >= depth) {                               // slot free: step jj - 3 done
-          ok = __all_sync(0xffffffffu, mbar_wait(&bars->stepf[(jj - 2) % kNSF], ((jj - 2) / kNSF) & 1));
+        if (jj >= depth) {
+          // the slot held K_{jj-kNK} (read by the Q K^T of the step before key tile jj-kNK)
+          // or V_{jj-kNV} (read by the P V of its own step): free once that step is done
+          const int m = isk ? jj - kNK : jj - kNV + 1;
+          ok = __all_sync(0xffffffffu, mbar_wait(&bars->stepf[m % kNSF], (m / kNSF) & 1));
           if (!ok) break;
         }
         // V rows that hold no key of this call must be finite (P is 0 there, but 0 x NaN is
@@ -472,25 +475,37 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant_
     if (ok && my.hi > my.lo)
       ok = __all_sync(0xffffffffu, mbar_wait(&bars->odone[t], 0));
     if (ok && my.hi > my.lo) {
+      // O_t / l -> bf16. Each warp stages its 32 rows in Q_t's shared memory (free once O_t
+      // is complete: every MMA reading Q_t came before), 16-byte chunk c of row r at
+      // r * 256 + (c ^ (r & 15)) * 16, then stores two whole rows (512 contiguous bytes) per
+      // instruction instead of 32 rows 8 KiB apart.
       tc_fence_after();
-      const bool store = q0 + t * kBM + r < n;
       const float inv = l > 0.f ? 1.f / l : 0.f;
-      __nv_bfloat16* orow = out + ((int64_t)(t0 + q0 + t * kBM + r) * H + h) * kD;
+      uint8_t* const stage = q_s + t * kTile;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         float o[32];
         tmem_ld32(o_col + c * 32, o);
         tmem_ld_wait();
-        if (store) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 wv;
-            wv.x = pack_bf16(o[e] * inv, o[e + 1] * inv);
-            wv.y = pack_bf16(o[e + 2] * inv, o[e + 3] * inv);
-            wv.z = pack_bf16(o[e + 4] * inv, o[e + 5] * inv);
-            wv.w = pack_bf16(o[e + 6] * inv, o[e + 7] * inv);
-            *reinterpret_cast<uint4*>(orow + c * 32 + e) = wv;
-          }
+        for (int e = 0; e < 32; e += 8) {
+          uint4 wv;
+          wv.x = pack_bf16(o[e] * inv, o[e + 1] * inv);
+          wv.y = pack_bf16(o[e + 2] * inv, o[e + 3] * inv);
+          wv.z = pack_bf16(o[e + 4] * inv, o[e + 5] * inv);
+          wv.w = pack_bf16(o[e + 6] * inv, o[e + 7] * inv);
+          const int ch = (c * 32 + e) / 8;                 // 16-byte chunk 0..15 of the row
+          *reinterpret_cast<uint4*>(stage + r * 256 + ((ch ^ (r & 15)) << 4)) = wv;
+        }
+      }
+      __syncwarp();
+      const int rows = n - (q0 + t * kBM);                 // rows of this tile in the prompt
+#pragma unroll 4
+      for (int i = 0; i < 16; ++i) {
+        const int rr = quarter * 32 + 2 * i + (lane >> 4), ch = lane & 15;
+        if (rr < rows) {
+          const uint4 wv = *reinterpret_cast<const uint4*>(stage + rr * 256 + ((ch ^ (rr & 15)) << 4));
+          *reinterpret_cast<uint4*>(out + ((int64_t)(t0 + q0 + t * kBM + rr) * H + h) * kD + ch * 8) = wv;
         }
       }
     } else if (!ok && lane == 0) {
