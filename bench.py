@@ -51,8 +51,7 @@ def parse():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--workload", default="hybrid_32layer",
-                    choices=["hybrid_32layer", "decode_single_layer", "prefill_chunked", "long_context_decode",
-                             "sliding_window", "state_precision", "block32", "bucketing", "prefill_lengths"],
+                    choices=["hybrid_32layer", *ROWS, *EXTRA_ROWS],
                     help="hybrid_32layer is the headline; the others are timed alone (e.g. for profiling)")
     ap.add_argument("--no-rows", action="store_true", help="skip the per-row measurements of the other workloads")
     return ap.parse_args()
@@ -698,6 +697,66 @@ def row_block32(hyb, device, stream, iters, seed=0):
                              peak_source="measured bf16_tflops (burst)")}
 
 
+def row_prefill_prefix(hyb, device, stream, iters, seed=0):
+    """Chunked prefill over a cached prefix: the last 2048-token chunk of 8 x 8192-token
+    prompts, H=32, D=128. Full layer = slot mapping + KV append of the chunk + tensor-core
+    causal prefill over the 6144 cached tokens and the chunk; Linear layer = tensor-core
+    chunked prefill (interface chunk 64) continuing each chain from its carried state."""
+    import torch
+    hbm, tf, _ = measured_peaks()
+    B, H, D, P, C = 8, 32, 128, 6144, 2048
+    g = W.rng(seed + 21)
+    pool = W.block_pool(g, np.full(B, P + C, np.int32))
+    NB = pool.num_blocks
+    d = hyb.dims(H, D, NB, pool.max_blocks, W.BF16)
+    q_lens = np.full(B, C, np.int32)
+    ctx_h = np.full(B, P, np.int32)
+    cu_h = W.cu_from_lens(q_lens)
+    T = int(cu_h[-1])
+    mk = lambda s_: W.device_rows_(torch.empty((T, H, D), dtype=torch.bfloat16, device=device), s_, D)
+    q, k, v, ql, kl, vl = (mk(70 + i) for i in range(6))
+    out, lo = torch.empty_like(q), torch.empty_like(q)
+    # the pool holds the cached prefix (random rows); the append writes the chunk behind it
+    kc = W.device_rows_(torch.empty((NB, H, 16, D), dtype=torch.bfloat16, device=device), 76, D)
+    vc = W.device_rows_(torch.empty_like(kc), 77, D)
+    st = W.device_state_(torch.empty((B, H, D, D), device=device), 78, ctx_h, D)
+    bt = torch.from_numpy(pool.block_tables).to(device)
+    cu = torch.from_numpy(cu_h).to(device)
+    ctx = torch.from_numpy(ctx_h).to(device)
+    slots = torch.arange(B, dtype=torch.int32, device=device)
+    reset = torch.zeros(B, dtype=torch.uint8, device=device)
+    slot = torch.empty(T, dtype=torch.int64, device=device)
+    lws = torch.empty(hyb.hyb_linear_attn_chunked_prefill_workspace_size(), dtype=torch.uint8, device=device)
+    sh = stream.cuda_stream
+    t_slot = _time(lambda: hyb.check(hyb.hyb_slot_mapping(slot, bt, cu, ctx, B, T, d, sh)), stream, iters)
+    t_app = _time(lambda: hyb.check(hyb.hyb_paged_kv_append(k, v, slot, T, kc, vc, d, sh)), stream, iters)
+    t_pf = _time(lambda: hyb.check(hyb.hyb_paged_attn_prefill_causal(out, q, kc, vc, bt, cu, ctx, B, T, C, d, sh)),
+                 stream, iters)
+    t_lin = _time(lambda: hyb.check(hyb.hyb_linear_attn_chunked_prefill(lo, ql, kl, vl, cu, ctx, st, B, slots, reset,
+                                                                        B, T, C, H, D, 64, W.BF16, lws,
+                                                                        lws.numel(), sh)),
+                  stream, iters)
+    _check_device(hyb)
+    i = np.arange(1, C + 1, dtype=np.float64)
+    pf_flops = 4.0 * H * D * B * float((P + i).sum())                    # each new row sees P + i keys
+    lin_flops = T * H * (4.0 * 64 * D + 4.0 * D * D)
+    lin_bytes = 4 * T * H * D * 2 + 2 * B * H * D * D * 4                # q,k,v read, o written; state read + written
+    lin_gbs = lin_bytes / (t_lin * 1e-3) / 1e9
+    res = {"workload": "prefill_prefix: 8 requests, 2048-token chunk over a 6144-token cached prefix, H=32, D=128, "
+                       "interface chunk 64 (computed as 128-token chunks), Linear state carried",
+           "value": round(T * 2 / ((t_slot + t_app + t_pf + t_lin) * 1e-3), 1), "unit": "prompt tokens/s per layer",
+           "ms": {"slot_mapping": round(t_slot, 4), "kv_append": round(t_app, 4), "prefill_causal": round(t_pf, 4),
+                  "linear_chunked_prefill": round(t_lin, 4)},
+           "roofline": _roof("tensor", pf_flops / (t_pf * 1e-3) / 1e12, tf, "TFLOP/s",
+                             "prefill_tc_kernel (causal over a cached prefix, paged)", pf_flops,
+                             peak_source="measured bf16_tflops (burst)"),
+           "linear_chunked_prefill": _roof("hbm", lin_gbs, hbm, "GB/s",
+                                           "linear_prefill_tc_kernel (128-token chunks, state carried)", lin_bytes)}
+    del q, k, v, ql, kl, vl, out, lo, kc, vc, st
+    torch.cuda.empty_cache()
+    return res
+
+
 def row_bucketing(hyb, device, stream, iters, seed=0):
     """Length-bucketed batching: the 32-layer decode step of the 64-request 80%/20% mix run as
     one call in arrival order, as one call sorted by length, and as two calls (requests with
@@ -880,7 +939,7 @@ def row_state_precision(hyb, device, stream, iters, seed=0):
 
 
 ROWS = {"decode_single_layer": row_single_layer, "long_context_decode": row_long_context,
-        "prefill_chunked": row_prefill, "sliding_window": row_sliding_window,
+        "prefill_chunked": row_prefill, "prefill_prefix": row_prefill_prefix, "sliding_window": row_sliding_window,
         "state_precision": row_state_precision, "block32": row_block32, "bucketing": row_bucketing}
 EXTRA_ROWS = {"prefill_lengths": row_prefill_lengths}   # --workload only, not in the default rows
 CPU_ROWS = ("decode_single_layer", "long_context_decode", "prefill_chunked")   # rows timed beside the oracle
