@@ -311,10 +311,11 @@ size_t hyb_linear_attn_chunked_prefill_workspace_size(void);
  * layers attend to every earlier key, and d->window must be 0.
  * Every layer's arguments are checked before the first launch. Results equal the
  * per-op calls bit for bit. In decode mode the layers overlap at their boundaries: a layer
- * after the first reads its cache (or state pool), the block table, seq_lens and the slot
- * mapping before the previous layer's kernels have finished, and its q/k/v after. No kernel
- * of the dispatch writes those, so this is exact as long as no layer's out aliases another
- * layer's cache, state pool or the batch metadata (which the caller must not do anyway). workspace serves the decode calls (see A3) and must hold
+ * after the first reads its inputs (q/k/v, cache or state pool, the block table, seq_lens
+ * and the slot mapping) and does its main work before the previous layer's kernels have
+ * finished, and writes the shared workspace only after. No kernel of the dispatch writes
+ * those inputs, so this is exact as long as no layer's out aliases another layer's q/k/v,
+ * cache, state pool or the batch metadata (which the caller must not do anyway). workspace serves the decode calls (see A3) and must hold
  * hyb_paged_attn_decode_workspace_size() bytes for the largest window among the layers
  * (window 0 when any FULL layer is present). In prefill mode it serves the LINEAR layers'
  * chunked prefill instead (one after another in stream order, sharing it) and must hold

@@ -120,10 +120,10 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict_
   using S = DecodeShape<T, D>;
   constexpr int VEC = S::VEC, LPR = S::LPR, TPI = S::TPI, ITER = S::ITER, TILE = S::TILE;
 
-  // early (decode after another layer of the same dispatch): this layer's cache, block table
-  // and lengths are not written by the kernels before it, so the row's length and block ids
-  // are read and its first K/V tiles requested before waiting for the previous kernel; q and
-  // the new row (which a model computes from the previous layer) are read after the wait.
+  // early (decode after another layer of the same dispatch): no kernel before it in the
+  // dispatch writes anything this layer reads (its cache, q, the new row, block table,
+  // lengths), so it runs its whole K/V stream while the previous kernel drains and waits for
+  // that kernel only before its first write of the shared split workspace or the output.
   if (!early) pdl_wait();                  // inputs may come from the previous kernel
   // decode: grid (splits, rows, H), the split index fastest; prefill: (rows, H, 1)
   const int h = PREFILL ? blockIdx.y : blockIdx.z, split = PREFILL ? 0 : blockIdx.x;
@@ -220,7 +220,6 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict_
   // this one writes. (A kernel that is not early has already waited, so whatever an early
   // kernel launched after it reads before its own wait was complete before this launch.)
   pdl_trigger();
-  if (early) pdl_wait();
   if (app_slot >= 0 && warp == kNW - 1) {  // the append: this step's row into its slot
     const int bsz = kBlockSize << rsh;
     const int64_t blk = app_slot / bsz, off = app_slot - blk * bsz;
@@ -345,6 +344,10 @@ paged_decode_kernel(T* __restrict__ out, const T* __restrict__ q, T* __restrict_
     red_ml[2 * warp + 1] = l;
   }
   __syncthreads();
+  // Early: the previous kernel (the previous layer's split combine) may still be reading the
+  // split workspace; every write comes after it has completed, and so does this kernel's end
+  // (so the next kernel's wait covers every earlier kernel of the dispatch).
+  if (early) pdl_wait();
 
   for (int t = threadIdx.x; t < D; t += kNW * 32) {
     float M = -INFINITY;

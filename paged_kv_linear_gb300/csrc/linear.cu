@@ -62,9 +62,10 @@ linear_step_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __rest
   constexpr int COLS = Sh::COLS, TPR = Sh::TPR, RPP = Sh::RPP, PASSES = Sh::PASSES;
   __shared__ float red[RPP][COLS];
 
-  // early (a step after another layer of the same dispatch): the state pool and the slots are
-  // not written by the kernels before it, so the state is loaded before waiting for the
-  // previous kernel; q, k and v (which a model computes from the previous layer) after.
+  // early (a step after another layer of the same dispatch): no kernel before it in the
+  // dispatch writes anything this step reads or writes (its state, q, k, v, out, the slots), so
+  // it runs while the previous kernel drains and waits for that kernel only at its end (so the
+  // next kernel's wait covers every earlier kernel of the dispatch).
   if (!early) pdl_wait();
   const int cb = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int slot = slots[b];
@@ -82,7 +83,6 @@ linear_step_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __rest
   for (int p = 0; p < PASSES; ++p)
     st[p] = __ldcs(reinterpret_cast<const float4*>(S + (int64_t)(rg + p * RPP) * D + col));
   pdl_trigger();                           // the next kernel may launch (it waits for this one)
-  if (early) pdl_wait();
   const float v0 = ldf(v + rowq + col), v1 = ldf(v + rowq + col + 1);
   const float v2 = ldf(v + rowq + col + 2), v3 = ldf(v + rowq + col + 3);
 
@@ -113,6 +113,7 @@ linear_step_kernel(T* __restrict__ out, const T* __restrict__ q, const T* __rest
     for (int g = 0; g < RPP; ++g) o += red[g][j];
     stf(out + rowq + cb * COLS + j, o);
   }
+  if (early) pdl_wait();
 }
 
 // 16-bit state elements for the state-precision comparison: widen exactly, round once (RNE).
