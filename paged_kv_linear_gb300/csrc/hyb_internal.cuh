@@ -73,10 +73,11 @@ bool decode_supported(int dtype, int D);
 // at slot[r] (-1: none) inside the decode launch, and the attention sees them; equal to a
 // KV append with the same slots followed by the decode, for slot[r] = -1 or the slot of
 // position seq_lens[r] - 1.
-// early (decode mode): the previous kernel on the stream writes neither this call's cache nor
-// its block table, lengths or slot mapping (true for every decode of a dispatch after its
-// first layer); the kernel then reads those and requests its first K/V tiles before waiting
-// for the previous kernel to complete.
+// early (decode mode): no earlier kernel that may still be running writes anything this call
+// reads (its q, new row, cache, block table, lengths or slot mapping; true for every decode
+// of a dispatch after its first layer); the kernel then streams its whole K/V range before
+// waiting for the previous kernel, and waits before its first write of the split workspace
+// or the output.
 struct DecodeAppend {
   const void* k;
   const void* v;
@@ -96,7 +97,8 @@ cudaError_t launch_linear_step_lowp(void* out, const void* q, const void* k, con
                                     void* pool, int state_dtype, int NS, const int32_t* slots,
                                     int B, int H, int D, int dtype, unsigned* status,
                                     cudaStream_t s);
-// early: as for the decode (the previous kernel writes neither this pool nor the slots)
+// early: as for the decode (no earlier kernel still running writes this pool, the slots or
+// q/k/v); the step then waits for the previous kernel only at its end
 cudaError_t launch_linear_step(void* out, const void* q, const void* k, const void* v,
                                float* pool, int NS, const int32_t* slots, int B, int H, int D,
                                int dtype, unsigned* status, cudaStream_t s, bool early = false);
