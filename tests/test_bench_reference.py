@@ -22,3 +22,18 @@ def test_reference_arm_prints_one_contract_line():
     assert j["unit"] == "req-tokens/s per layer" and j["config"]["workload"].startswith("hybrid_32layer")
     assert j["cpu_baseline"]["kind"] == "oracle" and j["cpu_baseline"]["cores"] >= 1
     assert j["e2e"]["value"] == j["value"] and j["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_every_row_can_be_timed_alone():
+    """`--workload` accepts the headline and every row (the default rows and the extra ones),
+    so each can be run on its own, e.g. under a profiler."""
+    sys.path.insert(0, ROOT)
+    import bench
+    argv = sys.argv
+    try:
+        for name in ["hybrid_32layer", *bench.ROWS, *bench.EXTRA_ROWS]:
+            sys.argv = ["bench.py", "--workload", name]
+            assert bench.parse().workload == name
+    finally:
+        sys.argv = argv
+    assert set(bench.CPU_ROWS) <= set(bench.ROWS)
